@@ -1,0 +1,146 @@
+"""Planted mistakes in the oracle (CPU only): each plausible error must make at
+least one pin fail, which shows the pins constrain the oracle and do not just
+restate it."""
+import numpy as np
+import pytest
+
+import oracle
+import oracle.zerogr_oracle as Z
+import synth
+from _helpers import tiny_catalogue
+
+
+def _exhaustive_pin_holds():
+    """The brute-force pin of test_oracle_pins, as a predicate."""
+    for seed, L, V, n, dtype in [(1, 3, 4, 20, "bf16"), (4, 3, 8, 40, "f32")]:
+        sids = tiny_catalogue(L, V, n, seed)
+        m = synth.make_model(L, V, 5, dtype, seed)
+        u = synth.make_requests(2, 5, seed)
+        trie = Z.Trie(sids, L, V)
+        res = Z.decode(trie, m, u, beam=n, K=n)
+        for q in range(2):
+            bs, bsc = Z.brute_force(trie, m, u[q])
+            if not np.array_equal(res.sids[q], bs) or np.max(np.abs(res.scores[q] - bsc)) > 1e-9:
+                return False
+            if abs(np.exp(res.scores[q]).sum() - 1.0) > 1e-6:
+                return False
+    return True
+
+
+def _membership_pin_holds():
+    cfg = synth.CONFIGS["tiny"]
+    sids = synth.make_catalogue(cfg)
+    m = synth.make_model(cfg.L, cfg.V, cfg.d)
+    u = synth.make_requests(1, cfg.d)
+    trie = Z.Trie(sids, cfg.L, cfg.V)
+    res = Z.decode(trie, m, u, beam=cfg.beam, K=cfg.topk)
+    return all(trie.contains(res.sids[0, i]) for i in range(cfg.topk))
+
+
+def _tie_pin_holds():
+    m = synth.make_model(1, 6, 4)
+    m.W[0][4] = m.W[0][1]
+    sids = np.array([[1], [4], [5]], dtype=np.int32)
+    res = Z.decode(Z.Trie(sids, 1, 6), m, synth.make_requests(1, 4), beam=3, K=3)
+    order = [int(t) for t in res.sids[0, :, 0]]
+    return order.index(1) < order.index(4)
+
+
+def _normalised_pin_holds():
+    z = np.random.default_rng(3).normal(0, 3, 300)
+    return abs(np.exp(Z.filtered_log_softmax(z)).sum() - 1.0) < 1e-6
+
+
+def test_pins_hold_on_the_real_oracle():
+    assert _exhaustive_pin_holds()
+    assert _membership_pin_holds()
+    assert _tie_pin_holds()
+    assert _normalised_pin_holds()
+
+
+def test_mistake_softmax_without_normaliser(monkeypatch):
+    monkeypatch.setattr(Z, "filtered_log_softmax", lambda z: np.asarray(z) - np.max(z))
+    assert not _normalised_pin_holds()
+    assert not _exhaustive_pin_holds()
+
+
+def test_mistake_softmax_over_full_codebook(monkeypatch):
+    """Normalising over all V tokens (score-first order) instead of the legal set."""
+    real = Z.decode
+
+    def score_first(trie, model, u, beam, K, requests=None):
+        orig = Z.step_logits
+        full = {}
+
+        def logits(Wd, s, T, h):
+            full["z"] = Wd[s - 1] @ h
+            return Wd[s - 1][T] @ h
+
+        def lsm(z):
+            zf = full["z"]
+            m = zf.max()
+            return np.asarray(z) - (m + np.log(np.exp(zf - m).sum()))
+
+        monkeypatch.setattr(Z, "step_logits", logits)
+        monkeypatch.setattr(Z, "filtered_log_softmax", lsm)
+        try:
+            return real(trie, model, u, beam, K, requests)
+        finally:
+            monkeypatch.setattr(Z, "step_logits", orig)
+
+    monkeypatch.setattr(Z, "decode", score_first)
+    assert not _exhaustive_pin_holds()
+
+
+def test_mistake_wrong_weight_step(monkeypatch):
+    monkeypatch.setattr(Z, "step_logits", lambda Wd, s, T, h: Wd[s % len(Wd)][T] @ h)
+    assert not _exhaustive_pin_holds()
+
+
+def test_mistake_sign_flip(monkeypatch):
+    monkeypatch.setattr(Z, "step_logits", lambda Wd, s, T, h: -(Wd[s - 1][T] @ h))
+    assert not _exhaustive_pin_holds()
+
+
+def test_mistake_hidden_not_advanced(monkeypatch):
+    monkeypatch.setattr(Z, "advance_hidden", lambda h, Cd, s, t: h)
+    assert not _exhaustive_pin_holds()
+
+
+def test_mistake_hidden_wrong_table(monkeypatch):
+    monkeypatch.setattr(Z, "advance_hidden", lambda h, Cd, s, t: h + Cd[-s][t])
+    assert not _exhaustive_pin_holds()
+
+
+def test_mistake_tie_break_reversed(monkeypatch):
+    monkeypatch.setattr(Z, "candidate_order", lambda vals, flat: np.lexsort((-flat, -vals)))
+    assert not _tie_pin_holds()
+
+
+def test_mistake_no_filter(monkeypatch):
+    monkeypatch.setattr(Z.Trie, "children", lambda self, p: np.arange(self.V))
+    assert not _membership_pin_holds()
+
+
+def test_mistake_successor_off_by_one(monkeypatch):
+    """A serializer whose rowptr is shifted by one entry breaks the index walk."""
+    real = Z.serialize_index
+
+    def shifted(sids, L, V, force_format=-1):
+        tabs = real(sids, L, V, force_format)
+        for t in tabs:
+            t.rowptr = np.concatenate([[0], t.rowptr[:-1] + 1]).astype(np.uint32)
+        return tabs
+
+    monkeypatch.setattr(Z, "serialize_index", shifted)
+    from conftest import read_golden
+    from _helpers import golden_catalogue
+    L, V, sids = golden_catalogue(read_golden("worked_example.txt"))
+    tabs = Z.serialize_index(sids, L, V)
+    with pytest.raises(Exception):
+        row = 0
+        for s, t in enumerate([3, 5]):
+            toks = Z.table_row_tokens(tabs[s], row, V)
+            j = int(np.nonzero(toks == t)[0][0])
+            row = int(tabs[s].rowptr[row]) + j
+        assert list(Z.table_row_tokens(tabs[2], row, V)) == [1, 4]
