@@ -1,0 +1,448 @@
+#!/usr/bin/env python
+"""Constrained decode throughput (filter + score + select) on one GB300.
+
+One step = one full L-step constrained beam decode of one request batch,
+all kernels of the CUDA library (index lookup, gather-add, selective or full
+projection, masked log-softmax, cumulative add, top-K select, emit), replayed
+from a CUDA graph with inputs resident in HBM and L2 flushed (a 256 MiB
+write) before every timed step.  Default workload: the mid-sparse catalogue
+(L=3, V=2048, 1M items, d=256, fp32 weights, batch 32, beam 32, top-K 32).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl zerogr|reference]
+
+Under torchrun (N > 1) every rank decodes its own request batch against a
+replicated index (independent replicas, no collective on the data path);
+the time is the max over ranks.  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import os
+
+# the CPU oracle leg is timed on one host thread; keep numpy's BLAS single-threaded
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import hashlib
+import json
+import math
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "constrained decode requests/s (filter+score+select)"
+UNIT = "requests/s"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def workload_desc(cfg) -> str:
+    return (f"{cfg.name}: L={cfg.L}, V={cfg.V}, {cfg.n_items:,} items ({cfg.catalogue}), d={cfg.d}, "
+            f"{cfg.w_dtype} W, batch {cfg.batch}, beam {cfg.beam}, top-K {cfg.topk}")
+
+
+# ---------------------------------------------------------------- distributed helpers
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def request_seed(rank: int) -> int:
+    """Each replica decodes its own batch (weak scaling)."""
+    return 1000 + rank
+
+
+def max_over_ranks(x: float, world: int, device="cpu") -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self) -> dict:
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.count(",") >= 7]
+        os.unlink(self.f.name)
+        sm = [float(r[0]) for r in rows if r[0].strip().replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[4:8]) if "Active" in v})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- roofline accounting
+
+def selective_bytes(st: dict, cfg, s: int) -> int:
+    """Algorithmic HBM bytes of one selective-projection launch at step s
+    (1-based): index rows read, hidden-state gather-add (parent hidden and
+    C_{s-1} row per beam, or u at step 1), the hidden written for the next
+    step, each distinct legal weight row once (the per-(beam, slot) re-reads
+    are L2 hits after the first), the padded slots and chunk partials
+    written."""
+    e = 4 if cfg.w_dtype == "f32" else 2
+    n = st["live_beams"]
+    b = st["index_bytes"]
+    b += n * cfg.d * 4 * (2 if s >= 2 else 1)
+    b += n * cfg.d * 4 if (2 <= s < cfg.L) else 0
+    b += st["unique_tokens"] * cfg.d * e
+    b += st["chunks"] * (32 * 4 + 8)
+    return int(b)
+
+
+def select_bytes(st: dict, cfg, s: int) -> int:
+    """Algorithmic bytes of one select launch: every legal candidate's score
+    and the chunk partials read once, beam state in, survivors out."""
+    n = st["live_beams"]
+    b = st["legal_slots"] * 4 + st["chunks"] * 8 + n * 16
+    b += cfg.batch * cfg.beam * 16
+    return int(b)
+
+
+def full_flops(st: dict, cfg, s: int) -> int:
+    n = cfg.batch * (1 if s == 1 else cfg.beam)
+    return 2 * n * cfg.V * cfg.d
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha1()
+    csrc = os.path.join(ROOT, "generative_recommendation_constrained_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def ncu_traffic(kernel: str, cfg_name: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+    except ValueError:
+        return None
+    ent = d.get(f"{cfg_name}:{kernel}")
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"),
+                "sm_max_mhz": d.get("sm_max_mhz", 2070.0), "src": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "sm_max_mhz": 2070.0, "src": "fallback"}
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+
+def oracle_rate(cfg, sids, model, u, budget_s: float):
+    """Requests/s of the CPU oracle (as it stands, one host thread) on a
+    bounded sample: requests decoded one at a time until budget_s elapses."""
+    import oracle
+    t0 = time.perf_counter()
+    trie = oracle.Trie(sids, cfg.L, cfg.V)
+    t_trie = time.perf_counter() - t0
+    done = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.decode(trie, model, u[done % u.shape[0]: done % u.shape[0] + 1], cfg.beam, cfg.topk)
+        done += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return done / dt, done, dt, t_trie
+
+
+def run_reference(args, cfg):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    sids = synth.make_catalogue(cfg, 0)
+    model = synth.make_model(cfg.L, cfg.V, cfg.d, cfg.w_dtype, 0)
+    u = synth.make_requests(cfg.batch, cfg.d, request_seed(0))
+    import oracle
+    trie = oracle.Trie(sids, cfg.L, cfg.V)
+    per_step = max(1, min(cfg.batch, args.ref_requests))
+    for i in range(args.warmup):
+        oracle.decode(trie, model, u[:1], cfg.beam, cfg.topk)
+    times = []
+    for i in range(args.steps):
+        lo = (i * per_step) % cfg.batch
+        sel = np.arange(lo, lo + per_step) % cfg.batch
+        t0 = time.perf_counter()
+        oracle.decode(trie, model, u[sel], cfg.beam, cfg.topk)
+        times.append(time.perf_counter() - t0)
+    ms = 1000.0 * sum(times) / len(times)
+    val = per_step / (ms / 1000.0)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_desc(cfg), "global_batch": per_step,
+                   "sample": f"{per_step} requests of the batch per step"},
+        "cpu_baseline": {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{per_step} requests per step x {args.steps} steps, fp64 numpy oracle"},
+        "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU leg
+
+def run_gpu(args, cfg):
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import generative_recommendation_constrained_gb300 as zg
+    from generative_recommendation_constrained_gb300.device import Decoder, DeviceModel
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream().cuda_stream
+
+    sids = synth.make_catalogue(cfg, 0)
+    model = synth.make_model(cfg.L, cfg.V, cfg.d, cfg.w_dtype, 0)
+    u = synth.make_requests(cfg.batch, cfg.d, request_seed(rank))
+    warm_u = synth.make_requests(cfg.batch, cfg.d, 99)
+    B, beam, K = cfg.batch, cfg.beam, cfg.topk
+
+    idx = zg.zg_index_build(sids, cfg.V, stream=stream)
+    info = zg.zg_index_info_get(idx)
+    dm = DeviceModel(model, dev)
+    u_dev = torch.from_numpy(u).to(dev)
+    plan = zg.zg_tune(idx, dm.struct, torch.from_numpy(warm_u).to(dev), B, beam, K, 20, stream)
+    variants, step_ms = zg.zg_plan_describe(plan)
+    dec = Decoder(idx, plan, dm, B, beam, K, dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def capture(d):
+        d(u_dev)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                d(u_dev)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        return g
+
+    def timed(g, steps, warmup):
+        for _ in range(warmup):
+            flush.fill_(1.0)
+            g.replay()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        barrier(world)
+        torch.cuda.synchronize()
+        for a, b in ev:
+            flush.fill_(1.0)
+            a.record()
+            g.replay()
+            b.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        return [a.elapsed_time(b) for a, b in ev]
+
+    graph = capture(dec)
+    sampler = ClockSampler(local)
+    t_clock0 = time.perf_counter()
+    times = timed(graph, args.steps, max(args.warmup, 3))
+    # keep the GPU busy long enough for the clock samples (untimed replays)
+    while time.perf_counter() - t_clock0 < 1.5:
+        for _ in range(50):
+            graph.replay()
+        torch.cuda.synchronize()
+    clocks = sampler.stop()
+    zg.zg_check_device_status(stream)
+
+    ms = statistics.fmean(times)
+    ms_max = max_over_ranks(ms, world, dev)
+    value = B * world / (ms_max / 1000.0)
+
+    # unconstrained full-vocabulary decode on the same inputs (the pages' speed reference)
+    udec = Decoder(None, None, dm, B, beam, K, dev)
+    ugraph = capture(udec)
+    utimes = timed(ugraph, max(10, args.steps // 2), 3)
+    ums = max_over_ranks(statistics.fmean(utimes), world, dev)
+
+    # per-kernel times and work counts (traced decode, L2 flushed before each)
+    traces = []
+    for _ in range(max(5, min(args.steps, 30))):
+        flush.fill_(1.0)
+        traces.append(dec.trace(u_dev))
+    L = cfg.L
+    kern = []
+    for s in range(1, L + 1):
+        st = traces[-1][s - 1]
+        avg = {k: statistics.fmean(t[s - 1][k] for t in traces) for k in ("ms_gather", "ms_project", "ms_select")}
+        name_p = "k_selective" if st["variant"] == 0 else "k_full_simt"
+        kern.append((avg["ms_project"], s, name_p, st))
+        kern.append((avg["ms_select"], s, "k_select", st))
+        if avg["ms_gather"] > 0:
+            kern.append((avg["ms_gather"], s, "k_gather_add", st))
+    kern.sort(key=lambda x: -x[0])
+    peaks = load_peaks()
+    top_ms, top_s, top_name, top_st = kern[0]
+    if top_name == "k_selective":
+        alg = selective_bytes(top_st, cfg, top_s)
+        achieved = alg / (top_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    elif top_name == "k_select":
+        alg = select_bytes(top_st, cfg, top_s)
+        achieved = alg / (top_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    elif top_name == "k_full_simt":
+        alg = full_flops(top_st, cfg, top_s)
+        achieved = alg / (top_ms * 1e-3) / 1e12
+        sm_mhz = clocks.get("sm_mhz") or peaks["sm_max_mhz"]
+        # 152 SMs x 128 fp32 FMA lanes x 2 flops per clock
+        roof = {"bound": "alu", "achieved": achieved, "peak": 152 * 128 * 2 * sm_mhz * 1e6 / 1e12,
+                "unit": "TFLOP/s"}
+    else:
+        alg = top_st["live_beams"] * cfg.d * 4 * 3
+        achieved = alg / (top_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = ncu_traffic(top_name, cfg.name)
+    roof["kernel"] = f"{top_name} (step {top_s})"
+    roof["ms_per_launch"] = top_ms
+    roof["algorithmic"] = alg
+    roof["peak_src"] = peaks["src"]
+
+    # end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    n_host = zg.zg_decode_host_workspace_size(idx, plan, dm.struct, B, beam, K)
+    ws_h = torch.empty(n_host, dtype=torch.uint8, device=dev)
+    u_pin = torch.from_numpy(u).pin_memory()
+    o_sids = torch.empty((B, K, L), dtype=torch.int32).pin_memory()
+    o_sc = torch.empty((B, K), dtype=torch.float32).pin_memory()
+    for _ in range(3):
+        zg.zg_decode_host(idx, plan, dm.struct, u_pin, B, beam, K, o_sids, o_sc, ws_h, n_host, stream)
+    e2e_steps = max(10, args.steps)
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        flush.fill_(1.0)
+        torch.cuda.synchronize()
+        zg.zg_decode_host(idx, plan, dm.struct, u_pin, B, beam, K, o_sids, o_sc, ws_h, n_host, stream)
+    e2e_ms = (time.perf_counter() - t0) * 1000.0 / e2e_steps
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
+
+    launches_per_step = sum(2 if v == 0 else (2 if s == 0 else 3) for s, v in enumerate(variants))
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, done, dt, t_trie = oracle_rate(cfg, sids, model, u, args.cpu_seconds)
+        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{done} requests of the workload decoded one at a time in {dt:.1f} s "
+                         f"(trie build {t_trie:.1f} s excluded), fp64 numpy, 1 thread"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": ms_max, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": cfg.w_dtype if cfg.w_dtype != "f32" else "f32",
+            "data": "synthetic",
+            "config": {"workload": workload_desc(cfg), "global_batch": B * world, "beam": beam, "topk": K,
+                       "plan": ["full" if v else "selective" for v in variants],
+                       "tune_ms": [[round(float(x), 4) for x in r] for r in step_ms],
+                       "l2": "flushed by a 256 MiB write before every timed step",
+                       "parallelism": f"replicas x{world}: requests sharded, index replicated, no collective",
+                       "index_bytes": info["bytes"], "dense_trie_bytes": info["dense_trie_bytes"]},
+            "p10_ms": float(np.percentile(times, 10)), "p50_ms": float(np.percentile(times, 50)),
+            "p90_ms": float(np.percentile(times, 90)),
+            "e2e": {"value": B * world / (e2e_ms / 1000.0), "unit": UNIT,
+                    "h2d_bytes_per_step": B * cfg.d * 4, "d2h_bytes_per_step": B * K * L * 4 + B * K * 4,
+                    "ms_per_step": e2e_ms},
+            "gpu_launches": launches_per_step * args.steps,
+            "gpu_launches_per_step": launches_per_step,
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "clocks": clocks,
+            "unconstrained": {"ms_per_step": ums, "value": B * world / (ums / 1000.0), "unit": UNIT,
+                              "constrained_speedup": ums / ms_max},
+            "kernels": [{"kernel": n, "step": s, "ms": round(t, 5)} for t, s, n, _ in kern],
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["zerogr", "reference"], default="zerogr")
+    ap.add_argument("--workload", default="mid_sparse", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-requests", type=int, default=2)
+    args = ap.parse_args(argv)
+    cfg = synth.CONFIGS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, cfg)
+    else:
+        run_gpu(args, cfg)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,549 @@
+// Decode engine: argument checks, workspace layout, per-step kernel
+// sequence, per-step variant tuning, and the C ABI around them.
+//
+// "ZeroGR: Filtering-First Constrained Decoding for Generative
+// Recommendation" (paper-daily.com digest):
+//   "Overall flow": the online engine runs four stages per decoding step;
+//   "Why computing fewer scores is not automatically faster", last part:
+//     before serving, warm-up requests time the variants of every step and
+//     the fastest is kept until the next model update;
+//   "Is the scheme really better": the unconstrained decode scores every
+//     token at every step and serves as the speed reference.
+#include <algorithm>
+#include <cmath>
+#include <vector>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "zg_internal.h"
+
+namespace zg {
+
+namespace {
+thread_local std::string g_err;
+
+int esize(int dt) { return dt == ZG_F32 ? 4 : 2; }
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct Dims {
+  int L, V, d, w_dtype, B, beam, K;
+  bool constrained;
+  int S_full;            // padded token stride of full scores
+  int nch_sel[ZG_MAX_STEPS];
+  int S_sel[ZG_MAX_STEPS];
+};
+
+struct WsLayout {
+  size_t tok_hist, par_hist, row[2], cum[2], h[2], Z, part, trace, u_stage, o_sids, o_scores, total;
+  size_t trace_bytes;
+};
+
+WsLayout layout(const Dims& m, bool host_io) {
+  WsLayout w{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align256(off + std::max<size_t>(bytes, 1));
+    return o;
+  };
+  const size_t BW = (size_t)m.B * m.beam;
+  const size_t hist = (size_t)std::max(m.L - 1, 1) * BW * 4;
+  w.tok_hist = take(hist);
+  w.par_hist = take(hist);
+  for (int i = 0; i < 2; ++i) {
+    w.row[i] = take(BW * 4);
+    w.cum[i] = take(BW * 4);
+    w.h[i] = take(BW * m.d * 4);
+  }
+  size_t zf = 0, pf = 0;
+  for (int s = 1; s <= m.L; ++s) {
+    const size_t N = (size_t)m.B * (s == 1 ? 1 : m.beam);
+    size_t S = m.S_full;
+    if (m.constrained) {
+      S = std::max<size_t>(S, m.S_sel[s - 1]);
+      pf = std::max(pf, N * m.nch_sel[s - 1]);
+    }
+    zf = std::max(zf, N * S);
+  }
+  w.Z = take(zf * 4);
+  w.part = take(pf * 8);
+  w.trace_bytes = 32 + (size_t)((m.V + 31) / 32) * 4;  // 4 counters + token mask
+  w.trace = take(w.trace_bytes);
+  if (host_io) {
+    w.u_stage = take((size_t)m.B * m.d * 4);
+    w.o_sids = take((size_t)m.B * m.K * m.L * 4);
+    w.o_scores = take((size_t)m.B * m.K * 4);
+  }
+  w.total = off;
+  return w;
+}
+
+zg_status check_common(const zg_index* idx, const zg_model* model, int B, int beam, int K, Dims* out) {
+  if (!model) return fail(ZG_ERR_INVALID_ARG, "model is NULL");
+  const zg_model& m = *model;
+  if (m.L < 1 || m.L > ZG_MAX_STEPS) return fail(ZG_ERR_INVALID_ARG, "model.L must be in [1, 8]");
+  if (m.V < 1 || m.V > 65536) return fail(ZG_ERR_INVALID_ARG, "model.V must be in [1, 65536]");
+  if (m.w_dtype != ZG_F32 && m.w_dtype != ZG_BF16 && m.w_dtype != ZG_F16)
+    return fail(ZG_ERR_INVALID_ARG, "model.w_dtype must be ZG_F32, ZG_BF16 or ZG_F16");
+  if (m.d < 8 || m.d % 8 != 0 || m.d * esize(m.w_dtype) > 2048)
+    return fail(ZG_ERR_INVALID_ARG, "model.d must be a multiple of 8 with d * sizeof(weight) <= 2048");
+  for (int s = 0; s < m.L; ++s) {
+    if (!m.W[s]) return fail(ZG_ERR_INVALID_ARG, "model.W[s] is NULL");
+    if (reinterpret_cast<uintptr_t>(m.W[s]) % 16) return fail(ZG_ERR_INVALID_ARG, "model.W[s] not 16-byte aligned");
+    if (s < m.L - 1) {
+      if (!m.C[s]) return fail(ZG_ERR_INVALID_ARG, "model.C[s] is NULL");
+      if (reinterpret_cast<uintptr_t>(m.C[s]) % 16) return fail(ZG_ERR_INVALID_ARG, "model.C[s] not 16-byte aligned");
+    }
+  }
+  if (B < 1) return fail(ZG_ERR_INVALID_ARG, "B must be >= 1");
+  if (beam < 1 || beam > ZG_MAX_BEAM) return fail(ZG_ERR_INVALID_ARG, "beam must be in [1, 512]");
+  if (K < 1 || K > beam) return fail(ZG_ERR_INVALID_ARG, "K must be in [1, beam]");
+  if (idx) {
+    if (idx->residency != ZG_RESIDENT_DEVICE || !idx->dev)
+      return fail(ZG_ERR_INVALID_ARG, "index is host-resident; build or load it with ZG_RESIDENT_DEVICE");
+    if (idx->L != m.L || idx->V != m.V) return fail(ZG_ERR_INVALID_ARG, "index and model disagree on L or V");
+  }
+  Dims d{};
+  d.L = m.L;
+  d.V = m.V;
+  d.d = m.d;
+  d.w_dtype = m.w_dtype;
+  d.B = B;
+  d.beam = beam;
+  d.K = K;
+  d.constrained = idx != nullptr;
+  d.S_full = (m.V + kChunk - 1) / kChunk * kChunk;
+  for (int s = 1; s <= m.L; ++s) {
+    int nch = 0;
+    if (idx) {
+      const StepMeta& sm = idx->steps[s - 1];
+      nch = sm.fmt == ZG_FMT_SPARSE ? (int)((sm.max_fanout + kChunk - 1) / kChunk) : (m.V + kChunk - 1) / kChunk;
+    }
+    d.nch_sel[s - 1] = nch;
+    d.S_sel[s - 1] = nch * kChunk;
+  }
+  *out = d;
+  return ZG_OK;
+}
+
+std::mutex g_status_mu;
+uint32_t* g_status_ptr[64] = {};
+
+zg_status get_status_ptr(uint32_t** p) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(ZG_ERR_UNSUPPORTED, "device ordinal >= 64");
+  std::lock_guard<std::mutex> lk(g_status_mu);
+  if (!g_status_ptr[dev]) {
+    e = status_word(&g_status_ptr[dev]);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status word)");
+  }
+  *p = g_status_ptr[dev];
+  return ZG_OK;
+}
+
+// Everything one decode needs, resolved once.
+struct Run {
+  Dims m;
+  WsLayout w;
+  uint8_t* ws;
+  const zg_index* idx;
+  const zg_model* model;
+  const float* u;
+  int32_t* out_sids;
+  float* out_scores;
+  uint32_t* status;
+};
+
+// Events around the kernels of one step (tracing only).
+struct StepTimer {
+  cudaEvent_t ev[4];  // start, after gather-add, after projection, after select
+};
+
+StepLaunch make_launch(const Run& r, int s, int variant) {
+  const Dims& m = r.m;
+  StepLaunch a{};
+  a.s = s;
+  a.L = m.L;
+  a.V = m.V;
+  a.d = m.d;
+  a.w_dtype = m.w_dtype;
+  a.B = m.B;
+  a.beam = m.beam;
+  a.K = m.K;
+  a.Wc = (s == 1) ? 1 : m.beam;
+  a.Wp = (s <= 2) ? 1 : m.beam;
+  a.keep = (s < m.L) ? m.beam : m.K;
+  if (r.idx) a.tab = r.idx->dev_step(s);
+  const size_t BW = (size_t)m.B * m.beam;
+  auto F32 = [&](size_t off) { return reinterpret_cast<float*>(r.ws + off); };
+  auto U32 = [&](size_t off) { return reinterpret_cast<uint32_t*>(r.ws + off); };
+  auto I32 = [&](size_t off) { return reinterpret_cast<int32_t*>(r.ws + off); };
+  if (s >= 2) {
+    const int pi = (s - 1) & 1;
+    a.row_in = r.idx ? U32(r.w.row[pi]) : nullptr;
+    a.cum_in = F32(r.w.cum[pi]);
+    a.par_in = I32(r.w.par_hist) + (size_t)(s - 2) * BW;
+    a.tok_in = I32(r.w.tok_hist) + (size_t)(s - 2) * BW;
+    a.h_prev = (s == 2) ? r.u : F32(r.w.h[pi]);
+    a.C_prev = r.model->C[s - 2];
+  }
+  a.u = r.u;
+  a.W = r.model->W[s - 1];
+  const bool full = (variant == ZG_FULL) || !r.idx;
+  // hidden of this step's beams: the next step's parents (s < L) and the
+  // full projection's input; at step 1 it is u itself
+  a.h_out = (s >= 2 && (s < m.L || full)) ? F32(r.w.h[s & 1]) : nullptr;
+  a.Z = F32(r.w.Z);
+  a.row_out = r.idx ? U32(r.w.row[s & 1]) : nullptr;
+  a.cum_out = F32(r.w.cum[s & 1]);
+  a.tok_hist = I32(r.w.tok_hist);
+  a.par_hist = I32(r.w.par_hist);
+  a.out_sids = r.out_sids;
+  a.out_scores = r.out_scores;
+  a.status = r.status;
+  if (!full) {
+    const StepMeta& sm = r.idx->steps[s - 1];
+    a.mode = sm.fmt == ZG_FMT_SPARSE ? kSelSparse : kSelDense;
+    a.nch = m.nch_sel[s - 1];
+    a.S = m.S_sel[s - 1];
+    a.part = reinterpret_cast<float2*>(r.ws + r.w.part);
+  } else {
+    a.mode = !r.idx ? kUncon : (r.idx->steps[s - 1].fmt == ZG_FMT_SPARSE ? kFullSparse : kFullDense);
+    a.nch = 0;
+    a.S = m.S_full;
+    a.part = nullptr;
+  }
+  return a;
+}
+
+zg_status run_step(const Run& r, int s, int variant, cudaStream_t st, const StepTimer* tm = nullptr) {
+  const StepLaunch a = make_launch(r, s, variant);
+  cudaError_t e;
+  if (tm) cudaEventRecord(tm->ev[0], st);
+  if (a.mode == kSelSparse || a.mode == kSelDense) {
+    if (tm) cudaEventRecord(tm->ev[1], st);
+    e = launch_selective(a, st);
+    if (e != cudaSuccess) return cuda_fail(e, "selective projection launch");
+  } else {
+    const float* H = r.u;
+    if (s >= 2) {
+      e = launch_gather_add(a, a.h_out, st);
+      if (e != cudaSuccess) return cuda_fail(e, "gather-add launch");
+      H = a.h_out;
+    }
+    if (tm) cudaEventRecord(tm->ev[1], st);
+    e = launch_full_simt(a, H, st);
+    if (e != cudaSuccess) return cuda_fail(e, "full projection launch");
+  }
+  if (tm) cudaEventRecord(tm->ev[2], st);
+  e = launch_select(a, st);
+  if (e != cudaSuccess) return cuda_fail(e, "select launch");
+  if (tm) cudaEventRecord(tm->ev[3], st);
+  return ZG_OK;
+}
+
+zg_status prepare(const zg_index* idx, const zg_plan* plan, const zg_model* model, const float* u, int B, int beam,
+                  int K, int32_t* out_sids, float* out_scores, void* ws, size_t ws_bytes, bool host_io, Run* r) {
+  Dims m;
+  zg_status st = check_common(idx, model, B, beam, K, &m);
+  if (st != ZG_OK) return st;
+  if (plan && plan->L != m.L) return fail(ZG_ERR_INVALID_ARG, "plan has a different number of steps");
+  if (!u || !out_sids || !out_scores) return fail(ZG_ERR_INVALID_ARG, "u, out_sids and out_scores must not be NULL");
+  if (!host_io && reinterpret_cast<uintptr_t>(u) % 16) return fail(ZG_ERR_INVALID_ARG, "u must be 16-byte aligned");
+  if (!ws) return fail(ZG_ERR_INVALID_ARG, "workspace is NULL");
+  if (reinterpret_cast<uintptr_t>(ws) % 256) return fail(ZG_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  WsLayout w = layout(m, host_io);
+  if (ws_bytes < w.total) return fail(ZG_ERR_INVALID_ARG, "workspace too small");
+  r->m = m;
+  r->w = w;
+  r->ws = static_cast<uint8_t*>(ws);
+  r->idx = idx;
+  r->model = model;
+  r->u = u;
+  r->out_sids = out_sids;
+  r->out_scores = out_scores;
+  return get_status_ptr(&r->status);
+}
+
+zg_status decode_steps(const Run& r, const zg_plan* plan, cudaStream_t st) {
+  for (int s = 1; s <= r.m.L; ++s) {
+    const int v = !r.idx ? ZG_FULL : (plan ? plan->variant[s - 1] : ZG_SELECTIVE);
+    zg_status e = run_step(r, s, v, st);
+    if (e != ZG_OK) return e;
+  }
+  return ZG_OK;
+}
+
+}  // namespace
+
+zg_status fail(zg_status code, const std::string& msg) {
+  g_err = msg;
+  return code;
+}
+
+zg_status cuda_fail(cudaError_t e, const char* what) {
+  g_err = std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+  return e == cudaErrorMemoryAllocation ? ZG_ERR_OUT_OF_MEMORY : ZG_ERR_CUDA;
+}
+
+}  // namespace zg
+
+using namespace zg;
+
+extern "C" {
+
+const char* zg_last_error(void) { return g_err.c_str(); }
+const char* zg_version(void) { return "zerogr-gb300 0.1 (sm_103a)"; }
+
+zg_status zg_plan_force(const zg_index* idx, int32_t B, int32_t beam, const uint8_t* variant, zg_plan** out) {
+  if (!out) return fail(ZG_ERR_INVALID_ARG, "zg_plan_force: out is NULL");
+  *out = nullptr;
+  if (!idx || !variant) return fail(ZG_ERR_INVALID_ARG, "zg_plan_force: idx and variant must not be NULL");
+  for (int s = 0; s < idx->L; ++s)
+    if (variant[s] != ZG_SELECTIVE && variant[s] != ZG_FULL)
+      return fail(ZG_ERR_INVALID_ARG, "zg_plan_force: variant must be ZG_SELECTIVE or ZG_FULL");
+  auto* p = new zg_plan();
+  p->L = idx->L;
+  p->B = B;
+  p->beam = beam;
+  p->variant.assign(variant, variant + idx->L);
+  p->step_ms.assign((size_t)idx->L * 2, -1.f);
+  *out = p;
+  return ZG_OK;
+}
+
+zg_status zg_plan_describe(const zg_plan* plan, uint8_t* variant, float* step_ms) {
+  if (!plan) return fail(ZG_ERR_INVALID_ARG, "zg_plan_describe: plan is NULL");
+  if (variant) std::memcpy(variant, plan->variant.data(), plan->L);
+  if (step_ms) std::memcpy(step_ms, plan->step_ms.data(), plan->step_ms.size() * sizeof(float));
+  return ZG_OK;
+}
+
+void zg_plan_free(zg_plan* plan) { delete plan; }
+
+zg_status zg_decode_workspace_size(const zg_index* idx, const zg_plan* plan, const zg_model* model, int32_t B,
+                                   int32_t beam, int32_t K, size_t* bytes) {
+  (void)plan;
+  if (!bytes) return fail(ZG_ERR_INVALID_ARG, "bytes is NULL");
+  Dims m;
+  zg_status st = check_common(idx, model, B, beam, K, &m);
+  if (st != ZG_OK) return st;
+  *bytes = layout(m, false).total;
+  return ZG_OK;
+}
+
+zg_status zg_decode_host_workspace_size(const zg_index* idx, const zg_plan* plan, const zg_model* model, int32_t B,
+                                        int32_t beam, int32_t K, size_t* bytes) {
+  (void)plan;
+  if (!bytes) return fail(ZG_ERR_INVALID_ARG, "bytes is NULL");
+  Dims m;
+  zg_status st = check_common(idx, model, B, beam, K, &m);
+  if (st != ZG_OK) return st;
+  *bytes = layout(m, true).total;
+  return ZG_OK;
+}
+
+zg_status zg_decode(const zg_index* idx, const zg_plan* plan, const zg_model* model, const float* u, int32_t B,
+                    int32_t beam, int32_t K, int32_t* out_sids, float* out_scores, void* workspace, size_t ws_bytes,
+                    void* stream) {
+  Run r;
+  zg_status st = prepare(idx, plan, model, u, B, beam, K, out_sids, out_scores, workspace, ws_bytes, false, &r);
+  if (st != ZG_OK) return st;
+  return decode_steps(r, plan, static_cast<cudaStream_t>(stream));
+}
+
+zg_status zg_decode_host(const zg_index* idx, const zg_plan* plan, const zg_model* model, const float* u_host,
+                         int32_t B, int32_t beam, int32_t K, int32_t* out_sids_host, float* out_scores_host,
+                         void* workspace, size_t ws_bytes, void* stream) {
+  Run r;
+  zg_status st =
+      prepare(idx, plan, model, u_host, B, beam, K, out_sids_host, out_scores_host, workspace, ws_bytes, true, &r);
+  if (st != ZG_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* u_dev = reinterpret_cast<float*>(r.ws + r.w.u_stage);
+  int32_t* sids_dev = reinterpret_cast<int32_t*>(r.ws + r.w.o_sids);
+  float* sc_dev = reinterpret_cast<float*>(r.ws + r.w.o_scores);
+  cudaError_t e = cudaMemcpyAsync(u_dev, u_host, (size_t)B * r.m.d * 4, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e, "zg_decode_host: copy of u");
+  r.u = u_dev;
+  r.out_sids = sids_dev;
+  r.out_scores = sc_dev;
+  st = decode_steps(r, plan, s);
+  if (st != ZG_OK) return st;
+  e = cudaMemcpyAsync(out_sids_host, sids_dev, (size_t)B * K * r.m.L * 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(out_scores_host, sc_dev, (size_t)B * K * 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "zg_decode_host: copy back");
+  return ZG_OK;
+}
+
+zg_status zg_tune(const zg_index* idx, const zg_model* model, const float* warm_u, int32_t B, int32_t beam, int32_t K,
+                  int32_t reps, void* stream, zg_plan** out) {
+  if (!out) return fail(ZG_ERR_INVALID_ARG, "zg_tune: out is NULL");
+  *out = nullptr;
+  if (!idx) return fail(ZG_ERR_INVALID_ARG, "zg_tune: idx is NULL (the unconstrained decode has one variant)");
+  if (!warm_u) return fail(ZG_ERR_INVALID_ARG, "zg_tune: warm_u is NULL");
+  if (reps < 1) reps = 1;
+  Dims m;
+  zg_status st = check_common(idx, model, B, beam, K, &m);
+  if (st != ZG_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  WsLayout w = layout(m, true);
+  void* ws = nullptr;
+  cudaError_t e = cudaMalloc(&ws, w.total);
+  if (e != cudaSuccess) return cuda_fail(e, "zg_tune: workspace allocation");
+  cudaEvent_t ev[2] = {nullptr, nullptr};
+  auto cleanup = [&]() {
+    for (auto& x : ev)
+      if (x) cudaEventDestroy(x);
+    cudaFree(ws);
+  };
+  if ((e = cudaEventCreate(&ev[0])) != cudaSuccess || (e = cudaEventCreate(&ev[1])) != cudaSuccess) {
+    cleanup();
+    return cuda_fail(e, "zg_tune: cudaEventCreate");
+  }
+  Run r;
+  r.m = m;
+  r.w = w;
+  r.ws = static_cast<uint8_t*>(ws);
+  r.idx = idx;
+  r.model = model;
+  r.u = warm_u;
+  r.out_sids = reinterpret_cast<int32_t*>(r.ws + w.o_sids);
+  r.out_scores = reinterpret_cast<float*>(r.ws + w.o_scores);
+  if ((st = get_status_ptr(&r.status)) != ZG_OK) {
+    cleanup();
+    return st;
+  }
+  auto* plan = new zg_plan();
+  plan->L = m.L;
+  plan->B = B;
+  plan->beam = beam;
+  plan->variant.assign(m.L, ZG_SELECTIVE);
+  plan->step_ms.assign((size_t)m.L * 2, -1.f);
+  for (int step = 1; step <= m.L && st == ZG_OK; ++step) {
+    float best = INFINITY;
+    int best_v = ZG_SELECTIVE;
+    for (int v = ZG_SELECTIVE; v <= ZG_FULL && st == ZG_OK; ++v) {
+      for (int i = 0; i < 2 && st == ZG_OK; ++i) st = run_step(r, step, v, s);
+      if (st != ZG_OK) break;
+      cudaEventRecord(ev[0], s);
+      for (int i = 0; i < reps && st == ZG_OK; ++i) st = run_step(r, step, v, s);
+      cudaEventRecord(ev[1], s);
+      if ((e = cudaEventSynchronize(ev[1])) != cudaSuccess) {
+        st = cuda_fail(e, "zg_tune: timing");
+        break;
+      }
+      float ms = 0.f;
+      cudaEventElapsedTime(&ms, ev[0], ev[1]);
+      ms /= reps;
+      plan->step_ms[(size_t)(step - 1) * 2 + v] = ms;
+      if (ms < best) {
+        best = ms;
+        best_v = v;
+      }
+    }
+    if (st != ZG_OK) break;
+    plan->variant[step - 1] = (uint8_t)best_v;
+    st = run_step(r, step, best_v, s);  // advance the state with the kept variant
+  }
+  if (st == ZG_OK && (e = cudaStreamSynchronize(s)) != cudaSuccess) st = cuda_fail(e, "zg_tune: synchronise");
+  cleanup();
+  if (st != ZG_OK) {
+    delete plan;
+    return st;
+  }
+  *out = plan;
+  return ZG_OK;
+}
+
+zg_status zg_decode_trace(const zg_index* idx, const zg_plan* plan, const zg_model* model, const float* u, int32_t B,
+                          int32_t beam, int32_t K, int32_t* out_sids, float* out_scores, void* workspace,
+                          size_t ws_bytes, void* stream, zg_trace* trace) {
+  if (!trace) return fail(ZG_ERR_INVALID_ARG, "zg_decode_trace: trace is NULL");
+  Run r;
+  zg_status st = prepare(idx, plan, model, u, B, beam, K, out_sids, out_scores, workspace, ws_bytes, false, &r);
+  if (st != ZG_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  std::memset(trace, 0, sizeof(*trace));
+  trace->L = r.m.L;
+  StepTimer tm[ZG_MAX_STEPS];
+  int made = 0;
+  cudaError_t e = cudaSuccess;
+  for (int i = 0; i < r.m.L && e == cudaSuccess; ++i)
+    for (int j = 0; j < 4 && e == cudaSuccess; ++j) {
+      e = cudaEventCreate(&tm[i].ev[j]);
+      if (e == cudaSuccess) ++made;
+    }
+  auto cleanup = [&]() {
+    for (int i = 0; i < made; ++i) cudaEventDestroy(tm[i / 4].ev[i % 4]);
+  };
+  if (e != cudaSuccess) {
+    cleanup();
+    return cuda_fail(e, "zg_decode_trace: cudaEventCreate");
+  }
+  auto* cnt = reinterpret_cast<unsigned long long*>(r.ws + r.w.trace);
+  auto* mask = reinterpret_cast<uint32_t*>(r.ws + r.w.trace + 32);
+  const int words = (r.m.V + 31) / 32;
+  std::vector<uint32_t> hmask(words);
+  for (int step = 1; step <= r.m.L; ++step) {
+    const int v = !r.idx ? ZG_FULL : (plan ? plan->variant[step - 1] : ZG_SELECTIVE);
+    st = run_step(r, step, v, s, &tm[step - 1]);
+    if (st != ZG_OK) break;
+    // untimed: what this step worked on (its entering state is still intact)
+    const StepLaunch a = make_launch(r, step, v);
+    unsigned long long hc[4];
+    e = cudaMemsetAsync(r.ws + r.w.trace, 0, r.w.trace_bytes, s);
+    if (e == cudaSuccess) e = launch_trace_touch(a, cnt, mask, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(hc, cnt, 32, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(hmask.data(), mask, (size_t)words * 4, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) {
+      st = cuda_fail(e, "zg_decode_trace: counting");
+      break;
+    }
+    zg_step_trace& t = trace->step[step - 1];
+    t.variant = v;
+    t.live_beams = (int32_t)hc[0];
+    t.legal_slots = (int64_t)hc[1];
+    t.chunks = (v == ZG_SELECTIVE) ? (int64_t)hc[2] : 0;
+    t.index_bytes = (int64_t)hc[3];
+    int64_t ut = 0;
+    for (uint32_t w : hmask) ut += __builtin_popcount(w);
+    t.unique_tokens = ut;
+    float g = 0.f, p = 0.f, q = 0.f;
+    cudaEventElapsedTime(&g, tm[step - 1].ev[0], tm[step - 1].ev[1]);
+    cudaEventElapsedTime(&p, tm[step - 1].ev[1], tm[step - 1].ev[2]);
+    cudaEventElapsedTime(&q, tm[step - 1].ev[2], tm[step - 1].ev[3]);
+    t.ms_gather = g;
+    t.ms_project = p;
+    t.ms_select = q;
+    trace->ms_total += g + p + q;
+  }
+  cleanup();
+  return st;
+}
+
+zg_status zg_check_device_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "zg_check_device_status: synchronise");
+  uint32_t* p = nullptr;
+  zg_status st = get_status_ptr(&p);
+  if (st != ZG_OK) return st;
+  uint32_t v = 0;
+  e = cudaMemcpy(&v, p, 4, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "zg_check_device_status: read");
+  if (!v) return ZG_OK;
+  cudaMemset(p, 0, 4);
+  std::string msg = "device status:";
+  if (v & kStatusRow) msg += " row out of range;";
+  if (v & kStatusToken) msg += " token out of range;";
+  if (v & kStatusTimeout) msg += " tensor-core wait expired;";
+  if (v & kStatusTmem) msg += " tensor-memory allocation failed;";
+  return fail(ZG_ERR_DEVICE_STATUS, msg);
+}
+
+}  // extern "C"

@@ -1,0 +1,118 @@
+// Internal declarations of the zerogr library (host engine <-> kernels).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "../../include/zerogr.h"
+
+namespace zg {
+
+constexpr uint32_t kDeadRow = 0xFFFFFFFFu;
+constexpr int kChunk = 32;  // slots scored by one warp work item (one per lane)
+
+// Device status bits (see zg_check_device_status).
+constexpr uint32_t kStatusRow = 1u;
+constexpr uint32_t kStatusToken = 2u;
+constexpr uint32_t kStatusTimeout = 4u;
+constexpr uint32_t kStatusTmem = 8u;
+
+// Host-side metadata of one step table.
+struct StepMeta {
+  int32_t fmt = 0;
+  uint32_t rows = 0, nnz = 0, words = 0, max_fanout = 0;
+  uint64_t off_rowptr = 0, off_payload = 0;      // byte offsets in the image
+  uint64_t bytes_rowptr = 0, bytes_payload = 0;  // payload bytes without padding
+};
+
+// Device view of one step table, passed to kernels by value.
+struct DevStep {
+  const uint32_t* rowptr;
+  const uint16_t* col;     // sparse steps
+  const uint32_t* bitmap;  // dense steps
+  uint32_t rows, nnz, words, max_fanout;
+  int32_t fmt;
+};
+
+// Per-step launch description built by the engine.
+enum SelectMode : int32_t {
+  kSelSparse = 0,   // selective scores, slot j = j-th legal token
+  kSelDense = 1,    // selective scores, slot = token, illegal slots -inf
+  kFullSparse = 2,  // full scores indexed by token, legal set from col[]
+  kFullDense = 3,   // full scores indexed by token, legal set from bitmap
+  kUncon = 4        // full scores, every token legal
+};
+
+struct StepLaunch {
+  int32_t s, L, V, d, w_dtype;
+  int32_t B, Wc, Wp;    // requests; beams per request now / at the previous step
+  int32_t keep;         // survivors per request (beam, or K at the last step)
+  int32_t beam;         // beam width (stride of state arrays)
+  int32_t K;
+  DevStep tab;          // zeroed in unconstrained mode
+  int32_t mode;         // SelectMode
+  int32_t S;            // slot stride of Z (selective) or V (full)
+  int32_t nch;          // chunks per beam (selective), else 0
+  // state entering the step (NULL at s = 1: one root beam, row 0, cum 0, h = u)
+  const uint32_t* row_in;
+  const float* cum_in;
+  const int32_t* par_in;   // parent index (within the request) of each beam
+  const int32_t* tok_in;   // token chosen at step s-1
+  const float* u;          // [B][d]
+  const float* h_prev;     // [B*Wp][d] hidden of the previous step's beams (s >= 3)
+  const float* C_prev;     // C_{s-1} [V][d] (s >= 2)
+  const void* W;           // W_s [V][d]
+  float* h_out;            // [B*Wc][d] hidden of this step's beams, or NULL
+  // scores
+  float* Z;                // [B*Wc][S]
+  float2* part;            // [B*Wc][nch] (max, sum exp) per chunk, selective only
+  // outputs
+  uint32_t* row_out;       // [B*beam] (s < L)
+  float* cum_out;          // [B*beam]
+  int32_t* tok_hist;       // [L-1][B*beam] token chosen at step j (j = 1..L-1)
+  int32_t* par_hist;       // [L-1][B*beam] parent index of that beam
+  int32_t* out_sids;       // [B][K][L] (s = L)
+  float* out_scores;       // [B][K]
+  uint32_t* status;        // device status word
+};
+
+// kernels (kernels.cu)
+cudaError_t launch_selective(const StepLaunch& a, cudaStream_t st);
+cudaError_t launch_gather_add(const StepLaunch& a, float* H, cudaStream_t st);
+cudaError_t launch_full_simt(const StepLaunch& a, const float* H, cudaStream_t st);
+cudaError_t launch_select(const StepLaunch& a, cudaStream_t st);
+cudaError_t status_word(uint32_t** dev_ptr);   // per-device status word address
+// Work counts of the beams entering a step (tracing only): counters[0..3] =
+// live beams, legal slots, chunks, index bytes; mask = V-bit set of touched
+// tokens.  Both must be zeroed by the caller.
+cudaError_t launch_trace_touch(const StepLaunch& a, unsigned long long* counters, uint32_t* mask,
+                               cudaStream_t st);
+
+// error reporting (engine.cpp)
+zg_status fail(zg_status code, const std::string& msg);
+zg_status cuda_fail(cudaError_t e, const char* what);
+
+}  // namespace zg
+
+struct zg_index {
+  int32_t L = 0, V = 0, residency = 0;
+  int64_t n_input = 0, n_unique = 0;
+  std::vector<zg::StepMeta> steps;
+  uint64_t total_bytes = 0;
+  uint8_t* dev = nullptr;          // device image (residency device)
+  std::vector<uint8_t> host;       // host image (residency host)
+  int32_t device = -1;
+  double ms_sort = 0, ms_count = 0, ms_fill = 0, ms_total = 0;
+
+  zg::DevStep dev_step(int s) const;  // s is 1-based
+};
+
+struct zg_plan {
+  int32_t L = 0, B = 0, beam = 0;
+  std::vector<uint8_t> variant;  // [L]
+  std::vector<float> step_ms;    // [L][2]
+};

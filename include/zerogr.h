@@ -1,0 +1,271 @@
+/*
+ * zerogr.h - C ABI of the GB300 (sm_103a) filtering-first constrained beam
+ * decoder over semantic IDs (SIDs).
+ *
+ * Method: "ZeroGR: Filtering-First Constrained Decoding for Generative
+ * Recommendation" (paper-daily.com digest).  Section names used below:
+ *   [Problem]  "What problem does it solve"  (SID beam search, validity filter)
+ *   [Order]    "Does filtering first change the result"  (legal-only softmax)
+ *   [Pipeline] "Overall flow"  (three parts; four stages per decoding step)
+ *   [Index]    "Why slice the index by decoding step"  (step tables, dense vs
+ *              sparse, implicit successor rows)
+ *   [Speed]    "Why computing fewer scores is not automatically faster"
+ *              (padded candidate slots, in-place weight rows, per-step
+ *              full-vs-selective choice made on warm-up requests)
+ *   [Results]  "Is the scheme really better"  (unconstrained decode as the
+ *              speed reference; chunked CPU rebuild streamed through two
+ *              buffers)
+ *
+ * Conventions (every call):
+ *   - Every call returns a zg_status; nothing exits, throws or traps.  After
+ *     a non-OK status, zg_last_error() gives a message (thread-local).
+ *   - "host" pointers are CPU memory; "device" pointers are CUDA device
+ *     memory of the current device (for example torch.Tensor.data_ptr()).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).
+ *   - Inputs are read-only and stay owned by the caller.  Handles
+ *     (zg_index, zg_plan) are owned by the library and released with their
+ *     *_free call.  Indexes and plans are read-only after creation and may be
+ *     shared by concurrent decodes; a workspace may not.
+ *   - Limits: 1 <= L <= 8, 1 <= V <= 65536, L * ceil(log2 V) <= 64,
+ *     d % 8 == 0 with d * sizeof(weight) <= 2048 bytes,
+ *     1 <= K <= beam <= 512, B >= 1.  Anything outside returns
+ *     ZG_ERR_INVALID_ARG (or ZG_ERR_UNSUPPORTED for the key-width limit).
+ */
+#ifndef ZEROGR_H
+#define ZEROGR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define ZG_API __attribute__((visibility("default")))
+#else
+#define ZG_API
+#endif
+
+#define ZG_MAX_STEPS 8
+#define ZG_MAX_BEAM 512
+
+typedef enum {
+  ZG_OK = 0,
+  ZG_ERR_INVALID_ARG = 1,
+  ZG_ERR_OUT_OF_MEMORY = 2,
+  ZG_ERR_CUDA = 3,
+  ZG_ERR_UNSUPPORTED = 4,
+  ZG_ERR_TIMEOUT = 5,
+  ZG_ERR_DEVICE_STATUS = 6,
+  ZG_ERR_IO = 7
+} zg_status;
+
+typedef enum { ZG_F32 = 0, ZG_BF16 = 1, ZG_F16 = 2 } zg_dtype;
+typedef enum { ZG_FMT_SPARSE = 0, ZG_FMT_DENSE = 1 } zg_format;
+typedef enum { ZG_SELECTIVE = 0, ZG_FULL = 1 } zg_variant;
+typedef enum { ZG_RESIDENT_DEVICE = 0, ZG_RESIDENT_HOST = 1 } zg_residency;
+typedef enum { ZG_FORMAT_AUTO = 0, ZG_FORMAT_ALL_SPARSE = 1, ZG_FORMAT_ALL_DENSE = 2 } zg_format_mode;
+
+typedef struct zg_index zg_index; /* opaque: step tables + host header */
+typedef struct zg_plan zg_plan;   /* opaque: per-step variant choice   */
+
+/* The synthetic model the decoder scores with ([Pipeline] stage 1 is the
+ * model's hidden vector; here h = u + sum_{j<s} C_j[t_j]).
+ *   C[s]: device float32 [V][d], row-major, s = 0..L-2 (the table added after
+ *         choosing the token of step s+1); C[L-1] is unused and may be NULL.
+ *   W[s]: device w_dtype [V][d], row-major, s = 0..L-1 (output head of step
+ *         s+1); rows must be 16-byte aligned (d % 8 == 0 ensures it).
+ * The struct and its pointer arrays are caller-owned. */
+typedef struct {
+  int32_t L, V, d, w_dtype;
+  const float* C[ZG_MAX_STEPS];
+  const void* W[ZG_MAX_STEPS];
+} zg_model;
+
+/* Index build options.  Zero-initialised = defaults. */
+typedef struct {
+  int32_t n_threads;           /* host threads; <= 0: all hardware threads          */
+  int32_t format_mode;         /* ZG_FORMAT_AUTO (per-step rule), ZG_FORMAT_ALL_SPARSE
+                                  or ZG_FORMAT_ALL_DENSE                             */
+  int32_t reserved;
+  int32_t residency;           /* ZG_RESIDENT_DEVICE (decodable) or ZG_RESIDENT_HOST
+                                  (no CUDA use at all: stats/export/save only)       */
+  uint64_t pinned_chunk_bytes; /* size of each of the two pinned staging buffers;
+                                  0: 64 MiB.  Grown if one first-token subtree's
+                                  slice of a step is larger.                         */
+} zg_build_opts;
+
+typedef struct {
+  int32_t format;          /* ZG_FMT_SPARSE or ZG_FMT_DENSE                  */
+  uint32_t rows;           /* distinct length-(s-1) prefixes                 */
+  uint32_t nnz;            /* legal (row, token) entries = rows of step s+1  */
+  uint32_t words_per_row;  /* 32-bit words of a dense bitmap row            */
+  uint32_t max_fanout;     /* slots per beam of this step (largest row)     */
+  uint32_t reserved;
+  double mean_fanout;      /* nnz / rows                                     */
+  double legal_fraction;   /* nnz / (rows * V)                               */
+  uint64_t bytes;          /* bytes of this step's table                     */
+} zg_step_stats;
+
+typedef struct {
+  int32_t L, V, residency, reserved;
+  int64_t n_input;           /* SIDs given                                     */
+  int64_t n_unique;          /* distinct SIDs (duplicates merged)              */
+  uint64_t bytes;            /* all step tables                                */
+  uint64_t dense_trie_bytes; /* the same catalogue as a dense prefix-trie
+                                tensor, one int32 child per (row, token):
+                                sum_s rows_s * V * 4 (computed, not allocated)  */
+  double ms_sort, ms_count, ms_fill, ms_total; /* build phases, host wall time */
+} zg_index_info;
+
+/* ---------------------------------------------------------------- index ---
+ * zg_index_build - [Index], [Results] (rebuild pipeline).
+ * Builds the step-sliced index from n catalogue SIDs on host threads: pack
+ * and sort, merge duplicates, count each first-token subtree's rows and
+ * entries (pass 1), lay the subtrees out by prefix sums, then fill them in
+ * parallel into two pinned buffers in turn while the other buffer's
+ * cudaMemcpyAsync to HBM runs on `stream` (pass 2).  No kernels run.
+ *   sids: host int32 [n][L], tokens in [0, V).  Caller-owned, read only.
+ * Table layout of step s (1-based): rows are the distinct length-(s-1)
+ * prefixes in lexicographic order; uint32 rowptr[rows+1]; a row's legal
+ * tokens ascending; entry e (in (row, token) order) is row e of step s+1.
+ * Sparse steps store uint16 col[nnz]; dense steps a uint32 bitmap
+ * [rows][ceil(V/32)] (bit t%32 of word t/32).  Automatic format: dense iff
+ * 4*rows*ceil(V/32) < 2*nnz.
+ * Returns ZG_ERR_INVALID_ARG for n < 1, bad L/V or a token out of range,
+ * ZG_ERR_UNSUPPORTED if L*ceil(log2 V) > 64, ZG_ERR_OUT_OF_MEMORY /
+ * ZG_ERR_CUDA on allocation or copy failure.  Returns after the copies end. */
+ZG_API zg_status zg_index_build(const int32_t* sids, int64_t n, int32_t L, int32_t V,
+                         const zg_build_opts* opts, void* stream, zg_index** out);
+
+/* Per-step table statistics (step is 1-based). */
+ZG_API zg_status zg_index_stats(const zg_index* idx, int32_t step, zg_step_stats* out);
+ZG_API zg_status zg_index_info_get(const zg_index* idx, zg_index_info* out);
+
+/* Canonical bytes of one step's table, for bit-exact comparison: uint32
+ * {format, rows, nnz, words_per_row}, uint32 rowptr[rows+1], then uint16
+ * col[nnz] zero-padded to 4 bytes (sparse) or uint32 bitmap[rows][words]
+ * (dense), little-endian.  If buf is NULL or *bytes is too small, *bytes is
+ * set to the size needed and ZG_ERR_INVALID_ARG is returned (buf NULL:
+ * ZG_OK). */
+ZG_API zg_status zg_index_export(const zg_index* idx, int32_t step, void* buf, size_t* bytes);
+
+/* Save to / load from a file: header, step metadata, table bytes and a
+ * 64-bit FNV-1a checksum.  Load fails with ZG_ERR_IO on a short, corrupt or
+ * foreign file. */
+ZG_API zg_status zg_index_save(const zg_index* idx, const char* path);
+ZG_API zg_status zg_index_load(const char* path, int32_t residency, void* stream, zg_index** out);
+ZG_API void zg_index_free(zg_index* idx);
+
+/* ---------------------------------------------------------------- plan ----
+ * [Speed]: before serving, warm-up requests time each scoring variant at
+ * every step; the fastest is kept until the next model update.
+ *   ZG_SELECTIVE: score only legal tokens, reading their weight rows in place
+ *                 into padded slots (one slot per legal token; every beam of
+ *                 the step gets max_fanout slots, or V on dense steps).
+ *   ZG_FULL:      project every token (a dense contraction), then pick the
+ *                 legal ones.
+ * zg_tune runs the decode step by step on warm_u (device float32 [B][d]):
+ * each variant of step s runs 2 warm-up times and `reps` timed times on the
+ * same entering state (CUDA events on `stream`); the faster is kept and
+ * advances the state.  Allocates and frees its own workspace.  Synchronous. */
+ZG_API zg_status zg_tune(const zg_index* idx, const zg_model* model, const float* warm_u, int32_t B,
+                  int32_t beam, int32_t K, int32_t reps, void* stream, zg_plan** out);
+/* A plan with a fixed variant per step (variant: host uint8 [L]). */
+ZG_API zg_status zg_plan_force(const zg_index* idx, int32_t B, int32_t beam, const uint8_t* variant,
+                        zg_plan** out);
+/* variant: host uint8 [L] (may be NULL); step_ms: host float [L][2] timings
+ * of {SELECTIVE, FULL} from zg_tune (-1 when not timed; may be NULL). */
+ZG_API zg_status zg_plan_describe(const zg_plan* plan, uint8_t* variant, float* step_ms);
+ZG_API void zg_plan_free(zg_plan* plan);
+
+/* --------------------------------------------------------------- decode ---
+ * Workspace bytes zg_decode needs for (idx, plan, model, B, beam, K); idx
+ * NULL = unconstrained decode. */
+ZG_API zg_status zg_decode_workspace_size(const zg_index* idx, const zg_plan* plan,
+                                   const zg_model* model, int32_t B, int32_t beam, int32_t K,
+                                   size_t* bytes);
+
+/* zg_decode - [Pipeline] online part, all L steps.  Per step and beam:
+ * look up the legal tokens of the beam's row, form the hidden vector
+ * (gather-add), score legal tokens (plan's variant), log-softmax over the
+ * legal tokens only ([Order]), add to the cumulative score, keep the best
+ * `beam` candidates per request (best K at the last step).  Ties order by
+ * lower parent-beam rank, then lower slot (ascending token).  One root beam
+ * per request.
+ *   idx:  device-resident index, or NULL for the unconstrained decode of
+ *         [Results] (every token legal, plan ignored, SIDs need not exist).
+ *   plan: per-step variants; NULL = ZG_SELECTIVE at every step.
+ *   u:    device float32 [B][d] request vectors.
+ *   out_sids:   device int32 [B][K][L]; out_scores: device float32 [B][K],
+ *               best first; rows beyond a request's candidates are -1/-inf.
+ *   workspace:  device, >= zg_decode_workspace_size bytes, 256-byte aligned;
+ *               caller-owned scratch, contents undefined on return.
+ * Asynchronous on `stream`: only kernel launches, so it can be captured in
+ * a CUDA graph.  Launch errors are returned; device-side invariant breaches
+ * are recorded for zg_check_device_status. */
+ZG_API zg_status zg_decode(const zg_index* idx, const zg_plan* plan, const zg_model* model,
+                    const float* u, int32_t B, int32_t beam, int32_t K, int32_t* out_sids,
+                    float* out_scores, void* workspace, size_t ws_bytes, void* stream);
+
+/* zg_decode with host buffers: copies u (host float32 [B][d], pinned memory
+ * recommended) to the device, decodes, copies out_sids (host int32
+ * [B][K][L]) and out_scores (host float32 [B][K]) back, and synchronises
+ * `stream`.  The workspace must be sized with zg_decode_host_workspace_size. */
+ZG_API zg_status zg_decode_host_workspace_size(const zg_index* idx, const zg_plan* plan,
+                                        const zg_model* model, int32_t B, int32_t beam,
+                                        int32_t K, size_t* bytes);
+ZG_API zg_status zg_decode_host(const zg_index* idx, const zg_plan* plan, const zg_model* model,
+                         const float* u_host, int32_t B, int32_t beam, int32_t K,
+                         int32_t* out_sids_host, float* out_scores_host, void* workspace,
+                         size_t ws_bytes, void* stream);
+
+/* Per-step record of zg_decode_trace. */
+typedef struct {
+  int32_t variant;        /* ZG_SELECTIVE or ZG_FULL (always ZG_FULL unconstrained) */
+  int32_t live_beams;     /* beams entering the step with a finite score           */
+  int64_t legal_slots;    /* sum of legal fan-outs F_b over live beams (V each when
+                             unconstrained)                                        */
+  int64_t chunks;         /* 32-slot chunks the selective kernel scores            */
+  int64_t unique_tokens;  /* distinct legal tokens = distinct W_s rows touched     */
+  int64_t index_bytes;    /* table bytes the filter reads: rowptr pairs plus column
+                             entries (sparse) or bitmap rows (dense)               */
+  float ms_gather;        /* gather-add kernel (full steps at s >= 2), else 0       */
+  float ms_project;       /* selective or full projection kernel                   */
+  float ms_select;        /* masked log-softmax + cumulative add + top-K kernel     */
+  float reserved;
+} zg_step_trace;
+
+typedef struct {
+  int32_t L, reserved;
+  zg_step_trace step[ZG_MAX_STEPS];
+  float ms_total;         /* sum of the timed kernels                               */
+} zg_trace;
+
+/* zg_decode_trace - the zg_decode computation (same kernels, same results)
+ * run step by step with CUDA events around every kernel launch on `stream`,
+ * plus an untimed counting kernel per step that fills the work counts above
+ * (the observability the per-step variant choice of [Speed] rests on).
+ * Synchronous; not for CUDA graph capture.  The workspace is the one sized by
+ * zg_decode_workspace_size. */
+ZG_API zg_status zg_decode_trace(const zg_index* idx, const zg_plan* plan, const zg_model* model,
+                                 const float* u, int32_t B, int32_t beam, int32_t K,
+                                 int32_t* out_sids, float* out_scores, void* workspace,
+                                 size_t ws_bytes, void* stream, zg_trace* trace);
+
+/* Synchronises `stream`, then reports and clears the device status word that
+ * kernels set instead of trapping (bit 0: row out of range, bit 1: token out
+ * of range, bit 2: a bounded wait in the tensor-core kernel expired, bit 3:
+ * tensor-memory allocation failed).  Non-zero -> ZG_ERR_DEVICE_STATUS. */
+ZG_API zg_status zg_check_device_status(void* stream);
+
+ZG_API const char* zg_last_error(void);
+ZG_API const char* zg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZEROGR_H */

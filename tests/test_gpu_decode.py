@@ -1,0 +1,284 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Element-by-element on seeded inputs: index tables bit-exact; top-K SIDs and
+scores per request within the fp32 tolerance 1e-4 (2e-2 for bf16/fp16
+weights), sets equal wherever the score gap exceeds the decision window.
+"""
+import itertools
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from _helpers import check_topk, golden_catalogue, tiny_catalogue
+from conftest import read_golden
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+WINDOW = 1e-4
+
+
+@pytest.fixture(scope="module")
+def zg():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    import generative_recommendation_constrained_gb300 as zg
+    return zg
+
+
+def _stream():
+    return torch.cuda.current_stream().cuda_stream
+
+
+def decode_gpu(zg, idx, model, u, beam, K, variants=None, dm=None, plan=None):
+    from generative_recommendation_constrained_gb300.device import Decoder, DeviceModel
+    dm = dm or DeviceModel(model)
+    B = u.shape[0]
+    if plan is None and variants is not None:
+        plan = zg.zg_plan_force(idx, B, beam, variants)
+    dec = Decoder(idx, plan, dm, B, beam, K)
+    s, sc = dec(torch.from_numpy(np.ascontiguousarray(u)).cuda())
+    torch.cuda.synchronize()
+    zg.zg_check_device_status(0)
+    return s.cpu().numpy(), sc.cpu().numpy()
+
+
+def tol_for(dtype):
+    return 1e-4 if dtype == "f32" else 2e-2
+
+
+# ------------------------------------------------------------------ index
+
+@pytest.mark.parametrize("name", ["tiny", "mid_sparse"])
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_device_index_bit_exact(zg, name, mode):
+    cfg = synth.CONFIGS[name]
+    sids = synth.make_catalogue(cfg)
+    idx = zg.zg_index_build(sids, cfg.V, format_mode=mode, stream=_stream(), pinned_chunk_bytes=1 << 16)
+    fmt = -1 if mode == 0 else mode - 1
+    tabs = oracle.serialize_index(sids, cfg.L, cfg.V, force_format=fmt)
+    for s in range(1, cfg.L + 1):
+        assert zg.zg_index_export(idx, s) == tabs[s - 1].export_bytes(), f"step {s}"
+
+
+def test_device_index_save_load(zg, tmp_path):
+    sids = tiny_catalogue(3, 64, 800, 3)
+    idx = zg.zg_index_build(sids, 64, stream=_stream())
+    p = str(tmp_path / "x.zgidx")
+    zg.zg_index_save(idx, p)
+    back = zg.zg_index_load(p, zg.ZG_RESIDENT_DEVICE, _stream())
+    for s in (1, 2, 3):
+        assert zg.zg_index_export(back, s) == zg.zg_index_export(idx, s)
+
+
+# ------------------------------------------------------------------ tiny config
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("variants", list(itertools.product([0, 1], repeat=3)))
+def test_tiny_every_plan_and_format(zg, mode, variants):
+    cfg = synth.CONFIGS["tiny"]
+    sids = synth.make_catalogue(cfg)
+    model = synth.make_model(cfg.L, cfg.V, cfg.d, cfg.w_dtype)
+    u = synth.make_requests(6, cfg.d)
+    idx = zg.zg_index_build(sids, cfg.V, format_mode=mode, stream=_stream())
+    trie = oracle.Trie(sids, cfg.L, cfg.V)
+    ref = oracle.decode(trie, model, u, cfg.beam, cfg.topk)
+    s, sc = decode_gpu(zg, idx, model, u, cfg.beam, cfg.topk, list(variants))
+    amb = check_topk(s, sc, ref, trie, model, u, 1e-4, WINDOW)
+    assert amb <= 2
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("variants", [[0, 0, 0], [1, 1, 1], [1, 0, 0]])
+def test_tiny_half_weights(zg, dtype, variants):
+    cfg = synth.CONFIGS["tiny"]
+    sids = synth.make_catalogue(cfg)
+    model = synth.make_model(cfg.L, cfg.V, cfg.d, dtype, 1)
+    u = synth.make_requests(6, cfg.d, 1)
+    idx = zg.zg_index_build(sids, cfg.V, stream=_stream())
+    trie = oracle.Trie(sids, cfg.L, cfg.V)
+    ref = oracle.decode(trie, model, u, cfg.beam, cfg.topk)
+    s, sc = decode_gpu(zg, idx, model, u, cfg.beam, cfg.topk, variants)
+    check_topk(s, sc, ref, trie, model, u, tol_for(dtype), WINDOW)
+
+
+# ------------------------------------------------------------------ mid sparse (the bench workload)
+
+@pytest.fixture(scope="module")
+def mid(zg):
+    cfg = synth.CONFIGS["mid_sparse"]
+    sids = synth.make_catalogue(cfg)
+    model = synth.make_model(cfg.L, cfg.V, cfg.d, cfg.w_dtype)
+    u = synth.make_requests(cfg.batch, cfg.d)
+    trie = oracle.Trie(sids, cfg.L, cfg.V)
+    ref = oracle.decode(trie, model, u, cfg.beam, cfg.topk)
+    idx = zg.zg_index_build(sids, cfg.V, stream=_stream())
+    return cfg, sids, model, u, trie, ref, idx
+
+
+@pytest.mark.parametrize("variants", [[0, 0, 0], [1, 1, 1], [1, 0, 0], [0, 1, 1]])
+def test_mid_sparse_parity(zg, mid, variants):
+    cfg, sids, model, u, trie, ref, idx = mid
+    s, sc = decode_gpu(zg, idx, model, u, cfg.beam, cfg.topk, variants)
+    amb = check_topk(s, sc, ref, trie, model, u, 1e-4, WINDOW)
+    assert amb <= cfg.batch // 4
+
+
+def test_mid_sparse_tuned_plan(zg, mid):
+    cfg, sids, model, u, trie, ref, idx = mid
+    from generative_recommendation_constrained_gb300.device import DeviceModel
+    dm = DeviceModel(model)
+    ud = torch.from_numpy(u).cuda()
+    plan = zg.zg_tune(idx, dm.struct, ud, cfg.batch, cfg.beam, cfg.topk, 5, _stream())
+    v, ms = zg.zg_plan_describe(plan)
+    assert set(v.tolist()) <= {0, 1} and (ms > 0).all()
+    for st in range(cfg.L):
+        assert v[st] == int(np.argmin(ms[st]))
+    s, sc = decode_gpu(zg, idx, model, u, cfg.beam, cfg.topk, plan=plan, dm=dm)
+    check_topk(s, sc, ref, trie, model, u, 1e-4, WINDOW)
+
+
+def test_plans_agree_with_each_other(zg, mid):
+    """The variant choice changes speed, not results (within rounding)."""
+    cfg, sids, model, u, trie, ref, idx = mid
+    a_s, a_sc = decode_gpu(zg, idx, model, u, cfg.beam, cfg.topk, [0, 0, 0])
+    b_s, b_sc = decode_gpu(zg, idx, model, u, cfg.beam, cfg.topk, [1, 1, 1])
+    assert np.max(np.abs(np.sort(a_sc, 1) - np.sort(b_sc, 1))) < 1e-4
+    same = np.mean([set(map(tuple, a_s[q])) == set(map(tuple, b_s[q])) for q in range(cfg.batch)])
+    assert same >= 0.75
+
+
+def test_deterministic(zg, mid):
+    cfg, sids, model, u, trie, ref, idx = mid
+    a = decode_gpu(zg, idx, model, u, cfg.beam, cfg.topk, [0, 0, 0])
+    b = decode_gpu(zg, idx, model, u, cfg.beam, cfg.topk, [0, 0, 0])
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_cuda_graph_replay(zg, mid):
+    cfg, sids, model, u, trie, ref, idx = mid
+    from generative_recommendation_constrained_gb300.device import Decoder, DeviceModel
+    dm = DeviceModel(model)
+    plan = zg.zg_plan_force(idx, cfg.batch, cfg.beam, [1, 0, 0])
+    dec = Decoder(idx, plan, dm, cfg.batch, cfg.beam, cfg.topk)
+    ud = torch.from_numpy(u).cuda()
+    dec(ud)
+    torch.cuda.synchronize()
+    want = (dec.out_sids.clone(), dec.out_scores.clone())
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            dec(ud)
+    torch.cuda.current_stream().wait_stream(s)
+    dec.out_sids.zero_()
+    dec.out_scores.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(dec.out_sids, want[0]) and torch.equal(dec.out_scores, want[1])
+
+
+def test_decode_host_buffers(zg, mid):
+    cfg, sids, model, u, trie, ref, idx = mid
+    from generative_recommendation_constrained_gb300.device import DeviceModel
+    dm = DeviceModel(model)
+    plan = zg.zg_plan_force(idx, cfg.batch, cfg.beam, [1, 0, 0])
+    n = zg.zg_decode_host_workspace_size(idx, plan, dm.struct, cfg.batch, cfg.beam, cfg.topk)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    u_h = torch.from_numpy(u).pin_memory()
+    o_s = torch.empty((cfg.batch, cfg.topk, cfg.L), dtype=torch.int32).pin_memory()
+    o_sc = torch.empty((cfg.batch, cfg.topk), dtype=torch.float32).pin_memory()
+    zg.zg_decode_host(idx, plan, dm.struct, u_h, cfg.batch, cfg.beam, cfg.topk, o_s, o_sc, ws, n, _stream())
+    s, sc = decode_gpu(zg, idx, model, u, cfg.beam, cfg.topk, plan=plan, dm=dm)
+    assert np.array_equal(o_s.numpy(), s) and np.array_equal(o_sc.numpy(), sc)
+
+
+# ------------------------------------------------------------------ exhaustive / special cases
+
+@pytest.mark.parametrize("seed,L,V,n,dtype", [(0, 2, 37, 90, "f32"), (1, 3, 8, 60, "bf16"),
+                                               (2, 3, 16, 120, "f16"), (3, 1, 50, 50, "f32"),
+                                               (4, 4, 6, 200, "f32")])
+@pytest.mark.parametrize("variants", ["sel", "full"])
+def test_exhaustive_small_catalogues(zg, seed, L, V, n, dtype, variants):
+    """beam >= number of items: the decode returns every item, best first,
+    with its summed filtered log-probabilities (brute force on the CPU)."""
+    sids = tiny_catalogue(L, V, n, seed)
+    d = 16
+    model = synth.make_model(L, V, d, dtype, seed)
+    u = synth.make_requests(3, d, seed)
+    idx = zg.zg_index_build(sids, V, stream=_stream())
+    trie = oracle.Trie(sids, L, V)
+    v = [0 if variants == "sel" else 1] * L
+    s, sc = decode_gpu(zg, idx, model, u, n, n, v)
+    for q in range(3):
+        bs, bsc = oracle.brute_force(trie, model, u[q])
+        assert np.max(np.abs(sc[q] - bsc)) < tol_for(dtype)
+        got = {tuple(x): y for x, y in zip(s[q], sc[q])}
+        assert set(got) == set(map(tuple, bs))
+        assert abs(np.exp(sc[q].astype(np.float64)).sum() - 1.0) < 1e-4
+
+
+def test_product_catalogue_matches_unconstrained(zg):
+    L, V, d = 3, 12, 16
+    sids = synth.product_catalogue(L, V)
+    model = synth.make_model(L, V, d, "f32", 3)
+    u = synth.make_requests(5, d, 3)
+    idx = zg.zg_index_build(sids, V, stream=_stream())
+    a_s, a_sc = decode_gpu(zg, idx, model, u, 16, 16, [0, 0, 0])
+    b_s, b_sc = decode_gpu(zg, None, model, u, 16, 16)
+    assert np.max(np.abs(a_sc - b_sc)) < 1e-5
+    ref = oracle.decode(None, model, u, 16, 16)
+    check_topk(b_s, b_sc, ref, None, model, u, 1e-4, WINDOW)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_unconstrained_vs_oracle(zg, dtype):
+    L, V, d = 3, 300, 64
+    model = synth.make_model(L, V, d, dtype, 4)
+    u = synth.make_requests(4, d, 4)
+    ref = oracle.decode(None, model, u, 16, 8)
+    s, sc = decode_gpu(zg, None, model, u, 16, 8)
+    check_topk(s, sc, ref, None, model, u, tol_for(dtype), WINDOW)
+
+
+def test_fewer_items_than_beam(zg):
+    sids = np.array([[0, 1, 2], [0, 1, 3], [5, 0, 0]], np.int32)
+    model = synth.make_model(3, 8, 8, "f32")
+    u = synth.make_requests(2, 8)
+    idx = zg.zg_index_build(sids, 8, stream=_stream())
+    trie = oracle.Trie(sids, 3, 8)
+    ref = oracle.decode(trie, model, u, 8, 6)
+    for v in ([0, 0, 0], [1, 1, 1]):
+        s, sc = decode_gpu(zg, idx, model, u, 8, 6, v)
+        assert (s[:, 3:] == -1).all() and np.isneginf(sc[:, 3:]).all()
+        check_topk(s, sc, ref, trie, model, u, 1e-4, WINDOW)
+
+
+def test_worked_example_decode(zg):
+    """After the prefix 3-5 only tokens 1 and 4 can follow: decoding the
+    worked-example catalogue never returns another 3-5-x item."""
+    L, V, sids = golden_catalogue(read_golden("worked_example.txt"))
+    model = synth.make_model(L, V, 8, "f32", 2)
+    u = synth.make_requests(4, 8, 2)
+    idx = zg.zg_index_build(sids, V, stream=_stream())
+    s, sc = decode_gpu(zg, idx, model, u, 16, 7, [0, 0, 0])
+    for q in range(4):
+        got = {tuple(x) for x in s[q]}
+        assert got == {tuple(x) for x in sids}
+        for x in got:
+            if x[:2] == (3, 5):
+                assert x[2] in (1, 4)
+
+
+def test_k_smaller_than_beam_and_beam_one(zg, mid):
+    cfg, sids, model, u, trie, ref, idx = mid
+    uu = u[:8]
+    for beam, K in ((32, 5), (1, 1), (3, 2)):
+        r = oracle.decode(trie, model, uu, beam, K)
+        s, sc = decode_gpu(zg, idx, model, uu, beam, K, [0, 0, 0])
+        check_topk(s, sc, r, trie, model, uu, 1e-4, WINDOW)
