@@ -113,7 +113,7 @@ class ClockSampler:
         sm = [float(r[0]) for r in rows if r[0].strip().replace(".", "").isdigit()]
         mx = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({n for r in rows for n, v in zip(names, r[4:8]) if "Active" in v})
+        reasons = sorted({n for r in rows for n, v in zip(names, r[4:8]) if v.strip() == "Active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
                 "reasons": reasons, "samples": len(rows)}
 
@@ -329,43 +329,42 @@ def run_gpu(args, cfg):
         flush.fill_(1.0)
         traces.append(dec.trace(u_dev))
     L = cfg.L
-    kern = []
-    for s in range(1, L + 1):
-        st = traces[-1][s - 1]
-        avg = {k: statistics.fmean(t[s - 1][k] for t in traces) for k in ("ms_gather", "ms_project", "ms_select")}
-        name_p = "k_selective" if st["variant"] == 0 else "k_full_simt"
-        kern.append((avg["ms_project"], s, name_p, st))
-        kern.append((avg["ms_select"], s, "k_select", st))
-        if avg["ms_gather"] > 0:
-            kern.append((avg["ms_gather"], s, "k_gather_add", st))
-    kern.sort(key=lambda x: -x[0])
+    s0 = traces[-1]["fused_from"] or (L + 1)
+    steps_last = traces[-1]["steps"]
+    kern = []   # (avg ms, steps, kernel name, algorithmic amount, bound)
     peaks = load_peaks()
-    top_ms, top_s, top_name, top_st = kern[0]
-    if top_name == "k_selective":
-        alg = selective_bytes(top_st, cfg, top_s)
-        achieved = alg / (top_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-    elif top_name == "k_select":
-        alg = select_bytes(top_st, cfg, top_s)
-        achieved = alg / (top_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-    elif top_name == "k_full_simt":
-        alg = full_flops(top_st, cfg, top_s)
-        achieved = alg / (top_ms * 1e-3) / 1e12
+    for s in range(1, s0):
+        st = steps_last[s - 1]
+        avg = {k: statistics.fmean(t["steps"][s - 1][k] for t in traces)
+               for k in ("ms_gather", "ms_project", "ms_select")}
+        if st["variant"] == 0:
+            kern.append((avg["ms_project"], [s], "k_selective", selective_bytes(st, cfg, s), "hbm"))
+        else:
+            kern.append((avg["ms_project"], [s], "k_full_simt", full_flops(st, cfg, s), "alu"))
+            if s >= 2:
+                kern.append((avg["ms_gather"], [s], "k_gather_add", st["live_beams"] * cfg.d * 12, "hbm"))
+        kern.append((avg["ms_select"], [s], "k_select", select_bytes(st, cfg, s), "hbm"))
+    if s0 <= L:
+        fused_ms = statistics.fmean(t["ms_fused"] for t in traces)
+        fb = sum(selective_bytes(steps_last[s - 1], cfg, s) + select_bytes(steps_last[s - 1], cfg, s)
+                 for s in range(s0, L + 1))
+        kern.append((fused_ms, list(range(s0, L + 1)), "k_decode_cluster", fb, "hbm"))
+    kern.sort(key=lambda x: -x[0])
+    top_ms, top_steps, top_name, alg, bound = kern[0]
+    if bound == "hbm":
+        roof = {"bound": "hbm", "achieved": alg / (top_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
         sm_mhz = clocks.get("sm_mhz") or peaks["sm_max_mhz"]
         # 152 SMs x 128 fp32 FMA lanes x 2 flops per clock
-        roof = {"bound": "alu", "achieved": achieved, "peak": 152 * 128 * 2 * sm_mhz * 1e6 / 1e12,
-                "unit": "TFLOP/s"}
-    else:
-        alg = top_st["live_beams"] * cfg.d * 4 * 3
-        achieved = alg / (top_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+        roof = {"bound": "alu", "achieved": alg / (top_ms * 1e-3) / 1e12,
+                "peak": 152 * 128 * 2 * sm_mhz * 1e6 / 1e12, "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = ncu_traffic(top_name, cfg.name)
-    roof["kernel"] = f"{top_name} (step {top_s})"
+    roof["kernel"] = f"{top_name} (steps {top_steps[0]}-{top_steps[-1]})"
     roof["ms_per_launch"] = top_ms
     roof["algorithmic"] = alg
     roof["peak_src"] = peaks["src"]
+    work = [{k: v for k, v in st.items() if not k.startswith("ms_")} for st in steps_last]
 
     # end to end through the C ABI with host buffers (pinned), copies inside the timed region
     n_host = zg.zg_decode_host_workspace_size(idx, plan, dm.struct, B, beam, K)
@@ -385,7 +384,8 @@ def run_gpu(args, cfg):
     e2e_ms = (time.perf_counter() - t0) * 1000.0 / e2e_steps
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
 
-    launches_per_step = sum(2 if v == 0 else (2 if s == 0 else 3) for s, v in enumerate(variants))
+    launches_per_step = sum(2 if v == 0 else (2 if s == 0 else 3) for s, v in enumerate(variants[:s0 - 1]))
+    launches_per_step += 1 if s0 <= L else 0
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -418,7 +418,8 @@ def run_gpu(args, cfg):
             "clocks": clocks,
             "unconstrained": {"ms_per_step": ums, "value": B * world / (ums / 1000.0), "unit": UNIT,
                               "constrained_speedup": ums / ms_max},
-            "kernels": [{"kernel": n, "step": s, "ms": round(t, 5)} for t, s, n, _ in kern],
+            "kernels": [{"kernel": n, "steps": st, "ms": round(t, 5)} for t, st, n, _, _ in kern],
+            "work": work,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -10,7 +10,7 @@ from ._lib import (DTYPES, LIB_PATH, ZG_BF16, ZG_F16, ZG_F32, ZG_FMT_DENSE, ZG_F
                    ZgError, make_model, zg_check_device_status, zg_decode, zg_decode_host,
                    zg_decode_host_workspace_size, zg_decode_trace, zg_decode_workspace_size, zg_index_build,
                    zg_index_export, zg_index_info_get, zg_index_load, zg_index_save, zg_index_stats,
-                   zg_plan_describe, zg_plan_force, zg_tune, zg_version)
+                   zg_plan_describe, zg_plan_force, zg_plan_set_fusion, zg_tune, zg_version)
 
 __all__ = [
     "DTYPES", "LIB_PATH", "ZG_BF16", "ZG_F16", "ZG_F32", "ZG_FMT_DENSE", "ZG_FMT_SPARSE",
@@ -19,5 +19,5 @@ __all__ = [
     "make_model", "zg_check_device_status", "zg_decode", "zg_decode_host",
     "zg_decode_host_workspace_size", "zg_decode_trace", "zg_decode_workspace_size", "zg_index_build",
     "zg_index_export", "zg_index_info_get", "zg_index_load", "zg_index_save", "zg_index_stats",
-    "zg_plan_describe", "zg_plan_force", "zg_tune", "zg_version",
+    "zg_plan_describe", "zg_plan_force", "zg_plan_set_fusion", "zg_tune", "zg_version",
 ]

@@ -63,8 +63,8 @@ class zg_step_trace(C.Structure):
 
 
 class zg_trace(C.Structure):
-    _fields_ = [("L", C.c_int32), ("reserved", C.c_int32), ("step", zg_step_trace * ZG_MAX_STEPS),
-                ("ms_total", C.c_float)]
+    _fields_ = [("L", C.c_int32), ("fused_from", C.c_int32), ("step", zg_step_trace * ZG_MAX_STEPS),
+                ("ms_fused", C.c_float), ("ms_total", C.c_float)]
 
 
 def _load():
@@ -83,6 +83,7 @@ def _load():
         "zg_tune": [vp, P(zg_model), vp, i32, i32, i32, i32, vp, P(vp)],
         "zg_plan_force": [vp, i32, i32, vp, P(vp)],
         "zg_plan_describe": [vp, vp, vp],
+        "zg_plan_set_fusion": [vp, i32],
         "zg_decode_workspace_size": [vp, vp, P(zg_model), i32, i32, i32, P(sz)],
         "zg_decode": [vp, vp, P(zg_model), vp, i32, i32, i32, vp, vp, vp, sz, vp],
         "zg_decode_host_workspace_size": [vp, vp, P(zg_model), i32, i32, i32, P(sz)],
@@ -269,10 +270,16 @@ def zg_check_device_status(stream: int = 0):
 
 
 def zg_decode_trace(idx: Index | None, plan: Plan | None, model: zg_model, u, B: int, beam: int, K: int,
-                    out_sids, out_scores, workspace, ws_bytes: int, stream: int = 0) -> list[dict]:
-    """Per-step kernel times (ms) and work counts of one traced decode."""
+                    out_sids, out_scores, workspace, ws_bytes: int, stream: int = 0) -> dict:
+    """Kernel times (ms) of zg_decode's launch sequence and, per step, of the
+    stand-alone step kernels with their work counts."""
     t = zg_trace()
     _check(lib.zg_decode_trace(idx, plan, C.byref(model), _ptr(u), B, beam, K, _ptr(out_sids),
                                _ptr(out_scores), _ptr(workspace), ws_bytes, stream or None, C.byref(t)))
-    return [{f: getattr(t.step[i], f) for f, _ in zg_step_trace._fields_ if f != "reserved"}
-            for i in range(t.L)]
+    steps = [{f: getattr(t.step[i], f) for f, _ in zg_step_trace._fields_ if f != "reserved"}
+             for i in range(t.L)]
+    return {"fused_from": t.fused_from, "ms_fused": t.ms_fused, "ms_total": t.ms_total, "steps": steps}
+
+
+def zg_plan_set_fusion(plan: Plan, enable: bool):
+    _check(lib.zg_plan_set_fusion(plan, 1 if enable else 0))

@@ -28,14 +28,14 @@ def _nvcc() -> str:
 def _flags(src: str):
     common = ["-O3", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden", "-lineinfo"]
     if src.endswith(".cu"):
-        return common + ARCH + ["-Xptxas", "-v"] if os.environ.get("ZG_PTXAS_V") else common + ARCH
-    return common + ["-x", "cu"] + ARCH if src.endswith("_dev.cpp") else common
+        return common + ARCH + (["-Xptxas", "-v"] if os.environ.get("ZG_PTXAS_V") else [])
+    return common
 
 
 def _compile(src: str) -> str:
     obj = os.path.join(BUILD, os.path.basename(src) + ".o")
     path = os.path.join(CSRC, src)
-    deps = [path] + [os.path.join(CSRC, h) for h in os.listdir(CSRC) if h.endswith(".h")]
+    deps = [path] + [os.path.join(CSRC, h) for h in os.listdir(CSRC) if h.endswith((".h", ".cuh"))]
     deps.append(os.path.join(HERE, "..", "include", "zerogr.h"))
     if os.path.exists(obj) and all(os.path.getmtime(obj) >= os.path.getmtime(d) for d in deps):
         return obj

@@ -268,11 +268,35 @@ zg_status prepare(const zg_index* idx, const zg_plan* plan, const zg_model* mode
   return get_status_ptr(&r->status);
 }
 
-zg_status decode_steps(const Run& r, const zg_plan* plan, cudaStream_t st) {
-  for (int s = 1; s <= r.m.L; ++s) {
-    const int v = !r.idx ? ZG_FULL : (plan ? plan->variant[s - 1] : ZG_SELECTIVE);
-    zg_status e = run_step(r, s, v, st);
+constexpr int kClusterCTAs = 8;  // CTAs of the fused kernel's cluster (one cluster per request)
+
+int variant_of(const Run& r, const zg_plan* plan, int s) {
+  return !r.idx ? ZG_FULL : (plan ? plan->variant[s - 1] : ZG_SELECTIVE);
+}
+
+// First step of the trailing run of selective steps that zg_decode fuses
+// (L+1: none).
+int fused_from(const Run& r, const zg_plan* plan) {
+  if (!r.idx || (plan && !plan->fused)) return r.m.L + 1;
+  int s0 = r.m.L + 1;
+  while (s0 > 1 && variant_of(r, plan, s0 - 1) == ZG_SELECTIVE) --s0;
+  return s0;
+}
+
+// zg_decode's launch sequence: stand-alone steps, then the fused suffix.
+zg_status decode_steps(const Run& r, const zg_plan* plan, cudaStream_t st, cudaEvent_t* fuse_ev = nullptr) {
+  const int s0 = fused_from(r, plan);
+  for (int s = 1; s < s0; ++s) {
+    zg_status e = run_step(r, s, variant_of(r, plan, s), st);
     if (e != ZG_OK) return e;
+  }
+  if (s0 <= r.m.L) {
+    StepLaunch steps[ZG_MAX_STEPS];
+    for (int s = 1; s <= r.m.L; ++s) steps[s - 1] = make_launch(r, s, ZG_SELECTIVE);
+    if (fuse_ev) cudaEventRecord(fuse_ev[0], st);
+    cudaError_t e = launch_decode_cluster(steps, s0, r.m.L, kClusterCTAs, st);
+    if (e != cudaSuccess) return cuda_fail(e, "fused cluster decode launch");
+    if (fuse_ev) cudaEventRecord(fuse_ev[1], st);
   }
   return ZG_OK;
 }
@@ -323,6 +347,12 @@ zg_status zg_plan_describe(const zg_plan* plan, uint8_t* variant, float* step_ms
 }
 
 void zg_plan_free(zg_plan* plan) { delete plan; }
+
+zg_status zg_plan_set_fusion(zg_plan* plan, int32_t enable) {
+  if (!plan) return fail(ZG_ERR_INVALID_ARG, "zg_plan_set_fusion: plan is NULL");
+  plan->fused = enable ? 1 : 0;
+  return ZG_OK;
+}
 
 zg_status zg_decode_workspace_size(const zg_index* idx, const zg_plan* plan, const zg_model* model, int32_t B,
                                    int32_t beam, int32_t K, size_t* bytes) {
@@ -470,28 +500,44 @@ zg_status zg_decode_trace(const zg_index* idx, const zg_plan* plan, const zg_mod
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   std::memset(trace, 0, sizeof(*trace));
   trace->L = r.m.L;
-  StepTimer tm[ZG_MAX_STEPS];
+  constexpr int kEv = 4 * ZG_MAX_STEPS + 4;
+  cudaEvent_t ev[kEv] = {};
   int made = 0;
   cudaError_t e = cudaSuccess;
-  for (int i = 0; i < r.m.L && e == cudaSuccess; ++i)
-    for (int j = 0; j < 4 && e == cudaSuccess; ++j) {
-      e = cudaEventCreate(&tm[i].ev[j]);
-      if (e == cudaSuccess) ++made;
-    }
+  for (; made < kEv && e == cudaSuccess; ++made) e = cudaEventCreate(&ev[made]);
   auto cleanup = [&]() {
-    for (int i = 0; i < made; ++i) cudaEventDestroy(tm[i / 4].ev[i % 4]);
+    for (int i = 0; i < kEv; ++i)
+      if (ev[i]) cudaEventDestroy(ev[i]);
   };
   if (e != cudaSuccess) {
     cleanup();
     return cuda_fail(e, "zg_decode_trace: cudaEventCreate");
   }
+  // pass 1: zg_decode's own launch sequence
+  const int s0 = fused_from(r, plan);
+  cudaEventRecord(ev[kEv - 2], s);
+  st = decode_steps(r, plan, s, s0 <= r.m.L ? &ev[kEv - 4] : nullptr);
+  cudaEventRecord(ev[kEv - 1], s);
+  if (st == ZG_OK && (e = cudaEventSynchronize(ev[kEv - 1])) != cudaSuccess) st = cuda_fail(e, "zg_decode_trace");
+  if (st != ZG_OK) {
+    cleanup();
+    return st;
+  }
+  cudaEventElapsedTime(&trace->ms_total, ev[kEv - 2], ev[kEv - 1]);
+  if (s0 <= r.m.L) {
+    trace->fused_from = s0;
+    cudaEventElapsedTime(&trace->ms_fused, ev[kEv - 4], ev[kEv - 3]);
+  }
+  // pass 2: stand-alone step kernels, each timed, with work counts
   auto* cnt = reinterpret_cast<unsigned long long*>(r.ws + r.w.trace);
   auto* mask = reinterpret_cast<uint32_t*>(r.ws + r.w.trace + 32);
   const int words = (r.m.V + 31) / 32;
   std::vector<uint32_t> hmask(words);
   for (int step = 1; step <= r.m.L; ++step) {
-    const int v = !r.idx ? ZG_FULL : (plan ? plan->variant[step - 1] : ZG_SELECTIVE);
-    st = run_step(r, step, v, s, &tm[step - 1]);
+    const int v = variant_of(r, plan, step);
+    StepTimer tm;
+    for (int j = 0; j < 4; ++j) tm.ev[j] = ev[4 * (step - 1) + j];
+    st = run_step(r, step, v, s, &tm);
     if (st != ZG_OK) break;
     // untimed: what this step worked on (its entering state is still intact)
     const StepLaunch a = make_launch(r, step, v);
@@ -514,14 +560,13 @@ zg_status zg_decode_trace(const zg_index* idx, const zg_plan* plan, const zg_mod
     int64_t ut = 0;
     for (uint32_t w : hmask) ut += __builtin_popcount(w);
     t.unique_tokens = ut;
-    float g = 0.f, p = 0.f, q = 0.f;
-    cudaEventElapsedTime(&g, tm[step - 1].ev[0], tm[step - 1].ev[1]);
-    cudaEventElapsedTime(&p, tm[step - 1].ev[1], tm[step - 1].ev[2]);
-    cudaEventElapsedTime(&q, tm[step - 1].ev[2], tm[step - 1].ev[3]);
-    t.ms_gather = g;
-    t.ms_project = p;
+    float g = 0.f, pj = 0.f, q = 0.f;
+    cudaEventElapsedTime(&g, tm.ev[0], tm.ev[1]);
+    cudaEventElapsedTime(&pj, tm.ev[1], tm.ev[2]);
+    cudaEventElapsedTime(&q, tm.ev[2], tm.ev[3]);
+    t.ms_gather = (v == ZG_FULL && step >= 2) ? g : 0.f;
+    t.ms_project = pj;
     t.ms_select = q;
-    trace->ms_total += g + p + q;
   }
   cleanup();
   return st;

@@ -1,0 +1,642 @@
+// Device building blocks shared by the per-step kernels and the cluster
+// decode kernel: weight-row conversion, order-preserving score keys, the
+// selective projection of one 32-slot chunk, and the CTA-level select.
+//
+// "ZeroGR: Filtering-First Constrained Decoding for Generative
+// Recommendation" (paper-daily.com digest), section "Why computing fewer
+// scores is not automatically faster": padded candidate slots (a slot
+// depends only on its beam and rank, empty slots score -inf), weight rows
+// read in place; section "Overall flow", stage 4: log-softmax over the
+// legal tokens only, add to the cumulative log-probability, choose beams.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "zg_internal.h"
+
+namespace zg {
+namespace dev {
+
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
+__device__ __forceinline__ void flag(uint32_t* st, uint32_t bit) { atomicOr(st, bit); }
+
+// Order-preserving map float -> uint32 (larger float -> larger key).  Every
+// non-NaN float maps to a non-zero key, so 0 marks "no candidate".
+__device__ __forceinline__ uint32_t f2ord(float f) {
+  uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float ord2f(uint32_t k) {
+  uint32_t u = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
+  return __uint_as_float(u);
+}
+
+// 16 bytes of weights -> fp32 lanes (exact widening for bf16/fp16).
+template <typename WT>
+struct Vec;
+template <>
+struct Vec<float> {
+  static constexpr int E = 4;
+  __device__ __forceinline__ static void cvt(const uint4& r, float* o) {
+    o[0] = __uint_as_float(r.x);
+    o[1] = __uint_as_float(r.y);
+    o[2] = __uint_as_float(r.z);
+    o[3] = __uint_as_float(r.w);
+  }
+};
+template <>
+struct Vec<__nv_bfloat16> {
+  static constexpr int E = 8;
+  __device__ __forceinline__ static void cvt(const uint4& r, float* o) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      o[2 * i] = __uint_as_float(w[i] << 16);
+      o[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+};
+template <>
+struct Vec<__half> {
+  static constexpr int E = 8;
+  __device__ __forceinline__ static void cvt(const uint4& r, float* o) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __half2 h2 = *reinterpret_cast<const __half2*>(&w[i]);
+      float2 f = __half22float2(h2);
+      o[2 * i] = f.x;
+      o[2 * i + 1] = f.y;
+    }
+  }
+};
+
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+// (max, sum exp(x - max)) pairs combine associatively.
+__device__ __forceinline__ float2 lse_combine(float2 a, float2 b) {
+  float m = fmaxf(a.x, b.x);
+  if (m == -INFINITY) return make_float2(-INFINITY, 0.f);
+  float s = 0.f;
+  if (a.y > 0.f) s += a.y * expf(a.x - m);
+  if (b.y > 0.f) s += b.y * expf(b.x - m);
+  return make_float2(m, s);
+}
+
+__device__ __forceinline__ float2 warp_lse(float2 acc) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    float2 other;
+    other.x = __shfl_xor_sync(kFull, acc.x, o);
+    other.y = __shfl_xor_sync(kFull, acc.y, o);
+    acc = lse_combine(acc, other);
+  }
+  return acc;
+}
+
+// State of beam k of request q entering step s.
+struct BeamState {
+  uint32_t row;
+  float cum;
+  int par, tok;
+};
+__device__ __forceinline__ BeamState load_beam(const StepLaunch& a, int q, int k) {
+  BeamState bs;
+  if (a.s == 1) {
+    bs.row = 0;
+    bs.cum = 0.f;
+    bs.par = 0;
+    bs.tok = 0;
+  } else {
+    const int i = q * a.beam + k;
+    bs.row = a.row_in ? a.row_in[i] : 0u;
+    bs.cum = a.cum_in[i];
+    bs.par = a.par_in[i];
+    bs.tok = a.tok_in[i];
+    if (bs.cum == -INFINITY) bs.row = kDeadRow;
+  }
+  return bs;
+}
+
+// ---------------------------------------------------------------------------
+// Selective projection of chunk c (slots 32c..32c+31) of beam k of request q
+// by one warp.  The warp gathers h_b = h_parent + C_{s-1}[token] (fp32,
+// lane-sliced in registers; written out once, by chunk 0, for the next step),
+// reads each legal token's weight row in place with coalesced 16-byte loads,
+// accumulates per-lane partial dots for the 32 rows and reduce-scatters them
+// with 31 shuffles so lane j ends with z of slot j.  It writes the chunk's 32
+// slots (-inf where empty) and its (max, sum exp) partial of the legal-only
+// log-sum-exp.  `row`, `rp0`, `F` are the beam's index row, first entry and
+// fan-out (checked by the caller).
+// ---------------------------------------------------------------------------
+template <typename WT, int VPL>
+__device__ __forceinline__ void score_chunk(const StepLaunch& a, int q, int k, const BeamState& bs, uint32_t rp0,
+                                            uint32_t F, int c, int lane) {
+  using VT = Vec<WT>;
+  constexpr int E = VT::E;
+  const int d = a.d;
+  const int nvec = d / E;
+  const int b = q * a.Wc + k;
+  const int j0 = c * kChunk;
+  uint32_t vmask;
+  int t_lane = 0;
+  if (a.mode == kSelDense) {
+    vmask = a.tab.bitmap[(size_t)bs.row * a.tab.words + c];
+    t_lane = j0 + lane;
+    if (a.V - j0 < 32) vmask &= (1u << (a.V - j0)) - 1u;
+  } else {
+    const int nvalid = min(32, (int)F - j0);
+    vmask = (nvalid >= 32) ? kFull : ((1u << nvalid) - 1u);
+    if (lane < nvalid) t_lane = a.tab.col[rp0 + j0 + lane];
+  }
+  if (((vmask >> lane) & 1u) && t_lane >= a.V) {
+    flag(a.status, kStatusToken);
+    vmask &= ~(1u << lane);
+  }
+  vmask = __ballot_sync(kFull, (vmask >> lane) & 1u);  // each lane vouches for its own slot
+
+  float h[VPL][E];
+  {
+    const float* hp;
+    const float* cr = nullptr;
+    if (a.s == 1) {
+      hp = a.u + (size_t)q * d;
+    } else {
+      hp = a.h_prev + ((size_t)q * a.Wp + bs.par) * d;
+      cr = a.C_prev + (size_t)bs.tok * d;
+    }
+    const bool write_h = (c == 0) && a.h_out;
+#pragma unroll
+    for (int r = 0; r < VPL; ++r) {
+      const int v = lane + 32 * r;
+#pragma unroll
+      for (int e = 0; e < E; ++e) h[r][e] = 0.f;
+      if (v < nvec) {
+#pragma unroll
+        for (int e4 = 0; e4 < E; e4 += 4) {
+          float4 x = *reinterpret_cast<const float4*>(hp + v * E + e4);
+          if (cr) {
+            const float4 y = *reinterpret_cast<const float4*>(cr + v * E + e4);
+            x.x += y.x;
+            x.y += y.y;
+            x.z += y.z;
+            x.w += y.w;
+          }
+          h[r][e4] = x.x;
+          h[r][e4 + 1] = x.y;
+          h[r][e4 + 2] = x.z;
+          h[r][e4 + 3] = x.w;
+          if (write_h) *reinterpret_cast<float4*>(a.h_out + (size_t)b * d + v * E + e4) = x;
+        }
+      }
+    }
+  }
+
+  float acc[32];
+#pragma unroll
+  for (int r = 0; r < 32; ++r) acc[r] = 0.f;
+  const WT* Wm = static_cast<const WT*>(a.W);
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    if (((vmask >> (8 * g)) & 0xFFu) == 0u) continue;
+    uint4 raw[8][VPL];
+#pragma unroll
+    for (int rr = 0; rr < 8; ++rr) {
+      const int r = 8 * g + rr;
+      const int t = __shfl_sync(kFull, t_lane, r);
+      const bool ok = (vmask >> r) & 1u;
+      const WT* wrow = Wm + (size_t)t * d;
+#pragma unroll
+      for (int vv = 0; vv < VPL; ++vv) {
+        const int v = lane + 32 * vv;
+        raw[rr][vv] = (ok && v < nvec) ? ldg_stream(wrow + v * E) : make_uint4(0, 0, 0, 0);
+      }
+    }
+#pragma unroll
+    for (int rr = 0; rr < 8; ++rr) {
+      float sacc = 0.f;
+#pragma unroll
+      for (int vv = 0; vv < VPL; ++vv) {
+        float w[E];
+        VT::cvt(raw[rr][vv], w);
+#pragma unroll
+        for (int e = 0; e < E; ++e) sacc = fmaf(w[e], h[vv][e], sacc);
+      }
+      acc[8 * g + rr] = sacc;
+    }
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const bool upper = lane & off;
+#pragma unroll
+    for (int i = 0; i < off; ++i) {
+      const float send = upper ? acc[i] : acc[i + off];
+      const float keep = upper ? acc[i + off] : acc[i];
+      acc[i] = keep + __shfl_xor_sync(kFull, send, off);
+    }
+  }
+  const bool valid = (vmask >> lane) & 1u;
+  const float z = valid ? acc[0] : -INFINITY;
+  const float m = warp_max(z);
+  const float e = valid ? expf(z - m) : 0.f;
+  float ssum = warp_sum(e);
+  ssum = __shfl_sync(kFull, ssum, 0);
+  a.Z[(size_t)b * a.S + j0 + lane] = z;
+  if (lane == 0) a.part[(size_t)b * a.nch + c] = make_float2(m, vmask ? ssum : 0.f);
+}
+
+// ---------------------------------------------------------------------------
+// Per-request beam table and select scratch (shared memory).
+// ---------------------------------------------------------------------------
+struct BeamTab {
+  uint32_t row[ZG_MAX_BEAM];
+  uint32_t rp[ZG_MAX_BEAM];
+  int cnt[ZG_MAX_BEAM];        // candidate positions (slots) of the beam
+  int nleg[ZG_MAX_BEAM];       // legal candidates of the beam
+  int items[ZG_MAX_BEAM];      // 32-slot chunks to score (cluster kernel)
+  float cum[ZG_MAX_BEAM];
+  float lse[ZG_MAX_BEAM];
+  int par[ZG_MAX_BEAM];
+  int tok[ZG_MAX_BEAM];
+  int start[ZG_MAX_BEAM + 1];  // flat candidate prefix
+  int istart[ZG_MAX_BEAM + 1]; // chunk prefix
+  int total, nlegal;
+};
+
+struct SelWork {
+  uint32_t hist[256];
+  unsigned long long win[ZG_MAX_BEAM];
+  int warp_tot[32];
+  uint32_t prefix, prefmask;
+  int need, cnt_gt, cnt_eq, nwin;
+  int all_eq;
+};
+
+// largest k with arr[k] <= c (arr ascending, arr[0] = 0)
+__device__ __forceinline__ int upper_find(const int* arr, int n, int c) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (arr[mid] <= c)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
+// Fill the beam table of request q entering step s (threads k < Wc), then
+// the flat-candidate and chunk prefixes.  Returns after __syncthreads.
+template <int NT>
+__device__ void build_beam_table(const StepLaunch& a, int q, BeamTab& bt) {
+  const int tid = threadIdx.x;
+  const bool constrained = (a.mode != kUncon);
+  const bool sparse_slots = (a.mode == kSelSparse || a.mode == kFullSparse);
+  for (int k = tid; k < a.Wc; k += NT) {
+    const BeamState bs = load_beam(a, q, k);
+    bool dead = (bs.row == kDeadRow);
+    uint32_t F = 0, rp = 0;
+    if (!dead && constrained) {
+      if (bs.row >= a.tab.rows) {
+        flag(a.status, kStatusRow);
+        dead = true;
+      } else {
+        rp = a.tab.rowptr[bs.row];
+        F = a.tab.rowptr[bs.row + 1] - rp;
+      }
+    } else if (!dead) {
+      F = (uint32_t)a.V;
+    }
+    bt.row[k] = bs.row;
+    bt.rp[k] = rp;
+    bt.cum[k] = bs.cum;
+    bt.par[k] = bs.par;
+    bt.tok[k] = bs.tok;
+    bt.cnt[k] = dead ? 0 : (sparse_slots ? (int)F : a.V);
+    bt.nleg[k] = dead ? 0 : (int)F;
+    bt.items[k] = dead ? 0 : (a.mode == kSelSparse ? (int)((F + kChunk - 1) / kChunk) : a.nch);
+    bt.lse[k] = 0.f;
+  }
+  __syncthreads();
+  if (tid < 32) {
+    // warp prefix sums over Wc <= 512 beams, 16 consecutive beams a lane
+    const int lane = tid;
+    const int per = (a.Wc + 31) / 32;
+    const int k0 = lane * per;
+    int sc = 0, si = 0, sl = 0;
+    for (int k = k0; k < min(k0 + per, a.Wc); ++k) {
+      sc += bt.cnt[k];
+      si += bt.items[k];
+      sl += bt.nleg[k];
+    }
+    int ic = sc, ii = si, il = sl;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int yc = __shfl_up_sync(kFull, ic, o);
+      const int yi = __shfl_up_sync(kFull, ii, o);
+      const int yl = __shfl_up_sync(kFull, il, o);
+      if (lane >= o) {
+        ic += yc;
+        ii += yi;
+        il += yl;
+      }
+    }
+    int rc = ic - sc, ri = ii - si;
+    for (int k = k0; k < min(k0 + per, a.Wc); ++k) {
+      bt.start[k] = rc;
+      bt.istart[k] = ri;
+      rc += bt.cnt[k];
+      ri += bt.items[k];
+    }
+    if (lane == 31) {
+      bt.start[a.Wc] = ic;
+      bt.istart[a.Wc] = ii;
+      bt.total = ic;
+      bt.nlegal = il;
+    }
+  }
+  __syncthreads();
+}
+
+// Legal-only log-sum-exp of every live beam (one warp per beam): from the
+// selective chunk partials, or by two passes over the full scores.
+template <int NT>
+__device__ void beam_lse(const StepLaunch& a, int q, BeamTab& bt) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int k = warp; k < a.Wc; k += NT / 32) {
+    if (bt.cnt[k] == 0) continue;
+    const int b = q * a.Wc + k;
+    float2 acc = make_float2(-INFINITY, 0.f);
+    if (a.mode == kSelSparse || a.mode == kSelDense) {
+      const int nch = (a.mode == kSelSparse) ? (bt.cnt[k] + kChunk - 1) / kChunk : a.nch;
+      for (int c = lane; c < nch; c += 32) acc = lse_combine(acc, a.part[(size_t)b * a.nch + c]);
+    } else {
+      const int n = bt.cnt[k];
+      const size_t zb = (size_t)b * a.S;
+      float m = -INFINITY, sm = 0.f;
+      for (int pass = 0; pass < 2; ++pass) {
+        for (int j = lane; j < n; j += 32) {
+          float z;
+          if (a.mode == kFullSparse)
+            z = a.Z[zb + a.tab.col[bt.rp[k] + j]];
+          else if (a.mode == kFullDense)
+            z = ((a.tab.bitmap[(size_t)bt.row[k] * a.tab.words + (j >> 5)] >> (j & 31)) & 1u) ? a.Z[zb + j]
+                                                                                          : -INFINITY;
+          else
+            z = a.Z[zb + j];
+          if (pass == 0)
+            m = fmaxf(m, z);
+          else if (z != -INFINITY)
+            sm += expf(z - m);
+        }
+        if (pass == 0) m = warp_max(m);
+      }
+      acc = make_float2(m, sm);
+    }
+    acc = warp_lse(acc);
+    if (lane == 0) bt.lse[k] = acc.x + logf(acc.y);
+  }
+}
+
+// Key of flat candidate c (0 = illegal slot).
+__device__ __forceinline__ uint32_t cand_key(const StepLaunch& a, const BeamTab& bt, int q, int c) {
+  const int k = upper_find(bt.start, a.Wc, c);
+  const int j = c - bt.start[k];
+  const size_t zb = (size_t)(q * a.Wc + k) * a.S;
+  float z;
+  switch (a.mode) {
+    case kSelSparse:
+    case kUncon:
+      z = a.Z[zb + j];
+      break;
+    case kFullSparse:
+      z = a.Z[zb + a.tab.col[bt.rp[k] + j]];
+      break;
+    default:  // kSelDense, kFullDense
+      if (!((a.tab.bitmap[(size_t)bt.row[k] * a.tab.words + (j >> 5)] >> (j & 31)) & 1u)) return 0u;
+      z = a.Z[zb + j];
+      break;
+  }
+  return f2ord(bt.cum[k] + (z - bt.lse[k]));
+}
+
+// ---------------------------------------------------------------------------
+// CTA-level select of the keep best legal candidates of request q: keys are
+// staged in shared memory when they fit (`cap` entries), then 8-bit radix
+// passes with warp-aggregated histograms narrow the threshold key (stopping
+// as soon as the threshold bin holds exactly the remainder), winners above
+// the threshold are collected, threshold ties go to the lowest flat slot
+// indices, and the winners are bitonic-sorted by (score desc, flat asc).
+// Leaves sw.win[0..n) sorted; returns n = min(keep, legal candidates).
+// ---------------------------------------------------------------------------
+template <int NT>
+__device__ int cta_select(const StepLaunch& a, int q, BeamTab& bt, SelWork& sw, uint32_t* keys, int cap) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int total = bt.total;
+  const int keep_n = min(a.keep, bt.nlegal);
+  const bool staged = total <= cap;
+  if (staged)
+    for (int c = tid; c < total; c += NT) keys[c] = cand_key(a, bt, q, c);
+  if (tid == 0) {
+    sw.nwin = 0;
+    sw.prefix = 0;
+    sw.prefmask = 0;
+    sw.need = keep_n;
+    sw.cnt_gt = 0;
+    sw.cnt_eq = bt.nlegal;
+    sw.all_eq = (keep_n == bt.nlegal) ? 1 : 0;
+  }
+  __syncthreads();
+  if (keep_n == 0) return 0;
+  for (int shift = 24; shift >= 0 && !sw.all_eq; shift -= 8) {
+    for (int i = tid; i < 256; i += NT) sw.hist[i] = 0;
+    __syncthreads();
+    const uint32_t pm = sw.prefmask, pv = sw.prefix;
+    for (int c0 = 0; c0 < total; c0 += NT) {
+      const int c = c0 + tid;
+      int dgt = -1;
+      if (c < total) {
+        const uint32_t key = staged ? keys[c] : cand_key(a, bt, q, c);
+        if (key && (key & pm) == pv) dgt = (int)((key >> shift) & 255u);
+      }
+      const unsigned act = __activemask();
+      const unsigned peers = __match_any_sync(act, dgt);
+      if (dgt >= 0 && lane == __ffs(peers) - 1) atomicAdd(&sw.hist[dgt], (uint32_t)__popc(peers));
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l owns bins [248 - 8l, 256 - 8l), scanned from the top
+      const int hi = 256 - 8 * lane;
+      uint32_t mine = 0;
+#pragma unroll
+      for (int i = 1; i <= 8; ++i) mine += sw.hist[hi - i];
+      uint32_t incl = mine;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const uint32_t excl = incl - mine;
+      const uint32_t target = (uint32_t)(sw.need - sw.cnt_gt);
+      const bool here = (excl < target) && (incl >= target);
+      const unsigned who = __ballot_sync(kFull, here);
+      if (here && lane == __ffs(who) - 1) {
+        uint32_t run = excl;
+        for (int i = hi - 1; i >= hi - 8; --i) {
+          const uint32_t hc = sw.hist[i];
+          if (run + hc >= target) {
+            sw.cnt_gt += (int)run;
+            sw.prefix |= (uint32_t)i << shift;
+            sw.prefmask |= 255u << shift;
+            sw.cnt_eq = (int)hc;
+            if ((int)hc == sw.need - sw.cnt_gt) sw.all_eq = 1;
+            break;
+          }
+          run += hc;
+        }
+      }
+    }
+    __syncthreads();
+  }
+  const uint32_t pm = sw.prefmask, pv = sw.prefix;
+  const int need_eq = sw.need - sw.cnt_gt;
+  const bool all_eq = sw.all_eq;
+  for (int c = tid; c < total; c += NT) {
+    const uint32_t key = staged ? keys[c] : cand_key(a, bt, q, c);
+    if (!key) continue;
+    const uint32_t mk = key & pm;
+    if (mk > pv || (all_eq && mk == pv)) {
+      const int slot = atomicAdd(&sw.nwin, 1);
+      if (slot < ZG_MAX_BEAM) sw.win[slot] = ((unsigned long long)key << 32) | (0xFFFFFFFFu - (uint32_t)c);
+    }
+  }
+  __syncthreads();
+  if (!all_eq) {
+    // ties at the exact threshold key: the need_eq lowest flat indices
+    int base = 0;
+    for (int c0 = 0; c0 < total && base < need_eq; c0 += NT) {
+      const int c = c0 + tid;
+      uint32_t key = 0;
+      if (c < total) key = staged ? keys[c] : cand_key(a, bt, q, c);
+      const bool f = key && key == pv;
+      const unsigned bal = __ballot_sync(kFull, f);
+      if (lane == 0) sw.warp_tot[warp] = __popc(bal);
+      __syncthreads();
+      int before = base;
+      for (int w = 0; w < warp; ++w) before += sw.warp_tot[w];
+      before += __popc(bal & ((1u << lane) - 1u));
+      if (f && before < need_eq) {
+        const int slot = atomicAdd(&sw.nwin, 1);
+        if (slot < ZG_MAX_BEAM) sw.win[slot] = ((unsigned long long)key << 32) | (0xFFFFFFFFu - (uint32_t)c);
+      }
+      int tile = 0;
+      for (int w = 0; w < NT / 32; ++w) tile += sw.warp_tot[w];
+      __syncthreads();
+      base += tile;
+    }
+  }
+  __syncthreads();
+  int P = 1;
+  while (P < keep_n) P <<= 1;
+  for (int i = keep_n + tid; i < P; i += NT) sw.win[i] = 0ull;
+  __syncthreads();
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = tid; i < P; i += NT) {
+        const int jx = i ^ stride;
+        if (jx > i) {
+          const bool desc = ((i & size) == 0);
+          const unsigned long long x = sw.win[i], y = sw.win[jx];
+          if (desc ? (x < y) : (x > y)) {
+            sw.win[i] = y;
+            sw.win[jx] = x;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  return keep_n;
+}
+
+// Write survivor i (< n) of the sorted winners, or a dead/padding row.
+__device__ __forceinline__ void write_survivor(const StepLaunch& a, int q, const BeamTab& bt, const SelWork& sw, int i,
+                                               int n) {
+  const int s = a.s;
+  const size_t BW = (size_t)a.B * a.beam;
+  const bool sparse_slots = (a.mode == kSelSparse || a.mode == kFullSparse);
+  if (i < n) {
+    const unsigned long long w = sw.win[i];
+    const uint32_t key = (uint32_t)(w >> 32);
+    const int c = (int)(0xFFFFFFFFu - (uint32_t)(w & 0xFFFFFFFFu));
+    const int k = upper_find(bt.start, a.Wc, c);
+    const int j = c - bt.start[k];
+    const float score = ord2f(key);
+    int t;
+    uint32_t nrow = 0;
+    if (sparse_slots) {
+      t = a.tab.col[bt.rp[k] + j];
+      nrow = bt.rp[k] + (uint32_t)j;
+    } else {
+      t = j;
+      if (a.mode != kUncon) {
+        const uint32_t* bm = a.tab.bitmap + (size_t)bt.row[k] * a.tab.words;
+        uint32_t rank = 0;
+        for (int wd = 0; wd < (t >> 5); ++wd) rank += __popc(bm[wd]);
+        rank += __popc(bm[t >> 5] & ((1u << (t & 31)) - 1u));
+        nrow = bt.rp[k] + rank;
+      }
+    }
+    if (s < a.L) {
+      const size_t o = (size_t)q * a.beam + i;
+      if (a.row_out) a.row_out[o] = nrow;
+      a.cum_out[o] = score;
+      a.tok_hist[(size_t)(s - 1) * BW + o] = t;
+      a.par_hist[(size_t)(s - 1) * BW + o] = k;
+    } else {
+      a.out_scores[(size_t)q * a.K + i] = score;
+      int32_t* sid = a.out_sids + ((size_t)q * a.K + i) * a.L;
+      sid[a.L - 1] = t;
+      int kc = k;
+      for (int sp = a.L - 1; sp >= 1; --sp) {
+        const size_t o = (size_t)(sp - 1) * BW + (size_t)q * a.beam + kc;
+        sid[sp - 1] = a.tok_hist[o];
+        kc = a.par_hist[o];
+      }
+    }
+  } else {
+    if (s < a.L) {
+      const size_t o = (size_t)q * a.beam + i;
+      if (a.row_out) a.row_out[o] = kDeadRow;
+      a.cum_out[o] = -INFINITY;
+      a.tok_hist[(size_t)(s - 1) * BW + o] = 0;
+      a.par_hist[(size_t)(s - 1) * BW + o] = 0;
+    } else {
+      a.out_scores[(size_t)q * a.K + i] = -INFINITY;
+      int32_t* sid = a.out_sids + ((size_t)q * a.K + i) * a.L;
+      for (int sp = 0; sp < a.L; ++sp) sid[sp] = -1;
+    }
+  }
+}
+
+}  // namespace dev
+}  // namespace zg

@@ -85,6 +85,9 @@ cudaError_t launch_selective(const StepLaunch& a, cudaStream_t st);
 cudaError_t launch_gather_add(const StepLaunch& a, float* H, cudaStream_t st);
 cudaError_t launch_full_simt(const StepLaunch& a, const float* H, cudaStream_t st);
 cudaError_t launch_select(const StepLaunch& a, cudaStream_t st);
+// Steps s0..L (all selective) in one cluster kernel, G CTAs per request;
+// steps[] holds the launch description of every step (1-based s at [s-1]).
+cudaError_t launch_decode_cluster(const StepLaunch* steps, int s0, int L, int G, cudaStream_t st);
 cudaError_t status_word(uint32_t** dev_ptr);   // per-device status word address
 // Work counts of the beams entering a step (tracing only): counters[0..3] =
 // live beams, legal slots, chunks, index bytes; mask = V-bit set of touched
@@ -113,6 +116,7 @@ struct zg_index {
 
 struct zg_plan {
   int32_t L = 0, B = 0, beam = 0;
+  int32_t fused = 1;
   std::vector<uint8_t> variant;  // [L]
   std::vector<float> step_ms;    // [L][2]
 };

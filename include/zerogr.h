@@ -176,6 +176,11 @@ ZG_API zg_status zg_tune(const zg_index* idx, const zg_model* model, const float
 /* A plan with a fixed variant per step (variant: host uint8 [L]). */
 ZG_API zg_status zg_plan_force(const zg_index* idx, int32_t B, int32_t beam, const uint8_t* variant,
                         zg_plan** out);
+/* Whether zg_decode runs the plan's trailing run of ZG_SELECTIVE steps as one
+ * fused kernel (a thread-block cluster per request, cluster barriers between
+ * scoring and selection); default 1.  0 runs every step as stand-alone
+ * kernels.  Results are identical either way. */
+ZG_API zg_status zg_plan_set_fusion(zg_plan* plan, int32_t enable);
 /* variant: host uint8 [L] (may be NULL); step_ms: host float [L][2] timings
  * of {SELECTIVE, FULL} from zg_tune (-1 when not timed; may be NULL). */
 ZG_API zg_status zg_plan_describe(const zg_plan* plan, uint8_t* variant, float* step_ms);
@@ -239,17 +244,22 @@ typedef struct {
 } zg_step_trace;
 
 typedef struct {
-  int32_t L, reserved;
-  zg_step_trace step[ZG_MAX_STEPS];
-  float ms_total;         /* sum of the timed kernels                               */
+  int32_t L;
+  int32_t fused_from;     /* first step zg_decode runs in its fused cluster kernel
+                             (0: none)                                              */
+  zg_step_trace step[ZG_MAX_STEPS]; /* stand-alone step kernels, step by step       */
+  float ms_fused;         /* zg_decode's fused cluster kernel                        */
+  float ms_total;         /* all kernels of zg_decode's own launch sequence          */
 } zg_trace;
 
-/* zg_decode_trace - the zg_decode computation (same kernels, same results)
- * run step by step with CUDA events around every kernel launch on `stream`,
- * plus an untimed counting kernel per step that fills the work counts above
- * (the observability the per-step variant choice of [Speed] rests on).
- * Synchronous; not for CUDA graph capture.  The workspace is the one sized by
- * zg_decode_workspace_size. */
+/* zg_decode_trace - two timed passes of the zg_decode computation on
+ * `stream` (CUDA events around every kernel launch): first zg_decode's own
+ * launch sequence (ms_fused, ms_total), then the stand-alone step kernels
+ * step by step (ms_gather/ms_project/ms_select) with an untimed counting
+ * kernel after each step that fills the work counts (the observability the
+ * per-step variant choice of [Speed] rests on).  Both passes give the same
+ * results; the outputs hold the second pass's.  Synchronous; not for CUDA
+ * graph capture.  The workspace is the one sized by zg_decode_workspace_size. */
 ZG_API zg_status zg_decode_trace(const zg_index* idx, const zg_plan* plan, const zg_model* model,
                                  const float* u, int32_t B, int32_t beam, int32_t K,
                                  int32_t* out_sids, float* out_scores, void* workspace,

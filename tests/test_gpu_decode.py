@@ -34,12 +34,13 @@ def _stream():
     return torch.cuda.current_stream().cuda_stream
 
 
-def decode_gpu(zg, idx, model, u, beam, K, variants=None, dm=None, plan=None):
+def decode_gpu(zg, idx, model, u, beam, K, variants=None, dm=None, plan=None, fused=True):
     from generative_recommendation_constrained_gb300.device import Decoder, DeviceModel
     dm = dm or DeviceModel(model)
     B = u.shape[0]
     if plan is None and variants is not None:
         plan = zg.zg_plan_force(idx, B, beam, variants)
+        zg.zg_plan_set_fusion(plan, fused)
     dec = Decoder(idx, plan, dm, B, beam, K)
     s, sc = dec(torch.from_numpy(np.ascontiguousarray(u)).cuda())
     torch.cuda.synchronize()
@@ -120,10 +121,11 @@ def mid(zg):
     return cfg, sids, model, u, trie, ref, idx
 
 
-@pytest.mark.parametrize("variants", [[0, 0, 0], [1, 1, 1], [1, 0, 0], [0, 1, 1]])
-def test_mid_sparse_parity(zg, mid, variants):
+@pytest.mark.parametrize("variants", [[0, 0, 0], [1, 1, 1], [1, 0, 0], [0, 1, 1], [0, 1, 0]])
+@pytest.mark.parametrize("fused", [True, False])
+def test_mid_sparse_parity(zg, mid, variants, fused):
     cfg, sids, model, u, trie, ref, idx = mid
-    s, sc = decode_gpu(zg, idx, model, u, cfg.beam, cfg.topk, variants)
+    s, sc = decode_gpu(zg, idx, model, u, cfg.beam, cfg.topk, variants, fused=fused)
     amb = check_topk(s, sc, ref, trie, model, u, 1e-4, WINDOW)
     assert amb <= cfg.batch // 4
 
@@ -282,3 +284,46 @@ def test_k_smaller_than_beam_and_beam_one(zg, mid):
         r = oracle.decode(trie, model, uu, beam, K)
         s, sc = decode_gpu(zg, idx, model, uu, beam, K, [0, 0, 0])
         check_topk(s, sc, r, trie, model, uu, 1e-4, WINDOW)
+
+
+@pytest.mark.parametrize("variants", [[0, 0, 0], [1, 0, 0], [0, 1, 0], [1, 1, 0]])
+def test_fused_equals_unfused(zg, mid, variants):
+    """The fused cluster kernel runs the same scoring and select code as the
+    stand-alone step kernels: results are bit-identical."""
+    cfg, sids, model, u, trie, ref, idx = mid
+    a = decode_gpu(zg, idx, model, u, cfg.beam, cfg.topk, variants, fused=True)
+    b = decode_gpu(zg, idx, model, u, cfg.beam, cfg.topk, variants, fused=False)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_fused_tiny_formats(zg, mode):
+    """Fused decode over all-sparse and all-dense tables, against the oracle."""
+    cfg = synth.CONFIGS["tiny"]
+    sids = synth.make_catalogue(cfg)
+    model = synth.make_model(cfg.L, cfg.V, cfg.d, cfg.w_dtype)
+    u = synth.make_requests(5, cfg.d, 2)
+    idx = zg.zg_index_build(sids, cfg.V, format_mode=mode, stream=_stream())
+    trie = oracle.Trie(sids, cfg.L, cfg.V)
+    ref = oracle.decode(trie, model, u, cfg.beam, cfg.topk)
+    s, sc = decode_gpu(zg, idx, model, u, cfg.beam, cfg.topk, [0, 0, 0], fused=True)
+    check_topk(s, sc, ref, trie, model, u, 1e-4, WINDOW)
+
+
+def test_trace_counts(zg, mid):
+    cfg, sids, model, u, trie, ref, idx = mid
+    from generative_recommendation_constrained_gb300.device import Decoder, DeviceModel
+    dm = DeviceModel(model)
+    plan = zg.zg_plan_force(idx, cfg.batch, cfg.beam, [1, 0, 0])
+    dec = Decoder(idx, plan, dm, cfg.batch, cfg.beam, cfg.topk)
+    tr = dec.trace(torch.from_numpy(u).cuda())
+    assert tr["fused_from"] == 2 and tr["ms_fused"] > 0 and tr["ms_total"] >= tr["ms_fused"]
+    st = tr["steps"]
+    assert st[0]["live_beams"] == cfg.batch and st[0]["legal_slots"] == cfg.batch * cfg.V
+    assert st[1]["live_beams"] == cfg.batch * cfg.beam
+    # oracle's candidate counts are the legal slots of the live beams
+    assert st[1]["legal_slots"] == int(ref.n_cand[:, 1].sum())
+    assert st[2]["legal_slots"] == int(ref.n_cand[:, 2].sum())
+    assert 0 < st[1]["unique_tokens"] <= cfg.V
+    s, sc = dec.out_sids.cpu().numpy(), dec.out_scores.cpu().numpy()
+    check_topk(s, sc, ref, trie, model, u, 1e-4, WINDOW)
