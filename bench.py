@@ -266,7 +266,7 @@ def run_gpu(args, cfg):
     dm = DeviceModel(model, dev)
     u_dev = torch.from_numpy(u).to(dev)
     plan = zg.zg_tune(idx, dm.struct, torch.from_numpy(warm_u).to(dev), B, beam, K, 20, stream)
-    variants, step_ms = zg.zg_plan_describe(plan)
+    variants, step_ms, cluster_ctas, fused_ms = zg.zg_plan_describe(plan)
     dec = Decoder(idx, plan, dm, B, beam, K, dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
@@ -302,6 +302,14 @@ def run_gpu(args, cfg):
         return [a.elapsed_time(b) for a, b in ev]
 
     graph = capture(dec)
+    if args.quick:
+        # short fixed sequence for profilers: warm-up replays and a few decodes
+        times = timed(graph, args.steps, max(args.warmup, 3))
+        zg.zg_check_device_status(stream)
+        if rank == 0:
+            print(json.dumps({"quick": True, "ms_per_step": statistics.fmean(times),
+                              "plan": [int(v) for v in variants], "cluster_ctas": int(cluster_ctas)}))
+        return
     sampler = ClockSampler(local)
     t_clock0 = time.perf_counter()
     times = timed(graph, args.steps, max(args.warmup, 3))
@@ -403,6 +411,8 @@ def run_gpu(args, cfg):
             "config": {"workload": workload_desc(cfg), "global_batch": B * world, "beam": beam, "topk": K,
                        "plan": ["full" if v else "selective" for v in variants],
                        "tune_ms": [[round(float(x), 4) for x in r] for r in step_ms],
+                       "cluster_ctas": int(cluster_ctas),
+                       "tune_fused_ms": [round(float(x), 4) for x in fused_ms],
                        "l2": "flushed by a 256 MiB write before every timed step",
                        "parallelism": f"replicas x{world}: requests sharded, index replicated, no collective",
                        "index_bytes": info["bytes"], "dense_trie_bytes": info["dense_trie_bytes"]},
@@ -437,6 +447,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-requests", type=int, default=2)
+    ap.add_argument("--quick", action="store_true",
+                    help="tune, capture and replay only (a short command for profilers)")
     args = ap.parse_args(argv)
     cfg = synth.CONFIGS[args.workload]
     if args.impl == "reference":

@@ -82,7 +82,7 @@ def _load():
         "zg_index_load": [C.c_char_p, i32, vp, P(vp)],
         "zg_tune": [vp, P(zg_model), vp, i32, i32, i32, i32, vp, P(vp)],
         "zg_plan_force": [vp, i32, i32, vp, P(vp)],
-        "zg_plan_describe": [vp, vp, vp],
+        "zg_plan_describe": [vp, vp, vp, vp, vp],
         "zg_plan_set_fusion": [vp, i32],
         "zg_decode_workspace_size": [vp, vp, P(zg_model), i32, i32, i32, P(sz)],
         "zg_decode": [vp, vp, P(zg_model), vp, i32, i32, i32, vp, vp, vp, sz, vp],
@@ -233,10 +233,13 @@ def zg_tune(idx: Index, model: zg_model, warm_u, B: int, beam: int, K: int, reps
 
 
 def zg_plan_describe(plan: Plan):
+    """(variant [L], step_ms [L, 2], cluster_ctas, fused_ms [5])."""
     v = np.zeros(plan.L, np.uint8)
     ms = np.zeros((plan.L, 2), np.float32)
-    _check(lib.zg_plan_describe(plan, v.ctypes.data, ms.ctypes.data))
-    return v, ms
+    g = C.c_int32(0)
+    fms = np.zeros(5, np.float32)
+    _check(lib.zg_plan_describe(plan, v.ctypes.data, ms.ctypes.data, C.byref(g), fms.ctypes.data))
+    return v, ms, g.value, fms
 
 
 def zg_decode_workspace_size(idx: Index | None, plan: Plan | None, model: zg_model, B: int, beam: int,
@@ -281,5 +284,8 @@ def zg_decode_trace(idx: Index | None, plan: Plan | None, model: zg_model, u, B:
     return {"fused_from": t.fused_from, "ms_fused": t.ms_fused, "ms_total": t.ms_total, "steps": steps}
 
 
-def zg_plan_set_fusion(plan: Plan, enable: bool):
-    _check(lib.zg_plan_set_fusion(plan, 1 if enable else 0))
+def zg_plan_set_fusion(plan: Plan, cluster_ctas):
+    """cluster_ctas: 0 (stand-alone step kernels) or 1, 2, 4, 8, 16; True = 8."""
+    if cluster_ctas is True:
+        cluster_ctas = 8
+    _check(lib.zg_plan_set_fusion(plan, int(cluster_ctas)))

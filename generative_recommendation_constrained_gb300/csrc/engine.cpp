@@ -268,7 +268,7 @@ zg_status prepare(const zg_index* idx, const zg_plan* plan, const zg_model* mode
   return get_status_ptr(&r->status);
 }
 
-constexpr int kClusterCTAs = 8;  // CTAs of the fused kernel's cluster (one cluster per request)
+constexpr int kClusterCTAs = 8;  // default CTAs of the fused kernel's cluster (one cluster per request)
 
 int variant_of(const Run& r, const zg_plan* plan, int s) {
   return !r.idx ? ZG_FULL : (plan ? plan->variant[s - 1] : ZG_SELECTIVE);
@@ -294,7 +294,8 @@ zg_status decode_steps(const Run& r, const zg_plan* plan, cudaStream_t st, cudaE
     StepLaunch steps[ZG_MAX_STEPS];
     for (int s = 1; s <= r.m.L; ++s) steps[s - 1] = make_launch(r, s, ZG_SELECTIVE);
     if (fuse_ev) cudaEventRecord(fuse_ev[0], st);
-    cudaError_t e = launch_decode_cluster(steps, s0, r.m.L, kClusterCTAs, st);
+    const int G = plan ? plan->fused : kClusterCTAs;
+    cudaError_t e = launch_decode_cluster(steps, s0, r.m.L, G, st);
     if (e != cudaSuccess) return cuda_fail(e, "fused cluster decode launch");
     if (fuse_ev) cudaEventRecord(fuse_ev[1], st);
   }
@@ -339,18 +340,24 @@ zg_status zg_plan_force(const zg_index* idx, int32_t B, int32_t beam, const uint
   return ZG_OK;
 }
 
-zg_status zg_plan_describe(const zg_plan* plan, uint8_t* variant, float* step_ms) {
+zg_status zg_plan_describe(const zg_plan* plan, uint8_t* variant, float* step_ms, int32_t* cluster_ctas,
+                           float* fused_ms) {
   if (!plan) return fail(ZG_ERR_INVALID_ARG, "zg_plan_describe: plan is NULL");
   if (variant) std::memcpy(variant, plan->variant.data(), plan->L);
   if (step_ms) std::memcpy(step_ms, plan->step_ms.data(), plan->step_ms.size() * sizeof(float));
+  if (cluster_ctas) *cluster_ctas = plan->fused;
+  if (fused_ms) std::memcpy(fused_ms, plan->fused_ms, sizeof(plan->fused_ms));
   return ZG_OK;
 }
 
 void zg_plan_free(zg_plan* plan) { delete plan; }
 
-zg_status zg_plan_set_fusion(zg_plan* plan, int32_t enable) {
+zg_status zg_plan_set_fusion(zg_plan* plan, int32_t cluster_ctas) {
   if (!plan) return fail(ZG_ERR_INVALID_ARG, "zg_plan_set_fusion: plan is NULL");
-  plan->fused = enable ? 1 : 0;
+  if (cluster_ctas != 0 && cluster_ctas != 1 && cluster_ctas != 2 && cluster_ctas != 4 && cluster_ctas != 8 &&
+      cluster_ctas != 16)
+    return fail(ZG_ERR_INVALID_ARG, "zg_plan_set_fusion: cluster_ctas must be 0, 1, 2, 4, 8 or 16");
+  plan->fused = cluster_ctas;
   return ZG_OK;
 }
 
@@ -479,6 +486,43 @@ zg_status zg_tune(const zg_index* idx, const zg_model* model, const float* warm_
     if (st != ZG_OK) break;
     plan->variant[step - 1] = (uint8_t)best_v;
     st = run_step(r, step, best_v, s);  // advance the state with the kept variant
+  }
+  // fused suffix: time each cluster size on the state entering it (the prefix
+  // steps are re-run, untimed, before every launch because the fused kernel
+  // reuses the state buffers)
+  if (st == ZG_OK) {
+    const int s0 = fused_from(r, plan);
+    if (s0 <= m.L) {
+      StepLaunch steps[ZG_MAX_STEPS];
+      for (int step = 1; step <= m.L; ++step) steps[step - 1] = make_launch(r, step, ZG_SELECTIVE);
+      const int sizes[5] = {1, 2, 4, 8, 16};
+      float best = INFINITY;
+      for (int gi = 0; gi < 5 && st == ZG_OK; ++gi) {
+        float sum = 0.f;
+        bool ok = true;
+        for (int i = 0; i < reps + 2 && ok; ++i) {
+          for (int step = 1; step < s0 && st == ZG_OK; ++step) st = run_step(r, step, plan->variant[step - 1], s);
+          if (st != ZG_OK) break;
+          cudaEventRecord(ev[0], s);
+          e = launch_decode_cluster(steps, s0, m.L, sizes[gi], s);
+          cudaEventRecord(ev[1], s);
+          if (e != cudaSuccess || cudaEventSynchronize(ev[1]) != cudaSuccess) {
+            ok = false;  // this cluster size cannot be scheduled here
+            cudaGetLastError();
+            break;
+          }
+          float ms = 0.f;
+          cudaEventElapsedTime(&ms, ev[0], ev[1]);
+          if (i >= 2) sum += ms;
+        }
+        if (st != ZG_OK) break;
+        plan->fused_ms[gi] = ok ? sum / reps : -1.f;
+        if (ok && sum / reps < best) {
+          best = sum / reps;
+          plan->fused = sizes[gi];
+        }
+      }
+    }
   }
   if (st == ZG_OK && (e = cudaStreamSynchronize(s)) != cudaSuccess) st = cuda_fail(e, "zg_tune: synchronise");
   cleanup();

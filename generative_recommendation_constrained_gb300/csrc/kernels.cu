@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(kClusterThreads, 2) k_decode_cluster(const __g
       beam_lse<NT>(a, q, bt);
       __syncthreads();
       const int n = cta_select<NT>(a, q, bt, sw, keys, A.cap);
-      for (int i = threadIdx.x; i < a.keep; i += NT) write_survivor(a, q, bt, sw, i, n);
+      write_survivors<NT>(a, q, bt, sw, n);
     }
     cl.sync();  // next beams visible to every CTA of the cluster
   }
@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(kSelThreads) k_select(const __grid_constant__ 
   beam_lse<kSelThreads>(a, q, bt);
   __syncthreads();
   const int n = cta_select<kSelThreads>(a, q, bt, sw, keys, kSelCap);
-  for (int i = threadIdx.x; i < a.keep; i += kSelThreads) write_survivor(a, q, bt, sw, i, n);
+  write_survivors<kSelThreads>(a, q, bt, sw, n);
 }
 
 // Tracing: counts of the work a step does, for roofline accounting.
@@ -320,6 +320,7 @@ cudaError_t launch_cluster_vpl(const MegaArgs& A, int B, int G, cudaStream_t st)
   static bool attr_done = false;  // per instantiation
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }

@@ -578,62 +578,72 @@ __device__ int cta_select(const StepLaunch& a, int q, BeamTab& bt, SelWork& sw, 
   return keep_n;
 }
 
-// Write survivor i (< n) of the sorted winners, or a dead/padding row.
-__device__ __forceinline__ void write_survivor(const StepLaunch& a, int q, const BeamTab& bt, const SelWork& sw, int i,
-                                               int n) {
+// Write the survivors (sorted winners) of request q, one warp per survivor:
+// the next beams (parent, token, next-step row, score) or, at the last step,
+// the output SIDs by following parent indices back; rows beyond n are dead
+// beams / padding.  On dense steps the next-step row is the row's first entry
+// plus the token's rank among the row's legal tokens (a warp popcount).
+template <int NT>
+__device__ void write_survivors(const StepLaunch& a, int q, const BeamTab& bt, const SelWork& sw, int n) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int s = a.s;
   const size_t BW = (size_t)a.B * a.beam;
   const bool sparse_slots = (a.mode == kSelSparse || a.mode == kFullSparse);
-  if (i < n) {
-    const unsigned long long w = sw.win[i];
-    const uint32_t key = (uint32_t)(w >> 32);
-    const int c = (int)(0xFFFFFFFFu - (uint32_t)(w & 0xFFFFFFFFu));
-    const int k = upper_find(bt.start, a.Wc, c);
-    const int j = c - bt.start[k];
-    const float score = ord2f(key);
-    int t;
-    uint32_t nrow = 0;
-    if (sparse_slots) {
-      t = a.tab.col[bt.rp[k] + j];
-      nrow = bt.rp[k] + (uint32_t)j;
-    } else {
-      t = j;
-      if (a.mode != kUncon) {
-        const uint32_t* bm = a.tab.bitmap + (size_t)bt.row[k] * a.tab.words;
-        uint32_t rank = 0;
-        for (int wd = 0; wd < (t >> 5); ++wd) rank += __popc(bm[wd]);
-        rank += __popc(bm[t >> 5] & ((1u << (t & 31)) - 1u));
-        nrow = bt.rp[k] + rank;
+  for (int i = warp; i < a.keep; i += NT / 32) {
+    if (i < n) {
+      const unsigned long long w = sw.win[i];
+      const uint32_t key = (uint32_t)(w >> 32);
+      const int c = (int)(0xFFFFFFFFu - (uint32_t)(w & 0xFFFFFFFFu));
+      const int k = upper_find(bt.start, a.Wc, c);
+      const int j = c - bt.start[k];
+      int t;
+      uint32_t nrow = 0;
+      if (sparse_slots) {
+        t = a.tab.col[bt.rp[k] + j];
+        nrow = bt.rp[k] + (uint32_t)j;
+      } else {
+        t = j;
+        if (a.mode != kUncon) {
+          const uint32_t* bm = a.tab.bitmap + (size_t)bt.row[k] * a.tab.words;
+          uint32_t rank = 0;
+          for (int wd = lane; wd < (t >> 5); wd += 32) rank += __popc(bm[wd]);
+          if (lane == 0) rank += __popc(bm[t >> 5] & ((1u << (t & 31)) - 1u));
+#pragma unroll
+          for (int o = 16; o; o >>= 1) rank += __shfl_xor_sync(kFull, rank, o);
+          nrow = bt.rp[k] + rank;
+        }
       }
-    }
-    if (s < a.L) {
-      const size_t o = (size_t)q * a.beam + i;
-      if (a.row_out) a.row_out[o] = nrow;
-      a.cum_out[o] = score;
-      a.tok_hist[(size_t)(s - 1) * BW + o] = t;
-      a.par_hist[(size_t)(s - 1) * BW + o] = k;
-    } else {
-      a.out_scores[(size_t)q * a.K + i] = score;
-      int32_t* sid = a.out_sids + ((size_t)q * a.K + i) * a.L;
-      sid[a.L - 1] = t;
-      int kc = k;
-      for (int sp = a.L - 1; sp >= 1; --sp) {
-        const size_t o = (size_t)(sp - 1) * BW + (size_t)q * a.beam + kc;
-        sid[sp - 1] = a.tok_hist[o];
-        kc = a.par_hist[o];
+      if (lane != 0) continue;
+      const float score = ord2f(key);
+      if (s < a.L) {
+        const size_t o = (size_t)q * a.beam + i;
+        if (a.row_out) a.row_out[o] = nrow;
+        a.cum_out[o] = score;
+        a.tok_hist[(size_t)(s - 1) * BW + o] = t;
+        a.par_hist[(size_t)(s - 1) * BW + o] = k;
+      } else {
+        a.out_scores[(size_t)q * a.K + i] = score;
+        int32_t* sid = a.out_sids + ((size_t)q * a.K + i) * a.L;
+        sid[a.L - 1] = t;
+        int kc = k;
+        for (int sp = a.L - 1; sp >= 1; --sp) {
+          const size_t o = (size_t)(sp - 1) * BW + (size_t)q * a.beam + kc;
+          sid[sp - 1] = a.tok_hist[o];
+          kc = a.par_hist[o];
+        }
       }
-    }
-  } else {
-    if (s < a.L) {
-      const size_t o = (size_t)q * a.beam + i;
-      if (a.row_out) a.row_out[o] = kDeadRow;
-      a.cum_out[o] = -INFINITY;
-      a.tok_hist[(size_t)(s - 1) * BW + o] = 0;
-      a.par_hist[(size_t)(s - 1) * BW + o] = 0;
-    } else {
-      a.out_scores[(size_t)q * a.K + i] = -INFINITY;
-      int32_t* sid = a.out_sids + ((size_t)q * a.K + i) * a.L;
-      for (int sp = 0; sp < a.L; ++sp) sid[sp] = -1;
+    } else if (lane == 0) {
+      if (s < a.L) {
+        const size_t o = (size_t)q * a.beam + i;
+        if (a.row_out) a.row_out[o] = kDeadRow;
+        a.cum_out[o] = -INFINITY;
+        a.tok_hist[(size_t)(s - 1) * BW + o] = 0;
+        a.par_hist[(size_t)(s - 1) * BW + o] = 0;
+      } else {
+        a.out_scores[(size_t)q * a.K + i] = -INFINITY;
+        int32_t* sid = a.out_sids + ((size_t)q * a.K + i) * a.L;
+        for (int sp = 0; sp < a.L; ++sp) sid[sp] = -1;
+      }
     }
   }
 }

@@ -116,7 +116,8 @@ struct zg_index {
 
 struct zg_plan {
   int32_t L = 0, B = 0, beam = 0;
-  int32_t fused = 1;
+  int32_t fused = 8;            // CTAs per cluster of the fused kernel; 0 = no fusion
+  float fused_ms[5] = {-1, -1, -1, -1, -1};  // tuned times for 1, 2, 4, 8, 16 CTAs
   std::vector<uint8_t> variant;  // [L]
   std::vector<float> step_ms;    // [L][2]
 };

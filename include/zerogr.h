@@ -176,14 +176,19 @@ ZG_API zg_status zg_tune(const zg_index* idx, const zg_model* model, const float
 /* A plan with a fixed variant per step (variant: host uint8 [L]). */
 ZG_API zg_status zg_plan_force(const zg_index* idx, int32_t B, int32_t beam, const uint8_t* variant,
                         zg_plan** out);
-/* Whether zg_decode runs the plan's trailing run of ZG_SELECTIVE steps as one
- * fused kernel (a thread-block cluster per request, cluster barriers between
- * scoring and selection); default 1.  0 runs every step as stand-alone
- * kernels.  Results are identical either way. */
-ZG_API zg_status zg_plan_set_fusion(zg_plan* plan, int32_t enable);
-/* variant: host uint8 [L] (may be NULL); step_ms: host float [L][2] timings
- * of {SELECTIVE, FULL} from zg_tune (-1 when not timed; may be NULL). */
-ZG_API zg_status zg_plan_describe(const zg_plan* plan, uint8_t* variant, float* step_ms);
+/* How zg_decode runs the plan's trailing run of ZG_SELECTIVE steps: as one
+ * fused kernel with a thread-block cluster of cluster_ctas CTAs (1, 2, 4, 8
+ * or 16) per request and cluster barriers between scoring and selection, or
+ * (0) as stand-alone step kernels.  Default 8; zg_tune times every size and
+ * keeps the fastest.  Results are identical either way. */
+ZG_API zg_status zg_plan_set_fusion(zg_plan* plan, int32_t cluster_ctas);
+/* variant: host uint8 [L]; step_ms: host float [L][2] timings of {SELECTIVE,
+ * FULL} from zg_tune (-1 when not timed); cluster_ctas: the fused kernel's
+ * cluster size (0: not fused); fused_ms: host float [5] timings of the fused
+ * kernel with 1, 2, 4, 8, 16 CTAs a cluster (-1 when not timed or not
+ * schedulable).  Any output may be NULL. */
+ZG_API zg_status zg_plan_describe(const zg_plan* plan, uint8_t* variant, float* step_ms,
+                                  int32_t* cluster_ctas, float* fused_ms);
 ZG_API void zg_plan_free(zg_plan* plan);
 
 /* --------------------------------------------------------------- decode ---

@@ -181,7 +181,11 @@ def test_decode_argument_checks(zg):
 def test_plan_force_checks(zg):
     idx = zg.zg_index_build(tiny_catalogue(3, 16, 50, 2), 16, residency=zg.ZG_RESIDENT_HOST)
     p = zg.zg_plan_force(idx, 2, 4, [0, 1, 0])
-    v, ms = zg.zg_plan_describe(p)
-    assert list(v) == [0, 1, 0] and (ms == -1).all()
+    v, ms, g, fms = zg.zg_plan_describe(p)
+    assert list(v) == [0, 1, 0] and (ms == -1).all() and g == 8 and (fms == -1).all()
+    zg.zg_plan_set_fusion(p, 0)
+    assert zg.zg_plan_describe(p)[2] == 0
+    with pytest.raises(zg.ZgError):
+        zg.zg_plan_set_fusion(p, 3)
     with pytest.raises(zg.ZgError):
         zg.zg_plan_force(idx, 2, 4, [0, 2, 0])

@@ -136,10 +136,13 @@ def test_mid_sparse_tuned_plan(zg, mid):
     dm = DeviceModel(model)
     ud = torch.from_numpy(u).cuda()
     plan = zg.zg_tune(idx, dm.struct, ud, cfg.batch, cfg.beam, cfg.topk, 5, _stream())
-    v, ms = zg.zg_plan_describe(plan)
+    v, ms, g, fms = zg.zg_plan_describe(plan)
     assert set(v.tolist()) <= {0, 1} and (ms > 0).all()
     for st in range(cfg.L):
         assert v[st] == int(np.argmin(ms[st]))
+    if v[-1] == 0:      # a selective suffix is fused with the fastest cluster size
+        ok = fms > 0
+        assert ok.any() and g == [1, 2, 4, 8, 16][int(np.argmin(np.where(ok, fms, np.inf)))]
     s, sc = decode_gpu(zg, idx, model, u, cfg.beam, cfg.topk, plan=plan, dm=dm)
     check_topk(s, sc, ref, trie, model, u, 1e-4, WINDOW)
 
@@ -287,12 +290,13 @@ def test_k_smaller_than_beam_and_beam_one(zg, mid):
 
 
 @pytest.mark.parametrize("variants", [[0, 0, 0], [1, 0, 0], [0, 1, 0], [1, 1, 0]])
-def test_fused_equals_unfused(zg, mid, variants):
+@pytest.mark.parametrize("cluster", [1, 2, 4, 8, 16])
+def test_fused_equals_unfused(zg, mid, variants, cluster):
     """The fused cluster kernel runs the same scoring and select code as the
-    stand-alone step kernels: results are bit-identical."""
+    stand-alone step kernels: results are bit-identical for every cluster size."""
     cfg, sids, model, u, trie, ref, idx = mid
-    a = decode_gpu(zg, idx, model, u, cfg.beam, cfg.topk, variants, fused=True)
-    b = decode_gpu(zg, idx, model, u, cfg.beam, cfg.topk, variants, fused=False)
+    a = decode_gpu(zg, idx, model, u, cfg.beam, cfg.topk, variants, fused=cluster)
+    b = decode_gpu(zg, idx, model, u, cfg.beam, cfg.topk, variants, fused=0)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
