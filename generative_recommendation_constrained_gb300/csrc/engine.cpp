@@ -35,7 +35,7 @@ struct Dims {
 };
 
 struct WsLayout {
-  size_t tok_hist, par_hist, row[2], cum[2], h[2], Z, part, trace, u_stage, o_sids, o_scores, total;
+  size_t tok_hist, par_hist, row[2], cum[2], h[2], hhi, hlo, Z, part, trace, u_stage, o_sids, o_scores, total;
   size_t trace_bytes;
 };
 
@@ -56,6 +56,9 @@ WsLayout layout(const Dims& m, bool host_io) {
     w.cum[i] = take(BW * 4);
     w.h[i] = take(BW * m.d * 4);
   }
+  const size_t half_bytes = (m.w_dtype == ZG_F32) ? 0 : BW * m.d * 2;  // tensor-core operand halves
+  w.hhi = take(half_bytes);
+  w.hlo = take(half_bytes);
   size_t zf = 0, pf = 0;
   for (int s = 1; s <= m.L; ++s) {
     const size_t N = (size_t)m.B * (s == 1 ? 1 : m.beam);
@@ -234,8 +237,16 @@ zg_status run_step(const Run& r, int s, int variant, cudaStream_t st, const Step
       if (e != cudaSuccess) return cuda_fail(e, "gather-add launch");
       H = a.h_out;
     }
+    const int M = a.B * a.Wc;
+    if (a.w_dtype != ZG_F32) {
+      e = launch_split_h(H, r.ws + r.w.hhi, r.ws + r.w.hlo, (size_t)M * a.d, a.w_dtype, st);
+      if (e != cudaSuccess) return cuda_fail(e, "hidden split launch");
+    }
     if (tm) cudaEventRecord(tm->ev[1], st);
-    e = launch_full_simt(a, H, st);
+    if (a.w_dtype != ZG_F32)
+      e = launch_full_tc(r.ws + r.w.hhi, r.ws + r.w.hlo, a.W, a.Z, M, a.V, a.d, a.S, a.w_dtype, a.status, st);
+    else
+      e = launch_full_simt(a, H, st);
     if (e != cudaSuccess) return cuda_fail(e, "full projection launch");
   }
   if (tm) cudaEventRecord(tm->ev[2], st);
@@ -608,7 +619,7 @@ zg_status zg_decode_trace(const zg_index* idx, const zg_plan* plan, const zg_mod
     cudaEventElapsedTime(&g, tm.ev[0], tm.ev[1]);
     cudaEventElapsedTime(&pj, tm.ev[1], tm.ev[2]);
     cudaEventElapsedTime(&q, tm.ev[2], tm.ev[3]);
-    t.ms_gather = (v == ZG_FULL && step >= 2) ? g : 0.f;
+    t.ms_gather = (v == ZG_FULL && (step >= 2 || r.m.w_dtype != ZG_F32)) ? g : 0.f;
     t.ms_project = pj;
     t.ms_select = q;
   }

@@ -1,0 +1,336 @@
+// Full projection on the 5th-generation tensor cores (sm_103a):
+//   Z[M][ldz] = H[M][d] . W[V][d]^T, fp32 accumulation in tensor memory.
+//
+// "ZeroGR: Filtering-First Constrained Decoding for Generative
+// Recommendation" (paper-daily.com digest), section "Why computing fewer
+// scores is not automatically faster": scoring every token is one regular
+// large matrix product that GPUs execute best; steps with many legal tokens
+// score everything, then pick the legal tokens.
+//
+// W_s is bf16 or fp16; the hidden vectors are fp32.  H is split as
+// H = H_hi + H_lo with both halves in W's type, and both products are
+// accumulated into the same fp32 accumulator, so the scores agree with the
+// fp32 selective projection to ~1e-6 instead of the ~1e-3 a single rounding
+// of H would give.
+//
+// One CTA computes a 128 x 256 tile: warp 0 issues TMA loads (128-byte
+// swizzled K-major tiles) into a 3-stage shared-memory ring guarded by
+// mbarriers, warp 1 owns the tensor-memory accumulator and issues
+// tcgen05.mma from one thread, warps 2-5 read the accumulator back with
+// tcgen05.ld and store the fp32 scores.  Every wait is bounded; on expiry the
+// kernel records kStatusTimeout, drains its own copies, frees its tensor
+// memory and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "zg_internal.h"
+
+namespace zg {
+namespace {
+
+constexpr int kBM = 128, kBN = 256, kBK = 64;  // tile; kBK bf16 = 128 bytes = one swizzle row
+constexpr int kStages = 3;
+constexpr int kTileA = kBM * kBK * 2;          // 16 KiB
+constexpr int kTileB = kBN * kBK * 2;          // 32 KiB
+constexpr int kStageBytes = 2 * kTileA + kTileB;
+constexpr int kTmemCols = 256;
+constexpr int kThreads = 192;
+constexpr uint32_t kSpinLimit = 1u << 26;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+// Bounded wait for the phase with the given parity; false on expiry.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  for (uint32_t it = 0; it < kSpinLimit; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile with 128-byte swizzle:
+// rows of 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc(const void* p) {
+  const uint64_t addr = smem_u32(p);
+  uint64_t d = 0;
+  d |= (addr & 0x3FFFFull) >> 4;          // start address
+  d |= (uint64_t)(16 >> 4) << 16;         // leading byte offset (unused with swizzle)
+  d |= (uint64_t)(1024 >> 4) << 32;       // stride byte offset: 8 rows x 128 B
+  d |= (uint64_t)1 << 46;                 // descriptor version
+  d |= (uint64_t)2 << 61;                 // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: f32 accumulate, A/B of type `ab` (0 f16, 1 bf16),
+// both K-major, M = 128, N = 256.
+__device__ __forceinline__ uint32_t instr_desc(uint32_t ab) {
+  return (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(
+          tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accum)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_full_tc(const __grid_constant__ CUtensorMap map_hi, const __grid_constant__ CUtensorMap map_lo,
+              const __grid_constant__ CUtensorMap map_w, float* __restrict__ Z, int M, int V, int d, int ldz,
+              uint32_t ab_type, uint32_t* status) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // stage buffers must sit on 1024-byte boundaries (swizzle atoms)
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t full_bar[kStages], empty_bar[kStages], acc_bar;
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * kBN, m0 = blockIdx.y * kBM;
+  const int nk = (d + kBK - 1) / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], 1);
+    }
+    mbar_init(&acc_bar, 1);
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = tmem_base;
+
+  if (warp == 0 && lane == 0) {
+    // producer: TMA ring
+    int issued = 0;
+    for (int kb = 0; kb < nk; ++kb) {
+      const int st = kb % kStages;
+      if (kb >= kStages && !mbar_wait(&empty_bar[st], ((kb / kStages) - 1) & 1)) {
+        atomicOr(status, kStatusTimeout);
+        atomicExch(&abort_flag, 1);
+        break;
+      }
+      if (atomicAdd(&abort_flag, 0)) break;
+      uint8_t* sa_hi = smem + st * kStageBytes;
+      uint8_t* sa_lo = sa_hi + kTileA;
+      uint8_t* sb = sa_lo + kTileA;
+      mbar_expect_tx(&full_bar[st], kStageBytes);
+      tma_load_2d(sa_hi, &map_hi, &full_bar[st], kb * kBK, m0);
+      tma_load_2d(sa_lo, &map_lo, &full_bar[st], kb * kBK, m0);
+      tma_load_2d(sb, &map_w, &full_bar[st], kb * kBK, n0);
+      ++issued;
+    }
+    // drain: every issued stage must have landed before the CTA may exit
+    for (int kb = (issued > kStages ? issued - kStages : 0); kb < issued; ++kb)
+      mbar_wait(&full_bar[kb % kStages], (kb / kStages) & 1);
+  } else if (warp == 1 && lane == 0) {
+    // MMA issuer
+    const uint32_t idesc = instr_desc(ab_type);
+    bool ok = true;
+    for (int kb = 0; kb < nk; ++kb) {
+      const int st = kb % kStages;
+      if (!mbar_wait(&full_bar[st], (kb / kStages) & 1) || atomicAdd(&abort_flag, 0)) {
+        atomicOr(status, kStatusTimeout);
+        atomicExch(&abort_flag, 1);
+        ok = false;
+        break;
+      }
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const uint8_t* sa_hi = smem + st * kStageBytes;
+      const uint8_t* sa_lo = sa_hi + kTileA;
+      const uint8_t* sb = sa_lo + kTileA;
+#pragma unroll
+      for (int kk = 0; kk < kBK / 16; ++kk) {
+        const uint64_t bd = smem_desc(sb + kk * 32);
+        mma_f16(tmem, smem_desc(sa_hi + kk * 32), bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+        mma_f16(tmem, smem_desc(sa_lo + kk * 32), bd, idesc, 1u);
+      }
+      mma_commit(&empty_bar[st]);  // stage free once these MMAs have read it
+    }
+    (void)ok;
+    mma_commit(&acc_bar);  // arrives once every MMA issued above has completed
+  } else if (warp >= 2) {
+    // epilogue: TMEM -> registers -> Z (one row per thread)
+    const bool got = mbar_wait(&acc_bar, 0);
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (!got) {
+      if (lane == 0) atomicOr(status, kStatusTimeout);
+    } else if (!atomicAdd(&abort_flag, 0)) {
+      const int quarter = warp & 3;
+      const int row = m0 + quarter * 32 + lane;
+      const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+      for (int c0 = 0; c0 < kBN; c0 += 32) {
+        float v[32];
+        tmem_ld32(lane_addr + (uint32_t)c0, v);
+        if (row < M) {
+          float* zr = Z + (size_t)row * ldz + n0 + c0;
+          if (n0 + c0 + 32 <= V) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) *reinterpret_cast<float4*>(zr + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+          } else {
+            for (int i = 0; i < 32 && n0 + c0 + i < V; ++i) zr[i] = v[i];
+          }
+        }
+      }
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 1) {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+// H (fp32) -> H_hi + H_lo in the weights' half type.
+template <typename HT>
+__device__ __forceinline__ HT to_half(float x);
+template <>
+__device__ __forceinline__ __nv_bfloat16 to_half<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+template <>
+__device__ __forceinline__ __half to_half<__half>(float x) {
+  return __float2half_rn(x);
+}
+template <typename HT>
+__device__ __forceinline__ float from_half(HT x);
+template <>
+__device__ __forceinline__ float from_half<__nv_bfloat16>(__nv_bfloat16 x) {
+  return __bfloat162float(x);
+}
+template <>
+__device__ __forceinline__ float from_half<__half>(__half x) {
+  return __half2float(x);
+}
+
+template <typename HT>
+__global__ void __launch_bounds__(256) k_split_h(const float* __restrict__ H, HT* __restrict__ hi, HT* __restrict__ lo,
+                                                 size_t n) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const float x = H[i];
+    const HT h = to_half<HT>(x);
+    hi[i] = h;
+    lo[i] = to_half<HT>(x - from_half<HT>(h));
+  }
+}
+
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*, const cuuint64_t*,
+                              const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn() {
+  static EncodeFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  }
+  return fn;
+}
+
+// 2-D K-major map: rows x d elements of 2 bytes, box box_rows x kBK, 128B swizzle.
+bool make_map(CUtensorMap* m, const void* base, int rows, int d, int box_rows, bool bf16) {
+  EncodeFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+size_t full_tc_smem_bytes() { return (size_t)kStages * kStageBytes + 1024; }
+
+cudaError_t launch_split_h(const float* H, void* hi, void* lo, size_t n, int w_dtype, cudaStream_t st) {
+  const int blocks = (int)std::min<size_t>((n + 255) / 256, 4096);
+  if (w_dtype == ZG_BF16)
+    k_split_h<__nv_bfloat16><<<blocks, 256, 0, st>>>(H, static_cast<__nv_bfloat16*>(hi),
+                                                     static_cast<__nv_bfloat16*>(lo), n);
+  else
+    k_split_h<__half><<<blocks, 256, 0, st>>>(H, static_cast<__half*>(hi), static_cast<__half*>(lo), n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_full_tc(const void* hi, const void* lo, const void* W, float* Z, int M, int V, int d, int ldz,
+                           int w_dtype, uint32_t* status, cudaStream_t st) {
+  const bool bf16 = (w_dtype == ZG_BF16);
+  CUtensorMap mh, ml, mw;
+  if (!make_map(&mh, hi, M, d, kBM, bf16) || !make_map(&ml, lo, M, d, kBM, bf16) ||
+      !make_map(&mw, W, V, d, kBN, bf16))
+    return cudaErrorInvalidValue;
+  static bool attr_done = false;
+  const size_t smem = full_tc_smem_bytes();
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(k_full_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  dim3 grid((V + kBN - 1) / kBN, (M + kBM - 1) / kBM);
+  k_full_tc<<<grid, kThreads, smem, st>>>(mh, ml, mw, Z, M, V, d, ldz, bf16 ? 1u : 0u, status);
+  return cudaGetLastError();
+}
+
+}  // namespace zg

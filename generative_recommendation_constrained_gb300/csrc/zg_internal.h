@@ -89,6 +89,10 @@ cudaError_t launch_select(const StepLaunch& a, cudaStream_t st);
 // steps[] holds the launch description of every step (1-based s at [s-1]).
 cudaError_t launch_decode_cluster(const StepLaunch* steps, int s0, int L, int G, cudaStream_t st);
 cudaError_t status_word(uint32_t** dev_ptr);   // per-device status word address
+// tensor-core full projection (kernels_tc.cu): H = hi + lo in W's half type
+cudaError_t launch_split_h(const float* H, void* hi, void* lo, size_t n, int w_dtype, cudaStream_t st);
+cudaError_t launch_full_tc(const void* hi, const void* lo, const void* W, float* Z, int M, int V, int d, int ldz,
+                           int w_dtype, uint32_t* status, cudaStream_t st);
 // Work counts of the beams entering a step (tracing only): counters[0..3] =
 // live beams, legal slots, chunks, index bytes; mask = V-bit set of touched
 // tokens.  Both must be zeroed by the caller.

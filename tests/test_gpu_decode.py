@@ -331,3 +331,22 @@ def test_trace_counts(zg, mid):
     assert 0 < st[1]["unique_tokens"] <= cfg.V
     s, sc = dec.out_sids.cpu().numpy(), dec.out_scores.cpu().numpy()
     check_topk(s, sc, ref, trie, model, u, 1e-4, WINDOW)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_tensor_core_full_matches_selective(zg, dtype):
+    """The tensor-core full projection (hidden split into two half-precision
+    parts) gives the same scores as the fp32 selective projection to 1e-4."""
+    L, V, d = 3, 700, 96
+    sids = tiny_catalogue(L, V, 5000, 11)
+    model = synth.make_model(L, V, d, dtype, 11)
+    u = synth.make_requests(40, d, 11)          # 40 x 16 beams: several 128-row tiles, ragged
+    idx = zg.zg_index_build(sids, V, stream=_stream())
+    a_s, a_sc = decode_gpu(zg, idx, model, u, 16, 16, [0, 0, 0])
+    b_s, b_sc = decode_gpu(zg, idx, model, u, 16, 16, [1, 1, 1])
+    fin = np.isfinite(a_sc)
+    assert np.array_equal(fin, np.isfinite(b_sc))
+    assert np.max(np.abs(a_sc[fin] - b_sc[fin])) < 1e-4
+    trie = oracle.Trie(sids, L, V)
+    ref = oracle.decode(trie, model, u, 16, 16, requests=range(6))
+    check_topk(b_s, b_sc, ref, trie, model, u, 1e-4, WINDOW, requests=range(6))
