@@ -353,10 +353,10 @@ def run_gpu(args, cfg):
                 kern.append((avg["ms_gather"], [s], "k_gather_add", st["live_beams"] * cfg.d * 12, "hbm"))
         kern.append((avg["ms_select"], [s], "k_select", select_bytes(st, cfg, s), "hbm"))
     if s0 <= L:
-        fused_ms = statistics.fmean(t["ms_fused"] for t in traces)
+        fused_kernel_ms = statistics.fmean(t["ms_fused"] for t in traces)
         fb = sum(selective_bytes(steps_last[s - 1], cfg, s) + select_bytes(steps_last[s - 1], cfg, s)
                  for s in range(s0, L + 1))
-        kern.append((fused_ms, list(range(s0, L + 1)), "k_decode_cluster", fb, "hbm"))
+        kern.append((fused_kernel_ms, list(range(s0, L + 1)), "k_decode_cluster", fb, "hbm"))
     kern.sort(key=lambda x: -x[0])
     top_ms, top_steps, top_name, alg, bound = kern[0]
     if bound == "hbm":

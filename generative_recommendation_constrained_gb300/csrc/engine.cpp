@@ -219,6 +219,8 @@ StepLaunch make_launch(const Run& r, int s, int variant) {
     a.S = m.S_full;
     a.part = nullptr;
   }
+  a.zq = (int64_t)a.Wc * a.S;      // contiguous beam rows (the full projection's layout)
+  a.pq = (int64_t)a.Wc * a.nch;
   return a;
 }
 
@@ -294,6 +296,24 @@ int fused_from(const Run& r, const zg_plan* plan) {
   return s0;
 }
 
+// Launch descriptions of the fused steps s0..L.  Clusters of different
+// requests run through the steps independently, so every fused step uses one
+// per-request stride for the slots and partials (the largest of the steps).
+void fused_launches(const Run& r, int s0, StepLaunch* steps) {
+  int64_t zq = 0, pq = 0;
+  for (int s = 1; s <= r.m.L; ++s) {
+    steps[s - 1] = make_launch(r, s, ZG_SELECTIVE);
+    if (s >= s0) {
+      zq = std::max(zq, steps[s - 1].zq);
+      pq = std::max(pq, steps[s - 1].pq);
+    }
+  }
+  for (int s = s0; s <= r.m.L; ++s) {
+    steps[s - 1].zq = zq;
+    steps[s - 1].pq = pq;
+  }
+}
+
 // zg_decode's launch sequence: stand-alone steps, then the fused suffix.
 zg_status decode_steps(const Run& r, const zg_plan* plan, cudaStream_t st, cudaEvent_t* fuse_ev = nullptr) {
   const int s0 = fused_from(r, plan);
@@ -303,7 +323,7 @@ zg_status decode_steps(const Run& r, const zg_plan* plan, cudaStream_t st, cudaE
   }
   if (s0 <= r.m.L) {
     StepLaunch steps[ZG_MAX_STEPS];
-    for (int s = 1; s <= r.m.L; ++s) steps[s - 1] = make_launch(r, s, ZG_SELECTIVE);
+    fused_launches(r, s0, steps);
     if (fuse_ev) cudaEventRecord(fuse_ev[0], st);
     const int G = plan ? plan->fused : kClusterCTAs;
     cudaError_t e = launch_decode_cluster(steps, s0, r.m.L, G, st);
@@ -498,27 +518,34 @@ zg_status zg_tune(const zg_index* idx, const zg_model* model, const float* warm_
     plan->variant[step - 1] = (uint8_t)best_v;
     st = run_step(r, step, best_v, s);  // advance the state with the kept variant
   }
-  // fused suffix: time each cluster size on the state entering it (the prefix
-  // steps are re-run, untimed, before every launch because the fused kernel
-  // reuses the state buffers)
+  // Whole-decode candidates: for every split point s0, the per-step best
+  // variants before s0 and selective steps from s0 on, fused with each
+  // cluster size (or, for s0 = L+1, no fused part).  The fastest decode wins.
   if (st == ZG_OK) {
-    const int s0 = fused_from(r, plan);
-    if (s0 <= m.L) {
-      StepLaunch steps[ZG_MAX_STEPS];
-      for (int step = 1; step <= m.L; ++step) steps[step - 1] = make_launch(r, step, ZG_SELECTIVE);
-      const int sizes[5] = {1, 2, 4, 8, 16};
-      float best = INFINITY;
+    const std::vector<uint8_t> best_steps = plan->variant;
+    const int sizes[5] = {1, 2, 4, 8, 16};
+    float best_total = INFINITY;
+    std::vector<uint8_t> best_v = best_steps;
+    int best_g = 0;
+    float best_gms[5] = {-1, -1, -1, -1, -1};
+    zg_plan cand = *plan;
+    for (int s0 = 1; s0 <= m.L + 1 && st == ZG_OK; ++s0) {
+      for (int step = 1; step <= m.L; ++step)
+        cand.variant[step - 1] = step < s0 ? best_steps[step - 1] : (uint8_t)ZG_SELECTIVE;
+      if (s0 > 1 && s0 <= m.L && cand.variant[s0 - 2] == ZG_SELECTIVE) continue;  // same as a smaller s0
+      float gms[5] = {-1, -1, -1, -1, -1};
       for (int gi = 0; gi < 5 && st == ZG_OK; ++gi) {
+        if (s0 > m.L && gi > 0) break;
+        cand.fused = (s0 > m.L) ? 0 : sizes[gi];
         float sum = 0.f;
         bool ok = true;
         for (int i = 0; i < reps + 2 && ok; ++i) {
-          for (int step = 1; step < s0 && st == ZG_OK; ++step) st = run_step(r, step, plan->variant[step - 1], s);
-          if (st != ZG_OK) break;
           cudaEventRecord(ev[0], s);
-          e = launch_decode_cluster(steps, s0, m.L, sizes[gi], s);
+          st = decode_steps(r, &cand, s);
           cudaEventRecord(ev[1], s);
-          if (e != cudaSuccess || cudaEventSynchronize(ev[1]) != cudaSuccess) {
-            ok = false;  // this cluster size cannot be scheduled here
+          if (st != ZG_OK || cudaEventSynchronize(ev[1]) != cudaSuccess) {
+            ok = false;  // e.g. this cluster size cannot be scheduled
+            st = ZG_OK;
             cudaGetLastError();
             break;
           }
@@ -526,14 +553,23 @@ zg_status zg_tune(const zg_index* idx, const zg_model* model, const float* warm_
           cudaEventElapsedTime(&ms, ev[0], ev[1]);
           if (i >= 2) sum += ms;
         }
-        if (st != ZG_OK) break;
-        plan->fused_ms[gi] = ok ? sum / reps : -1.f;
-        if (ok && sum / reps < best) {
-          best = sum / reps;
-          plan->fused = sizes[gi];
+        if (!ok) continue;
+        const float avg = sum / reps;
+        if (s0 <= m.L) gms[gi] = avg;
+        if (avg < best_total) {
+          best_total = avg;
+          best_v = cand.variant;
+          best_g = cand.fused;
+          std::memcpy(best_gms, gms, sizeof gms);
         }
       }
+      if (best_g && std::equal(best_v.begin(), best_v.end(), cand.variant.begin()))
+        std::memcpy(best_gms, gms, sizeof gms);
     }
+    plan->variant = best_v;
+    plan->fused = best_g;
+    std::memcpy(plan->fused_ms, best_gms, sizeof best_gms);
+    plan->plan_ms = best_total;
   }
   if (st == ZG_OK && (e = cudaStreamSynchronize(s)) != cudaSuccess) st = cuda_fail(e, "zg_tune: synchronise");
   cleanup();

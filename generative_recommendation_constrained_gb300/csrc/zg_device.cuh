@@ -260,8 +260,8 @@ __device__ __forceinline__ void score_chunk(const StepLaunch& a, int q, int k, c
   const float e = valid ? expf(z - m) : 0.f;
   float ssum = warp_sum(e);
   ssum = __shfl_sync(kFull, ssum, 0);
-  a.Z[(size_t)b * a.S + j0 + lane] = z;
-  if (lane == 0) a.part[(size_t)b * a.nch + c] = make_float2(m, vmask ? ssum : 0.f);
+  a.Z[(size_t)q * a.zq + (size_t)k * a.S + j0 + lane] = z;
+  if (lane == 0) a.part[(size_t)q * a.pq + (size_t)k * a.nch + c] = make_float2(m, vmask ? ssum : 0.f);
 }
 
 // ---------------------------------------------------------------------------
@@ -384,14 +384,14 @@ __device__ void beam_lse(const StepLaunch& a, int q, BeamTab& bt) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int k = warp; k < a.Wc; k += NT / 32) {
     if (bt.cnt[k] == 0) continue;
-    const int b = q * a.Wc + k;
     float2 acc = make_float2(-INFINITY, 0.f);
     if (a.mode == kSelSparse || a.mode == kSelDense) {
       const int nch = (a.mode == kSelSparse) ? (bt.cnt[k] + kChunk - 1) / kChunk : a.nch;
-      for (int c = lane; c < nch; c += 32) acc = lse_combine(acc, a.part[(size_t)b * a.nch + c]);
+      const float2* pp = a.part + (size_t)q * a.pq + (size_t)k * a.nch;
+      for (int c = lane; c < nch; c += 32) acc = lse_combine(acc, pp[c]);
     } else {
       const int n = bt.cnt[k];
-      const size_t zb = (size_t)b * a.S;
+      const size_t zb = (size_t)q * a.zq + (size_t)k * a.S;
       float m = -INFINITY, sm = 0.f;
       for (int pass = 0; pass < 2; ++pass) {
         for (int j = lane; j < n; j += 32) {
@@ -421,7 +421,7 @@ __device__ void beam_lse(const StepLaunch& a, int q, BeamTab& bt) {
 __device__ __forceinline__ uint32_t cand_key(const StepLaunch& a, const BeamTab& bt, int q, int c) {
   const int k = upper_find(bt.start, a.Wc, c);
   const int j = c - bt.start[k];
-  const size_t zb = (size_t)(q * a.Wc + k) * a.S;
+  const size_t zb = (size_t)q * a.zq + (size_t)k * a.S;
   float z;
   switch (a.mode) {
     case kSelSparse:

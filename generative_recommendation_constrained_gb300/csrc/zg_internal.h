@@ -55,8 +55,12 @@ struct StepLaunch {
   int32_t K;
   DevStep tab;          // zeroed in unconstrained mode
   int32_t mode;         // SelectMode
-  int32_t S;            // slot stride of Z (selective) or V (full)
+  int32_t S;            // slot stride of a beam's row of Z (selective) or padded V (full)
   int32_t nch;          // chunks per beam (selective), else 0
+  int64_t zq;           // stride of a request's rows of Z (floats): the slots of beam k of
+                        // request q start at q*zq + k*S.  Constant across the steps a fused
+                        // kernel runs, so requests never overwrite each other's slots.
+  int64_t pq;           // stride of a request's chunk partials (float2): q*pq + k*nch + c
   // state entering the step (NULL at s = 1: one root beam, row 0, cum 0, h = u)
   const uint32_t* row_in;
   const float* cum_in;
@@ -68,8 +72,8 @@ struct StepLaunch {
   const void* W;           // W_s [V][d]
   float* h_out;            // [B*Wc][d] hidden of this step's beams, or NULL
   // scores
-  float* Z;                // [B*Wc][S]
-  float2* part;            // [B*Wc][nch] (max, sum exp) per chunk, selective only
+  float* Z;                // [B][zq]
+  float2* part;            // [B][pq] (max, sum exp) per chunk, selective only
   // outputs
   uint32_t* row_out;       // [B*beam] (s < L)
   float* cum_out;          // [B*beam]
@@ -121,7 +125,8 @@ struct zg_index {
 struct zg_plan {
   int32_t L = 0, B = 0, beam = 0;
   int32_t fused = 8;            // CTAs per cluster of the fused kernel; 0 = no fusion
-  float fused_ms[5] = {-1, -1, -1, -1, -1};  // tuned times for 1, 2, 4, 8, 16 CTAs
+  float fused_ms[5] = {-1, -1, -1, -1, -1};  // tuned decode times with 1, 2, 4, 8, 16 CTAs a cluster
+  float plan_ms = -1.f;                      // tuned decode time of the kept plan
   std::vector<uint8_t> variant;  // [L]
   std::vector<float> step_ms;    // [L][2]
 };
