@@ -314,6 +314,30 @@ void fused_launches(const Run& r, int s0, StepLaunch* steps) {
   }
 }
 
+// Tables the fused kernel prefetches into L2 at launch, in priority order,
+// up to a budget of half the L2: the output heads W_s of the fused steps,
+// their index tables, then the token tables C_{s-1} their gather-add reads.
+int prefetch_set(const Run& r, int s0, PrefetchRegion* pf) {
+  constexpr uint64_t kBudget = 64ull << 20;
+  uint64_t used = 0;
+  int n = 0;
+  auto add = [&](const void* p, uint64_t bytes) {
+    if (!p || n >= kMaxPrefetch || used + bytes > kBudget) return;
+    pf[n].ptr = p;
+    pf[n].bytes = bytes;
+    used += bytes;
+    ++n;
+  };
+  const uint64_t wrow = (uint64_t)r.m.d * (r.m.w_dtype == ZG_F32 ? 4 : 2);
+  for (int s = s0; s <= r.m.L; ++s) add(r.model->W[s - 1], wrow * r.m.V);
+  for (int s = s0; s <= r.m.L; ++s) {
+    const StepMeta& sm = r.idx->steps[s - 1];
+    add(r.idx->dev + sm.off_rowptr, sm.off_payload + sm.bytes_payload - sm.off_rowptr);
+  }
+  for (int s = std::max(s0, 2); s <= r.m.L; ++s) add(r.model->C[s - 2], (uint64_t)r.m.d * 4 * r.m.V);
+  return n;
+}
+
 // zg_decode's launch sequence: stand-alone steps, then the fused suffix.
 zg_status decode_steps(const Run& r, const zg_plan* plan, cudaStream_t st, cudaEvent_t* fuse_ev = nullptr) {
   const int s0 = fused_from(r, plan);
@@ -324,9 +348,11 @@ zg_status decode_steps(const Run& r, const zg_plan* plan, cudaStream_t st, cudaE
   if (s0 <= r.m.L) {
     StepLaunch steps[ZG_MAX_STEPS];
     fused_launches(r, s0, steps);
+    PrefetchRegion pf[kMaxPrefetch];
+    const int npf = prefetch_set(r, s0, pf);
     if (fuse_ev) cudaEventRecord(fuse_ev[0], st);
     const int G = plan ? plan->fused : kClusterCTAs;
-    cudaError_t e = launch_decode_cluster(steps, s0, r.m.L, G, st);
+    cudaError_t e = launch_decode_cluster(steps, s0, r.m.L, G, pf, npf, st);
     if (e != cudaSuccess) return cuda_fail(e, "fused cluster decode launch");
     if (fuse_ev) cudaEventRecord(fuse_ev[1], st);
   }
@@ -530,6 +556,7 @@ zg_status zg_tune(const zg_index* idx, const zg_model* model, const float* warm_
     float best_gms[5] = {-1, -1, -1, -1, -1};
     zg_plan cand = *plan;
     for (int s0 = 1; s0 <= m.L + 1 && st == ZG_OK; ++s0) {
+      bool best_here = false;
       for (int step = 1; step <= m.L; ++step)
         cand.variant[step - 1] = step < s0 ? best_steps[step - 1] : (uint8_t)ZG_SELECTIVE;
       if (s0 > 1 && s0 <= m.L && cand.variant[s0 - 2] == ZG_SELECTIVE) continue;  // same as a smaller s0
@@ -560,11 +587,10 @@ zg_status zg_tune(const zg_index* idx, const zg_model* model, const float* warm_
           best_total = avg;
           best_v = cand.variant;
           best_g = cand.fused;
-          std::memcpy(best_gms, gms, sizeof gms);
+          best_here = true;
         }
       }
-      if (best_g && std::equal(best_v.begin(), best_v.end(), cand.variant.begin()))
-        std::memcpy(best_gms, gms, sizeof gms);
+      if (best_here) std::memcpy(best_gms, gms, sizeof gms);  // every cluster size timed at this split
     }
     plan->variant = best_v;
     plan->fused = best_g;

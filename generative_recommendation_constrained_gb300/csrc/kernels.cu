@@ -32,7 +32,8 @@ namespace cg = cooperative_groups;
 constexpr int kSelThreads = 512;
 constexpr int kSelCap = 12288;       // keys staged in shared memory by k_select
 constexpr int kClusterThreads = 256;
-constexpr int kClusterCap = 16384;   // keys staged by the cluster kernel's rank-0 CTA
+constexpr int kClusterCap = 12288;   // slot scores / keys held by the cluster kernel's rank-0 CTA
+constexpr int kClusterPcap = 2048;   // chunk partials and masks held by the rank-0 CTA
 
 // ---------------------------------------------------------------------------
 // Stand-alone selective step: one warp per (beam, chunk) item, grid-stride,
@@ -64,15 +65,56 @@ __global__ void __launch_bounds__(256) k_selective(const __grid_constant__ StepL
 
 // ---------------------------------------------------------------------------
 // Cluster decode of the selective steps s0..L (all steps selective).
+//
+// Per step: every CTA builds the request's beam table, the cluster's warps
+// score its (beam, chunk) items and, when the request's candidates fit,
+// write the slot scores, chunk partials and chunk legal masks straight into
+// the rank-0 CTA's shared memory (distributed shared memory); a cluster
+// barrier publishes them; the rank-0 CTA computes the legal-only
+// log-sum-exps and keys in shared memory, selects and writes the next
+// beams; a second cluster barrier publishes those.  Larger requests go
+// through the global slot buffer instead.  At launch every CTA prefetches
+// its share of the fused steps' tables into L2 with bulk prefetches.
 // ---------------------------------------------------------------------------
 struct MegaArgs {
-  int32_t s0, L, cap, pad;
+  int32_t s0, L, cap, pcap;
+  int32_t npf, pad;
+  uint64_t pf_total;
+  PrefetchRegion pf[kMaxPrefetch];
   StepLaunch st[ZG_MAX_STEPS];
 };
 
+__device__ __forceinline__ void l2_prefetch(const MegaArgs& A) {
+  using u64 = unsigned long long;
+  const u64 total = A.pf_total;
+  if (!total) return;
+  const u64 per = ((total + gridDim.x - 1) / gridDim.x + 15ull) & ~15ull;
+  const u64 lo = (u64)blockIdx.x * per;
+  const u64 hi = total < lo + per ? total : lo + per;
+  if (lo >= hi) return;
+  u64 piece = (((hi - lo) + blockDim.x - 1) / blockDim.x + 15ull) & ~15ull;
+  if (piece < 4096ull) piece = 4096ull;
+  const u64 my_lo = lo + (u64)threadIdx.x * piece;
+  const u64 my_hi = hi < my_lo + piece ? hi : my_lo + piece;
+  u64 off = 0;
+  for (int i = 0; i < A.npf && my_lo < my_hi; ++i) {
+    const u64 rb = A.pf[i].bytes;
+    const u64 x = my_lo > off ? my_lo : off;
+    const u64 y = my_hi < off + rb ? my_hi : off + rb;
+    if (x < y) {
+      const char* p = static_cast<const char*>(A.pf[i].ptr) + (x - off);
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"((uint32_t)(y - x)) : "memory");
+    }
+    off += rb;
+  }
+}
+
 template <typename WT, int VPL>
 __global__ void __launch_bounds__(kClusterThreads, 2) k_decode_cluster(const __grid_constant__ MegaArgs A) {
-  extern __shared__ __align__(16) uint32_t keys[];
+  extern __shared__ __align__(16) uint32_t dyn[];
+  uint32_t* zsm = dyn;                                        // [cap] slot scores, then keys
+  float2* psm = reinterpret_cast<float2*>(dyn + A.cap);       // [pcap] chunk partials
+  uint32_t* msm = reinterpret_cast<uint32_t*>(psm + A.pcap);  // [pcap] chunk legal masks
   __shared__ BeamTab bt;
   __shared__ SelWork sw;
   constexpr int NT = kClusterThreads, NW = NT / 32;
@@ -81,10 +123,18 @@ __global__ void __launch_bounds__(kClusterThreads, 2) k_decode_cluster(const __g
   const int r = (int)cl.block_rank();
   const int q = blockIdx.x / G;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  l2_prefetch(A);
   for (int s = A.s0; s <= A.L; ++s) {
     const StepLaunch& a = A.st[s - 1];
     build_beam_table<NT>(a, q, bt);
     const int nitems = bt.istart[a.Wc];
+    const bool in_smem = bt.total <= A.cap && nitems <= A.pcap;
+    SlotSink sink{};
+    if (in_smem) {
+      sink.z = cl.map_shared_rank(reinterpret_cast<float*>(zsm), 0);
+      sink.part = cl.map_shared_rank(psm, 0);
+      sink.mask = cl.map_shared_rank(msm, 0);
+    }
     for (int it = r * NW + warp; it < nitems; it += G * NW) {
       const int k = upper_find(bt.istart, a.Wc, it);
       const int c = it - bt.istart[k];
@@ -93,16 +143,30 @@ __global__ void __launch_bounds__(kClusterThreads, 2) k_decode_cluster(const __g
       bs.cum = bt.cum[k];
       bs.par = bt.par[k];
       bs.tok = bt.tok[k];
-      score_chunk<WT, VPL>(a, q, k, bs, bt.rp[k], (uint32_t)bt.nleg[k], c, lane);
+      sink.flat0 = bt.start[k] + c * kChunk;
+      sink.item = it;
+      sink.cnt = bt.cnt[k];
+      score_chunk<WT, VPL>(a, q, k, bs, bt.rp[k], (uint32_t)bt.nleg[k], c, lane, in_smem ? &sink : nullptr);
     }
-    cl.sync();  // slots and partials of the whole request are now visible
+    cl.sync();  // slots and partials of the whole request are now visible to rank 0
     if (r == 0) {
-      beam_lse<NT>(a, q, bt);
-      __syncthreads();
-      const int n = cta_select<NT>(a, q, bt, sw, keys, A.cap);
-      write_survivors<NT>(a, q, bt, sw, n);
+      int n;
+      if (in_smem) {
+        beam_lse_smem<NT>(a, bt, psm);
+        __syncthreads();
+        keys_from_z<NT>(a, bt, zsm);
+        n = cta_select<NT>(a, q, bt, sw, zsm, true);
+        write_survivors<NT>(a, q, bt, sw, n, msm);
+      } else {
+        beam_lse<NT>(a, q, bt);
+        __syncthreads();
+        const bool staged = bt.total <= A.cap;
+        if (staged) stage_keys_global<NT>(a, q, bt, zsm);
+        n = cta_select<NT>(a, q, bt, sw, zsm, staged);
+        write_survivors<NT>(a, q, bt, sw, n);
+      }
     }
-    cl.sync();  // next beams visible to every CTA of the cluster
+    cl.sync();  // next beams visible to every CTA of the cluster; rank 0's buffers free again
   }
 }
 
@@ -221,7 +285,9 @@ __global__ void __launch_bounds__(kSelThreads) k_select(const __grid_constant__ 
   build_beam_table<kSelThreads>(a, q, bt);
   beam_lse<kSelThreads>(a, q, bt);
   __syncthreads();
-  const int n = cta_select<kSelThreads>(a, q, bt, sw, keys, kSelCap);
+  const bool staged = bt.total <= kSelCap;
+  if (staged) stage_keys_global<kSelThreads>(a, q, bt, keys);
+  const int n = cta_select<kSelThreads>(a, q, bt, sw, keys, staged);
   write_survivors<kSelThreads>(a, q, bt, sw, n);
 }
 
@@ -316,7 +382,7 @@ cudaError_t launch_sel_t(const StepLaunch& a, cudaStream_t st) {
 template <typename WT, int VPL>
 cudaError_t launch_cluster_vpl(const MegaArgs& A, int B, int G, cudaStream_t st) {
   auto kern = k_decode_cluster<WT, VPL>;
-  const size_t smem = (size_t)A.cap * 4;
+  const size_t smem = (size_t)A.cap * 4 + (size_t)A.pcap * 12;
   static bool attr_done = false;  // per instantiation
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -364,11 +430,19 @@ cudaError_t launch_selective(const StepLaunch& a, cudaStream_t st) {
   }
 }
 
-cudaError_t launch_decode_cluster(const StepLaunch* steps, int s0, int L, int G, cudaStream_t st) {
+cudaError_t launch_decode_cluster(const StepLaunch* steps, int s0, int L, int G, const PrefetchRegion* pf, int npf,
+                                  cudaStream_t st) {
   MegaArgs A{};
   A.s0 = s0;
   A.L = L;
   A.cap = kClusterCap;
+  A.pcap = kClusterPcap;
+  A.npf = std::min(npf, kMaxPrefetch);
+  for (int i = 0; i < A.npf; ++i) {
+    A.pf[i] = pf[i];
+    A.pf[i].bytes &= ~15ull;  // bulk prefetch sizes are multiples of 16 bytes
+    A.pf_total += A.pf[i].bytes;
+  }
   for (int s = 0; s < L; ++s) A.st[s] = steps[s];
   const StepLaunch& a = steps[L - 1];
   switch (a.w_dtype) {

@@ -148,9 +148,20 @@ __device__ __forceinline__ BeamState load_beam(const StepLaunch& a, int q, int k
 // log-sum-exp.  `row`, `rp0`, `F` are the beam's index row, first entry and
 // fan-out (checked by the caller).
 // ---------------------------------------------------------------------------
+// Destination of a chunk's scores inside the cluster: the rank-0 CTA's shared
+// memory (reached through distributed shared memory), or none (global Z).
+struct SlotSink {
+  float* z;        // z of flat candidate start[k] + j
+  float2* part;    // chunk partials, by item istart[k] + c
+  uint32_t* mask;  // chunk legal masks, by item
+  int flat0;       // flat index of the chunk's first slot
+  int item;        // item index of the chunk
+  int cnt;         // slots of the beam (flat candidates it owns)
+};
+
 template <typename WT, int VPL>
 __device__ __forceinline__ void score_chunk(const StepLaunch& a, int q, int k, const BeamState& bs, uint32_t rp0,
-                                            uint32_t F, int c, int lane) {
+                                            uint32_t F, int c, int lane, const SlotSink* sink = nullptr) {
   using VT = Vec<WT>;
   constexpr int E = VT::E;
   const int d = a.d;
@@ -260,8 +271,16 @@ __device__ __forceinline__ void score_chunk(const StepLaunch& a, int q, int k, c
   const float e = valid ? expf(z - m) : 0.f;
   float ssum = warp_sum(e);
   ssum = __shfl_sync(kFull, ssum, 0);
-  a.Z[(size_t)q * a.zq + (size_t)k * a.S + j0 + lane] = z;
-  if (lane == 0) a.part[(size_t)q * a.pq + (size_t)k * a.nch + c] = make_float2(m, vmask ? ssum : 0.f);
+  if (sink) {
+    if (j0 + lane < sink->cnt) sink->z[sink->flat0 + lane] = z;
+    if (lane == 0) {
+      sink->part[sink->item] = make_float2(m, vmask ? ssum : 0.f);
+      sink->mask[sink->item] = vmask;
+    }
+  } else {
+    a.Z[(size_t)q * a.zq + (size_t)k * a.S + j0 + lane] = z;
+    if (lane == 0) a.part[(size_t)q * a.pq + (size_t)k * a.nch + c] = make_float2(m, vmask ? ssum : 0.f);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -417,6 +436,35 @@ __device__ void beam_lse(const StepLaunch& a, int q, BeamTab& bt) {
   }
 }
 
+// Legal-only log-sum-exp of every live beam from chunk partials held in
+// shared memory by item (one warp per beam).
+template <int NT>
+__device__ void beam_lse_smem(const StepLaunch& a, BeamTab& bt, const float2* psm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int k = warp; k < a.Wc; k += NT / 32) {
+    if (bt.cnt[k] == 0) continue;
+    float2 acc = make_float2(-INFINITY, 0.f);
+    for (int c = lane; c < bt.items[k]; c += 32) acc = lse_combine(acc, psm[bt.istart[k] + c]);
+    acc = warp_lse(acc);
+    if (lane == 0) bt.lse[k] = acc.x + logf(acc.y);
+  }
+}
+
+// In place: z of flat candidate c (-inf for an empty slot) -> its key
+// (0 for an empty slot).  Same arithmetic as cand_key.
+template <int NT>
+__device__ void keys_from_z(const StepLaunch& a, const BeamTab& bt, uint32_t* zk) {
+  const int total = bt.total;
+  int c = threadIdx.x;
+  if (c >= total) return;
+  int k = upper_find(bt.start, a.Wc, c);
+  for (; c < total; c += NT) {
+    while (bt.start[k + 1] <= c) ++k;
+    const float z = __uint_as_float(zk[c]);
+    zk[c] = (z == -INFINITY) ? 0u : f2ord(bt.cum[k] + (z - bt.lse[k]));
+  }
+}
+
 // Key of flat candidate c (0 = illegal slot).
 __device__ __forceinline__ uint32_t cand_key(const StepLaunch& a, const BeamTab& bt, int q, int c) {
   const int k = upper_find(bt.start, a.Wc, c);
@@ -448,14 +496,45 @@ __device__ __forceinline__ uint32_t cand_key(const StepLaunch& a, const BeamTab&
 // indices, and the winners are bitonic-sorted by (score desc, flat asc).
 // Leaves sw.win[0..n) sorted; returns n = min(keep, legal candidates).
 // ---------------------------------------------------------------------------
+// Stage the keys of every candidate in shared memory (four independent
+// candidates a thread in flight).
 template <int NT>
-__device__ int cta_select(const StepLaunch& a, int q, BeamTab& bt, SelWork& sw, uint32_t* keys, int cap) {
+__device__ void stage_keys_global(const StepLaunch& a, int q, const BeamTab& bt, uint32_t* keys) {
+  const int total = bt.total;
+  for (int c0 = threadIdx.x; c0 < total; c0 += 4 * NT) {
+    uint32_t kk[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c = c0 + u * NT;
+      kk[u] = (c < total) ? cand_key(a, bt, q, c) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (c0 + u * NT < total) keys[c0 + u * NT] = kk[u];
+  }
+}
+
+// Descending bitonic sort of up to 32 values held one a lane (warp-wide).
+__device__ __forceinline__ unsigned long long warp_sort_desc(unsigned long long v, int lane) {
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const unsigned long long o = __shfl_xor_sync(kFull, v, j);
+      const bool desc = (lane & k) == 0;
+      const bool lower = (lane & j) == 0;
+      const bool take_max = (lower == desc);
+      v = take_max ? (v > o ? v : o) : (v < o ? v : o);
+    }
+  }
+  return v;
+}
+
+template <int NT>
+__device__ int cta_select(const StepLaunch& a, int q, BeamTab& bt, SelWork& sw, uint32_t* keys, bool staged) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int total = bt.total;
   const int keep_n = min(a.keep, bt.nlegal);
-  const bool staged = total <= cap;
-  if (staged)
-    for (int c = tid; c < total; c += NT) keys[c] = cand_key(a, bt, q, c);
   if (tid == 0) {
     sw.nwin = 0;
     sw.prefix = 0;
@@ -555,6 +634,14 @@ __device__ int cta_select(const StepLaunch& a, int q, BeamTab& bt, SelWork& sw, 
     }
   }
   __syncthreads();
+  if (keep_n <= 32) {
+    if (warp == 0) {
+      const unsigned long long v = warp_sort_desc(lane < keep_n ? sw.win[lane] : 0ull, lane);
+      if (lane < keep_n) sw.win[lane] = v;
+    }
+    __syncthreads();
+    return keep_n;
+  }
   int P = 1;
   while (P < keep_n) P <<= 1;
   for (int i = keep_n + tid; i < P; i += NT) sw.win[i] = 0ull;
@@ -578,18 +665,19 @@ __device__ int cta_select(const StepLaunch& a, int q, BeamTab& bt, SelWork& sw, 
   return keep_n;
 }
 
-// Write the survivors (sorted winners) of request q, one warp per survivor:
+// Write the survivors (sorted winners) of request q, one thread a survivor:
 // the next beams (parent, token, next-step row, score) or, at the last step,
 // the output SIDs by following parent indices back; rows beyond n are dead
 // beams / padding.  On dense steps the next-step row is the row's first entry
-// plus the token's rank among the row's legal tokens (a warp popcount).
+// plus the token's rank among the row's legal tokens: from the chunk legal
+// masks in shared memory when given (cluster kernel), else from the bitmap.
 template <int NT>
-__device__ void write_survivors(const StepLaunch& a, int q, const BeamTab& bt, const SelWork& sw, int n) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+__device__ void write_survivors(const StepLaunch& a, int q, const BeamTab& bt, const SelWork& sw, int n,
+                                const uint32_t* msm = nullptr) {
   const int s = a.s;
   const size_t BW = (size_t)a.B * a.beam;
   const bool sparse_slots = (a.mode == kSelSparse || a.mode == kFullSparse);
-  for (int i = warp; i < a.keep; i += NT / 32) {
+  for (int i = threadIdx.x; i < a.keep; i += NT) {
     if (i < n) {
       const unsigned long long w = sw.win[i];
       const uint32_t key = (uint32_t)(w >> 32);
@@ -604,16 +692,19 @@ __device__ void write_survivors(const StepLaunch& a, int q, const BeamTab& bt, c
       } else {
         t = j;
         if (a.mode != kUncon) {
-          const uint32_t* bm = a.tab.bitmap + (size_t)bt.row[k] * a.tab.words;
           uint32_t rank = 0;
-          for (int wd = lane; wd < (t >> 5); wd += 32) rank += __popc(bm[wd]);
-          if (lane == 0) rank += __popc(bm[t >> 5] & ((1u << (t & 31)) - 1u));
-#pragma unroll
-          for (int o = 16; o; o >>= 1) rank += __shfl_xor_sync(kFull, rank, o);
+          if (msm) {
+            const uint32_t* mk = msm + bt.istart[k];
+            for (int wd = 0; wd < (t >> 5); ++wd) rank += __popc(mk[wd]);
+            rank += __popc(mk[t >> 5] & ((1u << (t & 31)) - 1u));
+          } else {
+            const uint32_t* bm = a.tab.bitmap + (size_t)bt.row[k] * a.tab.words;
+            for (int wd = 0; wd < (t >> 5); ++wd) rank += __popc(bm[wd]);
+            rank += __popc(bm[t >> 5] & ((1u << (t & 31)) - 1u));
+          }
           nrow = bt.rp[k] + rank;
         }
       }
-      if (lane != 0) continue;
       const float score = ord2f(key);
       if (s < a.L) {
         const size_t o = (size_t)q * a.beam + i;
@@ -632,7 +723,7 @@ __device__ void write_survivors(const StepLaunch& a, int q, const BeamTab& bt, c
           kc = a.par_hist[o];
         }
       }
-    } else if (lane == 0) {
+    } else {
       if (s < a.L) {
         const size_t o = (size_t)q * a.beam + i;
         if (a.row_out) a.row_out[o] = kDeadRow;

@@ -89,9 +89,17 @@ cudaError_t launch_selective(const StepLaunch& a, cudaStream_t st);
 cudaError_t launch_gather_add(const StepLaunch& a, float* H, cudaStream_t st);
 cudaError_t launch_full_simt(const StepLaunch& a, const float* H, cudaStream_t st);
 cudaError_t launch_select(const StepLaunch& a, cudaStream_t st);
+// A device region the fused kernel prefetches into L2 (16-byte aligned).
+struct PrefetchRegion {
+  const void* ptr;
+  uint64_t bytes;
+};
+constexpr int kMaxPrefetch = 24;
 // Steps s0..L (all selective) in one cluster kernel, G CTAs per request;
-// steps[] holds the launch description of every step (1-based s at [s-1]).
-cudaError_t launch_decode_cluster(const StepLaunch* steps, int s0, int L, int G, cudaStream_t st);
+// steps[] holds the launch description of every step (1-based s at [s-1]);
+// pf[] lists the tables to prefetch into L2 at launch.
+cudaError_t launch_decode_cluster(const StepLaunch* steps, int s0, int L, int G, const PrefetchRegion* pf, int npf,
+                                  cudaStream_t st);
 cudaError_t status_word(uint32_t** dev_ptr);   // per-device status word address
 // tensor-core full projection (kernels_tc.cu): H = hi + lo in W's half type
 cudaError_t launch_split_h(const float* H, void* hi, void* lo, size_t n, int w_dtype, cudaStream_t st);
