@@ -32,7 +32,7 @@ namespace cg = cooperative_groups;
 constexpr int kSelThreads = 512;
 constexpr int kSelCap = 12288;       // keys staged in shared memory by k_select
 constexpr int kClusterThreads = 256;
-constexpr int kClusterCap = 12288;   // slot scores / keys held by the cluster kernel's rank-0 CTA
+constexpr int kClusterCap = 11264;   // slot scores / keys held by the cluster kernel's rank-0 CTA
 constexpr int kClusterPcap = 2048;   // chunk partials and masks held by the rank-0 CTA
 
 // ---------------------------------------------------------------------------
@@ -115,9 +115,9 @@ __global__ void __launch_bounds__(kClusterThreads, 2) k_decode_cluster(const __g
   uint32_t* zsm = dyn;                                        // [cap] slot scores, then keys
   float2* psm = reinterpret_cast<float2*>(dyn + A.cap);       // [pcap] chunk partials
   uint32_t* msm = reinterpret_cast<uint32_t*>(psm + A.pcap);  // [pcap] chunk legal masks
-  __shared__ BeamTab bt;
-  __shared__ SelWork sw;
   constexpr int NT = kClusterThreads, NW = NT / 32;
+  __shared__ BeamTab bt;
+  __shared__ SelWorkT<NW> sw;
   cg::cluster_group cl = cg::this_cluster();
   const int G = (int)cl.num_blocks();
   const int r = (int)cl.block_rank();
@@ -152,17 +152,15 @@ __global__ void __launch_bounds__(kClusterThreads, 2) k_decode_cluster(const __g
     if (r == 0) {
       int n;
       if (in_smem) {
-        beam_lse_smem<NT>(a, bt, psm);
-        __syncthreads();
-        keys_from_z<NT>(a, bt, zsm);
-        n = cta_select<NT>(a, q, bt, sw, zsm, true);
+        beam_lse_sel<NT>(a, q, bt, psm);
+        n = cta_select<NT>(a, q, bt, sw, zsm, kZStaged);  // its first barrier publishes the lse
         write_survivors<NT>(a, q, bt, sw, n, msm);
       } else {
         beam_lse<NT>(a, q, bt);
         __syncthreads();
         const bool staged = bt.total <= A.cap;
         if (staged) stage_keys_global<NT>(a, q, bt, zsm);
-        n = cta_select<NT>(a, q, bt, sw, zsm, staged);
+        n = cta_select<NT>(a, q, bt, sw, zsm, staged ? kKeysStaged : kGlobal);
         write_survivors<NT>(a, q, bt, sw, n);
       }
     }
@@ -280,14 +278,14 @@ __global__ void __launch_bounds__(256) k_full_simt(const float* __restrict__ H, 
 __global__ void __launch_bounds__(kSelThreads) k_select(const __grid_constant__ StepLaunch a) {
   extern __shared__ __align__(16) uint32_t keys[];
   __shared__ BeamTab bt;
-  __shared__ SelWork sw;
+  __shared__ SelWorkT<kSelThreads / 32> sw;
   const int q = blockIdx.x;
   build_beam_table<kSelThreads>(a, q, bt);
   beam_lse<kSelThreads>(a, q, bt);
   __syncthreads();
   const bool staged = bt.total <= kSelCap;
   if (staged) stage_keys_global<kSelThreads>(a, q, bt, keys);
-  const int n = cta_select<kSelThreads>(a, q, bt, sw, keys, staged);
+  const int n = cta_select<kSelThreads>(a, q, bt, sw, keys, staged ? kKeysStaged : kGlobal);
   write_survivors<kSelThreads>(a, q, bt, sw, n);
 }
 

@@ -301,8 +301,9 @@ struct BeamTab {
   int total, nlegal;
 };
 
-struct SelWork {
-  uint32_t hist[256];
+template <int NW>
+struct SelWorkT {
+  uint32_t whist[NW][256];  // private radix histogram of each warp
   unsigned long long win[ZG_MAX_BEAM];
   int warp_tot[32];
   uint32_t prefix, prefmask;
@@ -396,19 +397,49 @@ __device__ void build_beam_table(const StepLaunch& a, int q, BeamTab& bt) {
   __syncthreads();
 }
 
+// Legal-only log-sum-exp of every live beam from its selective chunk
+// partials (m_c, s_c): lse = M + log(sum_c s_c exp(m_c - M)), M = max_c m_c.
+// Eight lanes a beam (four beams a warp at once), two passes over the
+// partials, width-8 shuffle reductions.  Partials come from shared memory
+// by item (psm) or from the global partial buffer (psm == nullptr).
+template <int NT>
+__device__ void beam_lse_sel(const StepLaunch& a, int q, BeamTab& bt, const float2* psm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int sub = lane >> 3, sl = lane & 7;
+  for (int k0 = warp * 4; k0 < a.Wc; k0 += (NT / 32) * 4) {
+    const int k = k0 + sub;
+    const bool live = (k < a.Wc) && bt.cnt[k] > 0;
+    const int n = live ? bt.items[k] : 0;
+    const float2* pp = psm ? psm + (live ? bt.istart[k] : 0)
+                           : a.part + (size_t)q * a.pq + (size_t)(live ? k : 0) * a.nch;
+    float m = -INFINITY;
+    for (int c = sl; c < n; c += 8) m = fmaxf(m, pp[c].x);
+#pragma unroll
+    for (int o = 4; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+    float sum = 0.f;
+    for (int c = sl; c < n; c += 8) {
+      const float2 p = pp[c];
+      if (p.y > 0.f) sum += p.y * expf(p.x - m);
+    }
+#pragma unroll
+    for (int o = 4; o; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
+    if (live && sl == 0) bt.lse[k] = m + logf(sum);
+  }
+}
+
 // Legal-only log-sum-exp of every live beam (one warp per beam): from the
 // selective chunk partials, or by two passes over the full scores.
 template <int NT>
 __device__ void beam_lse(const StepLaunch& a, int q, BeamTab& bt) {
+  if (a.mode == kSelSparse || a.mode == kSelDense) {
+    beam_lse_sel<NT>(a, q, bt, nullptr);
+    return;
+  }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int k = warp; k < a.Wc; k += NT / 32) {
     if (bt.cnt[k] == 0) continue;
     float2 acc = make_float2(-INFINITY, 0.f);
-    if (a.mode == kSelSparse || a.mode == kSelDense) {
-      const int nch = (a.mode == kSelSparse) ? (bt.cnt[k] + kChunk - 1) / kChunk : a.nch;
-      const float2* pp = a.part + (size_t)q * a.pq + (size_t)k * a.nch;
-      for (int c = lane; c < nch; c += 32) acc = lse_combine(acc, pp[c]);
-    } else {
+    {
       const int n = bt.cnt[k];
       const size_t zb = (size_t)q * a.zq + (size_t)k * a.S;
       float m = -INFINITY, sm = 0.f;
@@ -433,35 +464,6 @@ __device__ void beam_lse(const StepLaunch& a, int q, BeamTab& bt) {
     }
     acc = warp_lse(acc);
     if (lane == 0) bt.lse[k] = acc.x + logf(acc.y);
-  }
-}
-
-// Legal-only log-sum-exp of every live beam from chunk partials held in
-// shared memory by item (one warp per beam).
-template <int NT>
-__device__ void beam_lse_smem(const StepLaunch& a, BeamTab& bt, const float2* psm) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int k = warp; k < a.Wc; k += NT / 32) {
-    if (bt.cnt[k] == 0) continue;
-    float2 acc = make_float2(-INFINITY, 0.f);
-    for (int c = lane; c < bt.items[k]; c += 32) acc = lse_combine(acc, psm[bt.istart[k] + c]);
-    acc = warp_lse(acc);
-    if (lane == 0) bt.lse[k] = acc.x + logf(acc.y);
-  }
-}
-
-// In place: z of flat candidate c (-inf for an empty slot) -> its key
-// (0 for an empty slot).  Same arithmetic as cand_key.
-template <int NT>
-__device__ void keys_from_z(const StepLaunch& a, const BeamTab& bt, uint32_t* zk) {
-  const int total = bt.total;
-  int c = threadIdx.x;
-  if (c >= total) return;
-  int k = upper_find(bt.start, a.Wc, c);
-  for (; c < total; c += NT) {
-    while (bt.start[k + 1] <= c) ++k;
-    const float z = __uint_as_float(zk[c]);
-    zk[c] = (z == -INFINITY) ? 0u : f2ord(bt.cum[k] + (z - bt.lse[k]));
   }
 }
 
@@ -530,8 +532,25 @@ __device__ __forceinline__ unsigned long long warp_sort_desc(unsigned long long 
   return v;
 }
 
-template <int NT>
-__device__ int cta_select(const StepLaunch& a, int q, BeamTab& bt, SelWork& sw, uint32_t* keys, bool staged) {
+// Where cta_select finds the candidates' keys.
+enum KeySrc { kKeysStaged = 0, kZStaged = 1, kGlobal = 2 };
+
+// ---------------------------------------------------------------------------
+// CTA-level select of the keep best legal candidates of request q.
+//   kKeysStaged: keys[] holds every candidate's key;
+//   kZStaged:    keys[] holds every candidate's z (-inf for an empty slot);
+//                the first radix pass turns them into keys in place;
+//   kGlobal:     keys are recomputed from the global slot buffer each pass.
+// 8-bit radix passes from the top byte narrow the threshold key (stopping as
+// soon as the threshold bin holds exactly the remainder); each warp counts
+// into a private histogram.  Winners above the threshold are collected,
+// threshold ties go to the lowest flat slot indices, and the winners are
+// sorted by (score desc, flat asc).  Leaves sw.win[0..n) sorted; returns
+// n = min(keep, legal candidates).
+// ---------------------------------------------------------------------------
+template <int NT, typename SW>
+__device__ int cta_select(const StepLaunch& a, int q, BeamTab& bt, SW& sw, uint32_t* keys, KeySrc src) {
+  constexpr int NW = NT / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int total = bt.total;
   const int keep_n = min(a.keep, bt.nlegal);
@@ -546,28 +565,51 @@ __device__ int cta_select(const StepLaunch& a, int q, BeamTab& bt, SelWork& sw, 
   }
   __syncthreads();
   if (keep_n == 0) return 0;
+  bool z_pending = (src == kZStaged);
+  if (sw.all_eq && z_pending) {
+    // everything is kept: keys are still needed for the order
+    for (int c = tid; c < total; c += NT) {
+      const int k = upper_find(bt.start, a.Wc, c);
+      const float z = __uint_as_float(keys[c]);
+      keys[c] = (z == -INFINITY) ? 0u : f2ord(bt.cum[k] + (z - bt.lse[k]));
+    }
+    z_pending = false;
+  }
   for (int shift = 24; shift >= 0 && !sw.all_eq; shift -= 8) {
-    for (int i = tid; i < 256; i += NT) sw.hist[i] = 0;
+    for (int i = tid; i < NW * 256; i += NT) (&sw.whist[0][0])[i] = 0u;
     __syncthreads();
     const uint32_t pm = sw.prefmask, pv = sw.prefix;
-    for (int c0 = 0; c0 < total; c0 += NT) {
-      const int c = c0 + tid;
-      int dgt = -1;
-      if (c < total) {
-        const uint32_t key = staged ? keys[c] : cand_key(a, bt, q, c);
-        if (key && (key & pm) == pv) dgt = (int)((key >> shift) & 255u);
+    uint32_t* wh = sw.whist[warp];
+    if (z_pending) {
+      int c = tid, k = (c < total) ? upper_find(bt.start, a.Wc, c) : 0;
+      for (; c < total; c += NT) {
+        while (bt.start[k + 1] <= c) ++k;
+        const float z = __uint_as_float(keys[c]);
+        const uint32_t key = (z == -INFINITY) ? 0u : f2ord(bt.cum[k] + (z - bt.lse[k]));
+        keys[c] = key;
+        if (key) atomicAdd(&wh[key >> 24], 1u);
       }
-      const unsigned act = __activemask();
-      const unsigned peers = __match_any_sync(act, dgt);
-      if (dgt >= 0 && lane == __ffs(peers) - 1) atomicAdd(&sw.hist[dgt], (uint32_t)__popc(peers));
+    } else {
+      for (int c = tid; c < total; c += NT) {
+        const uint32_t key = (src == kGlobal) ? cand_key(a, bt, q, c) : keys[c];
+        if (key && (key & pm) == pv) atomicAdd(&wh[(key >> shift) & 255u], 1u);
+      }
     }
+    z_pending = false;
     __syncthreads();
     if (warp == 0) {
       // lane l owns bins [248 - 8l, 256 - 8l), scanned from the top
       const int hi = 256 - 8 * lane;
+      uint32_t cnt8[8];
       uint32_t mine = 0;
 #pragma unroll
-      for (int i = 1; i <= 8; ++i) mine += sw.hist[hi - i];
+      for (int i = 0; i < 8; ++i) {
+        uint32_t h = 0;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) h += sw.whist[w][hi - 1 - i];
+        cnt8[i] = h;
+        mine += h;
+      }
       uint32_t incl = mine;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -579,19 +621,22 @@ __device__ int cta_select(const StepLaunch& a, int q, BeamTab& bt, SelWork& sw, 
       const bool here = (excl < target) && (incl >= target);
       const unsigned who = __ballot_sync(kFull, here);
       if (here && lane == __ffs(who) - 1) {
-        uint32_t run = excl;
-        for (int i = hi - 1; i >= hi - 8; --i) {
-          const uint32_t hc = sw.hist[i];
-          if (run + hc >= target) {
-            sw.cnt_gt += (int)run;
-            sw.prefix |= (uint32_t)i << shift;
-            sw.prefmask |= 255u << shift;
-            sw.cnt_eq = (int)hc;
-            if ((int)hc == sw.need - sw.cnt_gt) sw.all_eq = 1;
-            break;
-          }
-          run += hc;
+        uint32_t run = excl, bin = 0, bc = 0;
+        bool found = false;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t hc = cnt8[i];
+          const bool hit = !found && (run + hc >= target);
+          bin = hit ? (uint32_t)(hi - 1 - i) : bin;
+          bc = hit ? hc : bc;
+          found = found || hit;
+          run += found ? 0u : hc;
         }
+        sw.cnt_gt += (int)run;
+        sw.prefix |= bin << shift;
+        sw.prefmask |= 255u << shift;
+        sw.cnt_eq = (int)bc;
+        if ((int)bc == sw.need - sw.cnt_gt) sw.all_eq = 1;
       }
     }
     __syncthreads();
@@ -600,7 +645,7 @@ __device__ int cta_select(const StepLaunch& a, int q, BeamTab& bt, SelWork& sw, 
   const int need_eq = sw.need - sw.cnt_gt;
   const bool all_eq = sw.all_eq;
   for (int c = tid; c < total; c += NT) {
-    const uint32_t key = staged ? keys[c] : cand_key(a, bt, q, c);
+    const uint32_t key = (src == kGlobal) ? cand_key(a, bt, q, c) : keys[c];
     if (!key) continue;
     const uint32_t mk = key & pm;
     if (mk > pv || (all_eq && mk == pv)) {
@@ -615,7 +660,7 @@ __device__ int cta_select(const StepLaunch& a, int q, BeamTab& bt, SelWork& sw, 
     for (int c0 = 0; c0 < total && base < need_eq; c0 += NT) {
       const int c = c0 + tid;
       uint32_t key = 0;
-      if (c < total) key = staged ? keys[c] : cand_key(a, bt, q, c);
+      if (c < total) key = (src == kGlobal) ? cand_key(a, bt, q, c) : keys[c];
       const bool f = key && key == pv;
       const unsigned bal = __ballot_sync(kFull, f);
       if (lane == 0) sw.warp_tot[warp] = __popc(bal);
@@ -628,7 +673,7 @@ __device__ int cta_select(const StepLaunch& a, int q, BeamTab& bt, SelWork& sw, 
         if (slot < ZG_MAX_BEAM) sw.win[slot] = ((unsigned long long)key << 32) | (0xFFFFFFFFu - (uint32_t)c);
       }
       int tile = 0;
-      for (int w = 0; w < NT / 32; ++w) tile += sw.warp_tot[w];
+      for (int w = 0; w < NW; ++w) tile += sw.warp_tot[w];
       __syncthreads();
       base += tile;
     }
@@ -671,8 +716,8 @@ __device__ int cta_select(const StepLaunch& a, int q, BeamTab& bt, SelWork& sw, 
 // beams / padding.  On dense steps the next-step row is the row's first entry
 // plus the token's rank among the row's legal tokens: from the chunk legal
 // masks in shared memory when given (cluster kernel), else from the bitmap.
-template <int NT>
-__device__ void write_survivors(const StepLaunch& a, int q, const BeamTab& bt, const SelWork& sw, int n,
+template <int NT, typename SW>
+__device__ void write_survivors(const StepLaunch& a, int q, const BeamTab& bt, const SW& sw, int n,
                                 const uint32_t* msm = nullptr) {
   const int s = a.s;
   const size_t BW = (size_t)a.B * a.beam;
