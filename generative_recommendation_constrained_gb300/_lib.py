@@ -89,6 +89,7 @@ def _load():
         "zg_decode_host_workspace_size": [vp, vp, P(zg_model), i32, i32, i32, P(sz)],
         "zg_decode_host": [vp, vp, P(zg_model), vp, i32, i32, i32, vp, vp, vp, sz, vp],
         "zg_decode_trace": [vp, vp, P(zg_model), vp, i32, i32, i32, vp, vp, vp, sz, vp, P(zg_trace)],
+        "zg_decode_static": [vp, vp, P(zg_model), vp, i32, i32, i32, vp, vp, vp],
         "zg_check_device_status": [vp],
     }
     for name, args in sigs.items():
@@ -266,6 +267,16 @@ def zg_decode_host(idx: Index | None, plan: Plan | None, model: zg_model, u_host
                    out_sids_host, out_scores_host, workspace, ws_bytes: int, stream: int = 0):
     _check(lib.zg_decode_host(idx, plan, C.byref(model), _ptr(u_host), B, beam, K, _ptr(out_sids_host),
                               _ptr(out_scores_host), _ptr(workspace), ws_bytes, stream or None))
+
+
+ZG_STATIC_SCRATCH_BYTES = 16 << 20
+
+
+def zg_decode_static(idx: Index | None, plan: Plan | None, model: zg_model, u, B: int, beam: int, K: int,
+                     out_sids, out_scores, stream: int = 0):
+    """zg_decode without a workspace: scratch from the library's static device array."""
+    _check(lib.zg_decode_static(idx, plan, C.byref(model), _ptr(u), B, beam, K, _ptr(out_sids),
+                                _ptr(out_scores), stream or None))
 
 
 def zg_check_device_status(stream: int = 0):

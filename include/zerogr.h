@@ -270,6 +270,32 @@ ZG_API zg_status zg_decode_trace(const zg_index* idx, const zg_plan* plan, const
                                  int32_t* out_sids, float* out_scores, void* workspace,
                                  size_t ws_bytes, void* stream, zg_trace* trace);
 
+/* Bytes of the static device scratch zg_decode_static decodes in. */
+#define ZG_STATIC_SCRATCH_BYTES (16u << 20)
+
+/* zg_decode_static - the paper has no counterpart; this is a deployment
+ * convenience.  zg_decode with no caller workspace and no allocation at all:
+ * the scratch is a fixed ZG_STATIC_SCRATCH_BYTES (16 MiB) array in the
+ * library's device memory, held by every GPU that loads the library until
+ * the process exits.  It serves callers that cannot allocate device memory
+ * when they decode: processes whose device memory is pre-reserved by another
+ * framework's allocator, request threads on which allocation (and the
+ * synchronisation that freeing implies) is not allowed, runtimes that plan
+ * memory statically.
+ * Arguments and results are those of zg_decode without workspace/ws_bytes.
+ * A decode whose zg_decode_workspace_size exceeds ZG_STATIC_SCRATCH_BYTES is
+ * rejected with ZG_ERR_INVALID_ARG before anything runs.  It calls no
+ * cudaMalloc, cudaFree or other allocating routine.  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture.
+ * Every call on a device shares the one array and it keeps the previous
+ * call's contents (the decode writes every scratch word before reading it,
+ * so nothing needs clearing): calls whose executions can overlap on the GPU
+ * (concurrent streams, other host threads) race and must not be issued. */
+ZG_API zg_status zg_decode_static(const zg_index* idx, const zg_plan* plan, const zg_model* model,
+                                  const float* u, int32_t B, int32_t beam, int32_t K,
+                                  int32_t* out_sids, float* out_scores, void* stream);
+
 /* Synchronises `stream`, then reports and clears the device status word that
  * kernels set instead of trapping (bit 0: row out of range, bit 1: token out
  * of range, bit 2: a bounded wait in the tensor-core kernel expired, bit 3:
