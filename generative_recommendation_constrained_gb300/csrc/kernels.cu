@@ -34,7 +34,6 @@ constexpr int kSelCap = 12288;       // keys staged in shared memory by k_select
 constexpr int kClusterThreads = 256;
 constexpr int kClusterCap = 11264;   // slot scores / keys held by the cluster kernel's rank-0 CTA
 constexpr int kClusterPcap = 2048;   // chunk partials and masks held by the rank-0 CTA
-constexpr int kSmallR = 12;          // keys a lane holds in the small-keep select
 
 // ---------------------------------------------------------------------------
 // Stand-alone selective step: one warp per (beam, chunk) item, grid-stride,
@@ -154,10 +153,7 @@ __global__ void __launch_bounds__(kClusterThreads, 2) k_decode_cluster(const __g
       int n;
       if (in_smem) {
         beam_lse_sel<NT>(a, q, bt, psm);
-        if (a.keep <= 32 && bt.total <= NW * 32 * kSmallR)
-          n = cta_select_small<NT, kSmallR>(a, bt, sw, zsm, true);
-        else
-          n = cta_select<NT>(a, q, bt, sw, zsm, kZStaged);  // its first barrier publishes the lse
+        n = cta_select<NT>(a, q, bt, sw, zsm, kZStaged);  // its first barrier publishes the lse
         write_survivors<NT>(a, q, bt, sw, n, msm);
       } else {
         beam_lse<NT>(a, q, bt);
@@ -289,11 +285,7 @@ __global__ void __launch_bounds__(kSelThreads) k_select(const __grid_constant__ 
   __syncthreads();
   const bool staged = bt.total <= kSelCap;
   if (staged) stage_keys_global<kSelThreads>(a, q, bt, keys);
-  int n;
-  if (staged && a.keep <= 32 && bt.total <= kSelThreads * kSmallR)
-    n = cta_select_small<kSelThreads, kSmallR>(a, bt, sw, keys, false);
-  else
-    n = cta_select<kSelThreads>(a, q, bt, sw, keys, staged ? kKeysStaged : kGlobal);
+  const int n = cta_select<kSelThreads>(a, q, bt, sw, keys, staged ? kKeysStaged : kGlobal);
   write_survivors<kSelThreads>(a, q, bt, sw, n);
 }
 

@@ -534,132 +534,6 @@ __device__ __forceinline__ unsigned long long warp_sort_desc(unsigned long long 
   return v;
 }
 
-// ---------------------------------------------------------------------------
-// Select for small keep (<= 32) with every candidate's key or z staged in
-// shared memory and at most NW*32*R candidates: no shared histograms, two
-// CTA barriers.
-//   1. each warp takes a contiguous slice of the flat candidates, R a lane in
-//      registers, and finds its local n-th largest key by a bitwise radix
-//      select (32 rounds; each counts prefix matches with one warp
-//      reduction); it appends its winners, in flat order, to a list;
-//   2. warp 0 repeats the bitwise select over the <= NW*keep listed winners
-//      and sorts the final keep by (score desc, flat asc) with shuffles.
-// Threshold ties go to the lowest flat indices at both levels, so the result
-// equals cta_select's.
-// ---------------------------------------------------------------------------
-
-// n-th largest (1 <= n <= number of non-zero keys) of the keys held R a lane
-// by the warp; returns it and the count of keys strictly above it.
-template <int R>
-__device__ __forceinline__ uint32_t warp_kth(const uint32_t (&kr)[R], int n, int* above_out) {
-  uint32_t P = 0, M = 0;
-  int above = 0;
-#pragma unroll 1
-  for (int b = 31; b >= 0; --b) {
-    const uint32_t bit = 1u << b;
-    int c = 0;
-#pragma unroll
-    for (int r = 0; r < R; ++r) c += (((kr[r] & M) == P) && (kr[r] & bit)) ? 1 : 0;
-    c = __reduce_add_sync(kFull, c);
-    if (above + c >= n)
-      P |= bit;
-    else
-      above += c;
-    M |= bit;
-  }
-  *above_out = above;
-  return P;
-}
-
-// Append the warp's winners (keys > T, then the first `eq_take` keys == T in
-// flat order r-major, lane-minor) as (key << 32 | ~flat) to list[0...];
-// flat(r, lane) = flat0[r] + lane.  Returns the number appended.
-template <int R>
-__device__ __forceinline__ int warp_collect(const uint32_t (&kr)[R], const int (&flat0)[R], uint32_t T, int eq_take,
-                                            unsigned long long* list, int lane) {
-  const unsigned lt = (1u << lane) - 1u;
-  int base = 0, eqseen = 0;
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    const bool gt = kr[r] > T;
-    const bool eq = kr[r] != 0u && kr[r] == T;
-    const unsigned eqb = __ballot_sync(kFull, eq);
-    const bool take = gt || (eq && (eqseen + __popc(eqb & lt)) < eq_take);
-    const unsigned tb = __ballot_sync(kFull, take);
-    if (take)
-      list[base + __popc(tb & lt)] =
-          ((unsigned long long)kr[r] << 32) | (0xFFFFFFFFu - (uint32_t)(flat0[r] + lane));
-    base += __popc(tb);
-    eqseen += __popc(eqb);
-  }
-  return base;
-}
-
-template <int NT, int R, typename SW>
-__device__ int cta_select_small(const StepLaunch& a, BeamTab& bt, SW& sw, uint32_t* zk, bool z_staged) {
-  constexpr int NW = NT / 32;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  __syncthreads();  // the beam table's log-sum-exps are complete
-  const int total = bt.total;
-  const int keep_n = min(a.keep, bt.nlegal);
-  if (keep_n == 0) return 0;
-  const int per = ((total + NW - 1) / NW + 31) & ~31;  // slice of a warp (<= 32*R)
-  const int c0 = warp * per;
-  uint32_t kr[R];
-  int f0[R];
-  int k = (c0 + lane < total) ? upper_find(bt.start, a.Wc, c0 + lane) : 0;
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    const int c = c0 + r * 32 + lane;
-    f0[r] = c0 + r * 32;
-    kr[r] = 0u;
-    if (r * 32 < per && c < total) {
-      while (bt.start[k + 1] <= c) ++k;
-      if (z_staged) {
-        const float z = __uint_as_float(zk[c]);
-        kr[r] = (z == -INFINITY) ? 0u : f2ord(bt.cum[k] + (z - bt.lse[k]));
-      } else {
-        kr[r] = zk[c];
-      }
-    }
-  }
-  int nz = 0;
-#pragma unroll
-  for (int r = 0; r < R; ++r) nz += kr[r] ? 1 : 0;
-  nz = __reduce_add_sync(kFull, nz);
-  const int n_w = min(keep_n, nz);
-  unsigned long long* lists = reinterpret_cast<unsigned long long*>(&sw.whist[0][0]);  // NW x 32
-  int got = 0;
-  if (n_w > 0) {
-    int above = 0;
-    const uint32_t T = warp_kth<R>(kr, n_w, &above);
-    got = warp_collect<R>(kr, f0, T, n_w - above, lists + warp * 32, lane);
-  }
-  if (lane == 0) sw.warp_tot[warp] = got;
-  __syncthreads();
-  if (warp == 0) {
-    // union of the warps' winners; warps own contiguous flat ranges and list
-    // their winners in flat order, so (warp, position) order is flat order
-    uint32_t kk[NW];
-    int ff[NW];
-#pragma unroll
-    for (int w = 0; w < NW; ++w) {
-      const unsigned long long v = lane < sw.warp_tot[w] ? lists[w * 32 + lane] : 0ull;
-      kk[w] = (uint32_t)(v >> 32);
-      ff[w] = v ? (int)(0xFFFFFFFFu - (uint32_t)(v & 0xFFFFFFFFu)) - lane : 0;
-    }
-    int above = 0;
-    const uint32_t T = warp_kth<NW>(kk, keep_n, &above);
-    warp_collect<NW>(kk, ff, T, keep_n - above, sw.win, lane);
-    __syncwarp();
-    const unsigned long long v = warp_sort_desc(lane < keep_n ? sw.win[lane] : 0ull, lane);
-    __syncwarp();
-    if (lane < keep_n) sw.win[lane] = v;
-  }
-  __syncthreads();
-  return keep_n;
-}
-
 // Where cta_select finds the candidates' keys.
 enum KeySrc { kKeysStaged = 0, kZStaged = 1, kGlobal = 2 };
 
