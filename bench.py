@@ -120,29 +120,34 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- roofline accounting
 
-def selective_bytes(st: dict, cfg, s: int) -> int:
-    """Algorithmic HBM bytes of one selective-projection launch at step s
-    (1-based): index rows read, hidden-state gather-add (parent hidden and
-    C_{s-1} row per beam, or u at step 1), the hidden written for the next
-    step, each distinct legal weight row once (the per-(beam, slot) re-reads
-    are L2 hits after the first), the padded slots and chunk partials
-    written."""
+def step_bytes(st: dict, cfg, s: int) -> int:
+    """Algorithmic bytes of step s (1-based) of the filtering-first decode,
+    one unit = one (live beam, legal slot) pair plus the per-beam terms:
+    the beam's index row (rowptr pair and its column entries, or its bitmap
+    row), the C_{s-1} row of its gather-add (s >= 2), one W_s row per
+    (beam, legal slot), and W (score, slot) survivor pairs per beam; the last
+    step adds the outputs B*K*(4L+4).  Re-reads of a weight row by other beams
+    are counted (most are L2 hits), so this is the work the method moves
+    through the memory system, not its HBM traffic."""
     e = 4 if cfg.w_dtype == "f32" else 2
     n = st["live_beams"]
     b = st["index_bytes"]
-    b += n * cfg.d * 4 * (2 if s >= 2 else 1)
-    b += n * cfg.d * 4 if (2 <= s < cfg.L) else 0
-    b += st["unique_tokens"] * cfg.d * e
-    b += st["chunks"] * (32 * 4 + 8)
+    b += n * cfg.d * 4 if s >= 2 else 0
+    b += st["legal_slots"] * cfg.d * e
+    b += n * cfg.beam * 8
+    if s == cfg.L:
+        b += cfg.batch * cfg.topk * (4 * cfg.L + 4)
     return int(b)
 
 
-def select_bytes(st: dict, cfg, s: int) -> int:
-    """Algorithmic bytes of one select launch: every legal candidate's score
-    and the chunk partials read once, beam state in, survivors out."""
+def step_unique_bytes(st: dict, cfg, s: int) -> int:
+    """Lower bound on the HBM bytes of step s with a cold L2: the index rows,
+    each distinct legal weight row once, the C rows, survivors."""
+    e = 4 if cfg.w_dtype == "f32" else 2
     n = st["live_beams"]
-    b = st["legal_slots"] * 4 + st["chunks"] * 8 + n * 16
-    b += cfg.batch * cfg.beam * 16
+    b = st["index_bytes"] + st["unique_tokens"] * cfg.d * e
+    b += n * cfg.d * 4 if s >= 2 else 0
+    b += n * cfg.beam * 8
     return int(b)
 
 
@@ -265,7 +270,11 @@ def run_gpu(args, cfg):
     info = zg.zg_index_info_get(idx)
     dm = DeviceModel(model, dev)
     u_dev = torch.from_numpy(u).to(dev)
-    plan = zg.zg_tune(idx, dm.struct, torch.from_numpy(warm_u).to(dev), B, beam, K, 20, stream)
+    if args.plan:
+        plan = zg.zg_plan_force(idx, B, beam, [1 if ch == "f" else 0 for ch in args.plan])
+        zg.zg_plan_set_fusion(plan, args.cluster)
+    else:
+        plan = zg.zg_tune(idx, dm.struct, torch.from_numpy(warm_u).to(dev), B, beam, K, 20, stream)
     variants, step_ms, cluster_ctas, fused_ms = zg.zg_plan_describe(plan)
     dec = Decoder(idx, plan, dm, B, beam, K, dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -346,21 +355,30 @@ def run_gpu(args, cfg):
         avg = {k: statistics.fmean(t["steps"][s - 1][k] for t in traces)
                for k in ("ms_gather", "ms_project", "ms_select")}
         if st["variant"] == 0:
-            kern.append((avg["ms_project"], [s], "k_selective", selective_bytes(st, cfg, s), "hbm"))
+            kern.append((avg["ms_project"], [s], "k_selective", step_bytes(st, cfg, s), "hbm",
+                         step_unique_bytes(st, cfg, s)))
         else:
-            kern.append((avg["ms_project"], [s], "k_full_simt", full_flops(st, cfg, s), "alu"))
-            if s >= 2:
-                kern.append((avg["ms_gather"], [s], "k_gather_add", st["live_beams"] * cfg.d * 12, "hbm"))
-        kern.append((avg["ms_select"], [s], "k_select", select_bytes(st, cfg, s), "hbm"))
+            name = "k_full_simt" if cfg.w_dtype == "f32" else "k_full_tc"
+            kern.append((avg["ms_project"], [s], name, full_flops(st, cfg, s),
+                         "alu" if cfg.w_dtype == "f32" else "tensor", None))
+            if s >= 2 or cfg.w_dtype != "f32":
+                kern.append((avg["ms_gather"], [s], "k_gather_add", st["live_beams"] * cfg.d * 12, "hbm", None))
+        kern.append((avg["ms_select"], [s], "k_select", st["legal_slots"] * 4 + st["live_beams"] * 16, "hbm",
+                     None))
     if s0 <= L:
         fused_kernel_ms = statistics.fmean(t["ms_fused"] for t in traces)
-        fb = sum(selective_bytes(steps_last[s - 1], cfg, s) + select_bytes(steps_last[s - 1], cfg, s)
-                 for s in range(s0, L + 1))
-        kern.append((fused_kernel_ms, list(range(s0, L + 1)), "k_decode_cluster", fb, "hbm"))
+        fb = sum(step_bytes(steps_last[s - 1], cfg, s) for s in range(s0, L + 1))
+        fu = sum(step_unique_bytes(steps_last[s - 1], cfg, s) for s in range(s0, L + 1))
+        kern.append((fused_kernel_ms, list(range(s0, L + 1)), "k_decode_cluster", fb, "hbm", fu))
     kern.sort(key=lambda x: -x[0])
-    top_ms, top_steps, top_name, alg, bound = kern[0]
+    top_ms, top_steps, top_name, alg, bound, uniq = kern[0]
     if bound == "hbm":
         roof = {"bound": "hbm", "achieved": alg / (top_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+        if uniq:
+            roof["achieved_distinct_rows"] = uniq / (top_ms * 1e-3) / 1e9
+    elif bound == "tensor":
+        roof = {"bound": "tensor", "achieved": alg / (top_ms * 1e-3) / 1e12, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s"}
     else:
         sm_mhz = clocks.get("sm_mhz") or peaks["sm_max_mhz"]
         # 152 SMs x 128 fp32 FMA lanes x 2 flops per clock
@@ -428,7 +446,7 @@ def run_gpu(args, cfg):
             "clocks": clocks,
             "unconstrained": {"ms_per_step": ums, "value": B * world / (ums / 1000.0), "unit": UNIT,
                               "constrained_speedup": ums / ms_max},
-            "kernels": [{"kernel": n, "steps": st, "ms": round(t, 5)} for t, st, n, _, _ in kern],
+            "kernels": [{"kernel": n, "steps": st, "ms": round(t, 5)} for t, st, n, _, _, _ in kern],
             "work": work,
         }
         print(json.dumps(line), flush=True)
@@ -449,8 +467,12 @@ def main(argv=None):
     ap.add_argument("--ref-requests", type=int, default=2)
     ap.add_argument("--quick", action="store_true",
                     help="tune, capture and replay only (a short command for profilers)")
+    ap.add_argument("--plan", default="", help="fixed per-step variants instead of tuning, e.g. sss or fss")
+    ap.add_argument("--cluster", type=int, default=8, help="fused cluster size with --plan (0: no fusion)")
     args = ap.parse_args(argv)
     cfg = synth.CONFIGS[args.workload]
+    if args.plan and len(args.plan) != cfg.L:
+        ap.error(f"--plan needs {cfg.L} letters (s or f)")
     if args.impl == "reference":
         run_reference(args, cfg)
     else:
