@@ -30,10 +30,28 @@ using namespace dev;
 namespace cg = cooperative_groups;
 
 constexpr int kSelThreads = 512;
-constexpr int kSelCap = 12288;       // keys staged in shared memory by k_select
+constexpr int kSelCap = 32768;       // keys staged in shared memory by k_select (one CTA a request)
 constexpr int kClusterThreads = 256;
 constexpr int kClusterCap = 11264;   // slot scores / keys held by the cluster kernel's rank-0 CTA
 constexpr int kClusterPcap = 2048;   // chunk partials and masks held by the rank-0 CTA
+
+// Select when the candidates do not fit in shared memory: filtered select
+// on 256-slot tile maxima when those fit in half the buffer, else the radix
+// select over the global slot buffer.  For full-score steps beam_lse has
+// already stored the tile maxima in buf when tile_z_ready.
+template <int NT, typename SW>
+__device__ int select_large(const StepLaunch& a, int q, BeamTab& bt, SW& sw, uint32_t* buf, int cap,
+                            bool tile_z_ready = false) {
+  const bool full = !(a.mode == kSelSparse || a.mode == kSelDense);
+  int rt, tw;
+  tile_layout(a.Wc, a.S, cap, &rt, &tw);
+  if (a.Wc * rt <= cap / 2 && (!full || tile_z_ready)) {
+    const int nrep = tile_rep_keys<NT>(a, q, bt, buf, rt, tw);
+    const int n = cta_select_filtered<NT>(a, q, bt, sw, buf, cap, nrep);
+    if (n >= 0) return n;
+  }
+  return cta_select<NT>(a, q, bt, sw, buf, kGlobal);
+}
 
 // ---------------------------------------------------------------------------
 // Stand-alone selective step: one warp per (beam, chunk) item, grid-stride,
@@ -159,8 +177,12 @@ __global__ void __launch_bounds__(kClusterThreads, 2) k_decode_cluster(const __g
         beam_lse<NT>(a, q, bt);
         __syncthreads();
         const bool staged = bt.total <= A.cap;
-        if (staged) stage_keys_global<NT>(a, q, bt, zsm);
-        n = cta_select<NT>(a, q, bt, sw, zsm, staged ? kKeysStaged : kGlobal);
+        if (staged) {
+          stage_keys_global<NT>(a, q, bt, zsm);
+          n = cta_select<NT>(a, q, bt, sw, zsm, kKeysStaged);
+        } else {
+          n = select_large<NT>(a, q, bt, sw, zsm, A.cap);
+        }
         write_survivors<NT>(a, q, bt, sw, n);
       }
     }
@@ -281,11 +303,20 @@ __global__ void __launch_bounds__(kSelThreads) k_select(const __grid_constant__ 
   __shared__ SelWorkT<kSelThreads / 32> sw;
   const int q = blockIdx.x;
   build_beam_table<kSelThreads>(a, q, bt);
-  beam_lse<kSelThreads>(a, q, bt);
-  __syncthreads();
   const bool staged = bt.total <= kSelCap;
-  if (staged) stage_keys_global<kSelThreads>(a, q, bt, keys);
-  const int n = cta_select<kSelThreads>(a, q, bt, sw, keys, staged ? kKeysStaged : kGlobal);
+  int rt, tw;
+  tile_layout(a.Wc, a.S, kSelCap, &rt, &tw);
+  const bool full = !(a.mode == kSelSparse || a.mode == kSelDense);
+  // tile maxima of full scores land in keys[] while the log-sum-exp is computed
+  beam_lse<kSelThreads>(a, q, bt, (!staged && full && a.Wc * rt <= kSelCap / 2) ? keys : nullptr, rt, tw);
+  __syncthreads();
+  int n;
+  if (staged) {
+    stage_keys_global<kSelThreads>(a, q, bt, keys);
+    n = cta_select<kSelThreads>(a, q, bt, sw, keys, kKeysStaged);
+  } else {
+    n = select_large<kSelThreads>(a, q, bt, sw, keys, kSelCap, true);
+  }
   write_survivors<kSelThreads>(a, q, bt, sw, n);
 }
 

@@ -431,8 +431,26 @@ __device__ void beam_lse_sel(const StepLaunch& a, int q, BeamTab& bt, const floa
 
 // Legal-only log-sum-exp of every live beam (one warp per beam): from the
 // selective chunk partials, or by two passes over the full scores.
+// Representative tiles of a step for the filtered select: rt tiles of tw
+// slots (a multiple of 32) a beam, at most half of a cap-entry buffer.
+__host__ __device__ __forceinline__ void tile_layout(int Wc, int S, int cap, int* rt, int* tw) {
+  int max_rt = (cap / 2) / (Wc > 0 ? Wc : 1);
+  if (max_rt < 1) max_rt = 1;
+  int r = (S + 255) / 256;
+  if (r > max_rt) r = max_rt;
+  if (r < 1) r = 1;
+  *rt = r;
+  *tw = ((S + r - 1) / r + 31) & ~31;
+}
+
+// Legal-only log-sum-exp of every live beam (one warp per beam): from the
+// selective chunk partials, or by two passes over the full scores.  For the
+// full scores, when rep_z is given, the maximum legal z of every tw-slot
+// tile of beam k is also stored (as float bits) at rep_z[k * rt + t]
+// (-inf for a tile without legal tokens).
 template <int NT>
-__device__ void beam_lse(const StepLaunch& a, int q, BeamTab& bt) {
+__device__ void beam_lse(const StepLaunch& a, int q, BeamTab& bt, uint32_t* rep_z = nullptr, int rt = 0,
+                         int tw = 256) {
   if (a.mode == kSelSparse || a.mode == kSelDense) {
     beam_lse_sel<NT>(a, q, bt, nullptr);
     return;
@@ -440,32 +458,33 @@ __device__ void beam_lse(const StepLaunch& a, int q, BeamTab& bt) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int k = warp; k < a.Wc; k += NT / 32) {
     if (bt.cnt[k] == 0) continue;
-    float2 acc = make_float2(-INFINITY, 0.f);
-    {
-      const int n = bt.cnt[k];
-      const size_t zb = (size_t)q * a.zq + (size_t)k * a.S;
-      float m = -INFINITY, sm = 0.f;
-      for (int pass = 0; pass < 2; ++pass) {
-        for (int j = lane; j < n; j += 32) {
-          float z;
-          if (a.mode == kFullSparse)
-            z = a.Z[zb + a.tab.col[bt.rp[k] + j]];
-          else if (a.mode == kFullDense)
-            z = ((a.tab.bitmap[(size_t)bt.row[k] * a.tab.words + (j >> 5)] >> (j & 31)) & 1u) ? a.Z[zb + j]
+    const int n = bt.cnt[k];
+    const size_t zb = (size_t)q * a.zq + (size_t)k * a.S;
+    auto zval = [&](int j) -> float {
+      if (a.mode == kFullSparse) return a.Z[zb + a.tab.col[bt.rp[k] + j]];
+      if (a.mode == kFullDense)
+        return ((a.tab.bitmap[(size_t)bt.row[k] * a.tab.words + (j >> 5)] >> (j & 31)) & 1u) ? a.Z[zb + j]
                                                                                           : -INFINITY;
-          else
-            z = a.Z[zb + j];
-          if (pass == 0)
-            m = fmaxf(m, z);
-          else if (z != -INFINITY)
-            sm += expf(z - m);
-        }
-        if (pass == 0) m = warp_max(m);
+      return a.Z[zb + j];
+    };
+    float m = -INFINITY;
+    for (int t = 0; t * tw < n; ++t) {
+      float tm = -INFINITY;
+      for (int i = 0; i < tw; i += 32) {
+        const int j = t * tw + i + lane;
+        if (j < n) tm = fmaxf(tm, zval(j));
       }
-      acc = make_float2(m, sm);
+      tm = warp_max(tm);
+      m = fmaxf(m, tm);
+      if (rep_z && lane == 0) rep_z[k * rt + t] = __float_as_uint(tm);
     }
-    acc = warp_lse(acc);
-    if (lane == 0) bt.lse[k] = acc.x + logf(acc.y);
+    float sm = 0.f;
+    for (int j = lane; j < n; j += 32) {
+      const float z = zval(j);
+      if (z != -INFINITY) sm += expf(z - m);
+    }
+    sm = warp_sum(sm);
+    if (lane == 0) bt.lse[k] = m + logf(sm);
   }
 }
 
@@ -532,6 +551,168 @@ __device__ __forceinline__ unsigned long long warp_sort_desc(unsigned long long 
     }
   }
   return v;
+}
+
+// k-th largest (1 <= kth <= n) of the non-zero keys[0..n) in shared memory:
+// returns T with count(> T) < kth <= count(>= T).  8-bit radix passes with
+// per-warp histograms.
+template <int NT, typename SW>
+__device__ uint32_t cta_kth(const uint32_t* keys, int n, int kth, SW& sw) {
+  constexpr int NW = NT / 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    sw.prefix = 0;
+    sw.prefmask = 0;
+    sw.need = kth;
+    sw.cnt_gt = 0;
+  }
+  __syncthreads();
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = tid; i < NW * 256; i += NT) (&sw.whist[0][0])[i] = 0u;
+    __syncthreads();
+    const uint32_t pm = sw.prefmask, pv = sw.prefix;
+    for (int c = tid; c < n; c += NT) {
+      const uint32_t key = keys[c];
+      if (key && (key & pm) == pv) atomicAdd(&sw.whist[warp][(key >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const int hi = 256 - 8 * lane;
+      uint32_t cnt8[8];
+      uint32_t mine = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        uint32_t h = 0;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) h += sw.whist[w][hi - 1 - i];
+        cnt8[i] = h;
+        mine += h;
+      }
+      uint32_t incl = mine;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const uint32_t excl = incl - mine;
+      const uint32_t target = (uint32_t)(sw.need - sw.cnt_gt);
+      const bool here = (excl < target) && (incl >= target);
+      const unsigned who = __ballot_sync(kFull, here);
+      if (here && lane == __ffs(who) - 1) {
+        uint32_t run = excl, bin = 0;
+        bool found = false;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const bool hit = !found && (run + cnt8[i] >= target);
+          bin = hit ? (uint32_t)(hi - 1 - i) : bin;
+          found = found || hit;
+          run += found ? 0u : cnt8[i];
+        }
+        sw.cnt_gt += (int)run;
+        sw.prefix |= bin << shift;
+        sw.prefmask |= 255u << shift;
+      }
+    }
+    __syncthreads();
+  }
+  return sw.prefix;
+}
+
+// Select when the request's candidates do not fit in shared memory.  rep[0,
+// nrep) holds the keys of true candidates (tile maxima); the keep-th largest
+// of them is a lower bound on the keep-th largest candidate, so one pass over
+// the global slot buffer keeps only candidates at or above it, as
+// (key << 32 | ~flat), in buf after rep; they are bitonic-sorted descending
+// and the first keep become the winners.  Returns -1 (nothing written) when
+// more candidates pass than the space holds; the caller then runs the full
+// radix select.
+template <int NT, typename SW>
+__device__ int cta_select_filtered(const StepLaunch& a, int q, BeamTab& bt, SW& sw, uint32_t* buf, int cap,
+                                   int nrep) {
+  const int tid = threadIdx.x;
+  const int total = bt.total;
+  const int keep_n = min(a.keep, bt.nlegal);
+  if (keep_n == 0) return 0;
+  __syncthreads();
+  const uint32_t tlb = (nrep >= keep_n) ? cta_kth<NT>(buf, nrep, keep_n, sw) : 1u;
+  const int off = (nrep + 1) & ~1;  // u64 alignment
+  unsigned long long* list = reinterpret_cast<unsigned long long*>(buf + off);
+  int lcap = 1;
+  while (lcap * 2 <= (cap - off) / 2) lcap *= 2;  // power of two, for the sort
+  if (tid == 0) sw.nwin = 0;
+  __syncthreads();
+  for (int c0 = tid; c0 < total; c0 += 4 * NT) {
+    uint32_t kk[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c = c0 + u * NT;
+      kk[u] = (c < total) ? cand_key(a, bt, q, c) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (kk[u] && kk[u] >= tlb) {
+        const int pos = atomicAdd(&sw.nwin, 1);
+        if (pos < lcap) list[pos] = ((unsigned long long)kk[u] << 32) | (0xFFFFFFFFu - (uint32_t)(c0 + u * NT));
+      }
+    }
+  }
+  __syncthreads();
+  const int nl = sw.nwin;
+  if (nl > lcap || nl < keep_n) return -1;
+  int P = 1;
+  while (P < nl) P <<= 1;
+  for (int i = nl + tid; i < P; i += NT) list[i] = 0ull;
+  __syncthreads();
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = tid; i < P; i += NT) {
+        const int jx = i ^ stride;
+        if (jx > i) {
+          const bool desc = ((i & size) == 0);
+          const unsigned long long x = list[i], y = list[jx];
+          if (desc ? (x < y) : (x > y)) {
+            list[i] = y;
+            list[jx] = x;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = tid; i < keep_n; i += NT) sw.win[i] = list[i];
+  __syncthreads();
+  return keep_n;
+}
+
+// Keys of the tile representatives for cta_select_filtered, in place in
+// rep[k * rt + t]: from the tile maxima of full scores stored by beam_lse
+// (float bits), or, for selective steps, from the maxima of each beam's
+// chunk partials, tw/32 chunks a tile.  Returns the number of
+// representatives (Wc * rt).
+template <int NT>
+__device__ int tile_rep_keys(const StepLaunch& a, int q, const BeamTab& bt, uint32_t* rep, int rt, int tw) {
+  const bool sel = (a.mode == kSelSparse || a.mode == kSelDense);
+  const int n = a.Wc * rt;
+  const int cpt = tw / kChunk;  // chunks a tile
+  for (int i = threadIdx.x; i < n; i += NT) {
+    const int k = i / rt, t = i - k * rt;
+    uint32_t key = 0u;
+    if (bt.cnt[k] > 0 && t * tw < bt.cnt[k]) {
+      float m;
+      if (sel) {
+        const float2* pp = a.part + (size_t)q * a.pq + (size_t)k * a.nch;
+        m = -INFINITY;
+        const int c1 = min(bt.items[k], cpt * (t + 1));
+        for (int c = cpt * t; c < c1; ++c) m = fmaxf(m, pp[c].x);
+      } else {
+        m = __uint_as_float(rep[i]);
+      }
+      if (m != -INFINITY) key = f2ord(bt.cum[k] + (m - bt.lse[k]));
+    }
+    rep[i] = key;
+  }
+  __syncthreads();
+  return n;
 }
 
 // Where cta_select finds the candidates' keys.

@@ -355,3 +355,62 @@ def test_tensor_core_full_matches_selective(zg, dtype):
     trie = oracle.Trie(sids, L, V)
     ref = oracle.decode(trie, model, u, 16, 16, requests=range(6))
     check_topk(b_s, b_sc, ref, trie, model, u, 1e-4, WINDOW, requests=range(6))
+
+
+# ------------------------------------------------------------------ large candidate sets (filtered select)
+
+def _dense2(V, n_first, p, seed):
+    """L=2 catalogue: n_first first tokens, each followed by every token with
+    probability p (dense step-2 rows)."""
+    rng = np.random.default_rng(seed)
+    first = np.sort(rng.choice(V, n_first, replace=False))
+    rows = []
+    for t in first:
+        kids = np.nonzero(rng.random(V) < p)[0]
+        rows.append(np.stack([np.full(kids.size, t), kids], 1))
+    return np.concatenate(rows).astype(np.int32)
+
+
+def test_unconstrained_large_candidate_set(zg):
+    """16 beams x 4,096 tokens a request exceed the select's shared-memory stage."""
+    L, V, d = 2, 4096, 64
+    model = synth.make_model(L, V, d, "bf16", 8)
+    u = synth.make_requests(3, d, 8)
+    ref = oracle.decode(None, model, u, 16, 16)
+    s, sc = decode_gpu(zg, None, model, u, 16, 16)
+    check_topk(s, sc, ref, None, model, u, 2e-2, WINDOW)
+
+
+@pytest.mark.parametrize("variants", [[1, 1], [0, 1], [1, 0], [0, 0]])
+def test_dense_full_step_large_candidate_set(zg, variants):
+    V, d = 4096, 64
+    sids = _dense2(V, 40, 0.9, 5)
+    model = synth.make_model(2, V, d, "f16", 5)
+    u = synth.make_requests(3, d, 5)
+    idx = zg.zg_index_build(sids, V, stream=_stream())
+    assert zg.zg_index_stats(idx, 2)["format"] == zg.ZG_FMT_DENSE
+    trie = oracle.Trie(sids, 2, V)
+    ref = oracle.decode(trie, model, u, 16, 16)
+    s, sc = decode_gpu(zg, idx, model, u, 16, 16, variants)
+    check_topk(s, sc, ref, trie, model, u, 2e-2, WINDOW)
+
+
+@pytest.mark.parametrize("cluster", [1, 8])
+def test_fused_hot_prefixes_large_candidate_set(zg, cluster):
+    """Sparse step 2 with first tokens of ~8,192 children: 8 beams x 8,192
+    slots a request exceed the fused kernel's shared-memory stage."""
+    V, d = 8192, 64
+    rng = np.random.default_rng(3)
+    hot = _dense2(V, 12, 0.97, 3)
+    cold_first = rng.choice(np.setdiff1d(np.arange(V), np.unique(hot[:, 0])), 200, replace=False)
+    cold = np.stack([np.repeat(cold_first, 3), rng.integers(0, V, 600)], 1)
+    sids = np.unique(np.concatenate([hot, cold]).astype(np.int32), axis=0)
+    model = synth.make_model(2, V, d, "f32", 3)
+    u = synth.make_requests(3, d, 3)
+    idx = zg.zg_index_build(sids, V, format_mode=1, stream=_stream())   # all sparse
+    trie = oracle.Trie(sids, 2, V)
+    ref = oracle.decode(trie, model, u, 8, 8)
+    a = decode_gpu(zg, idx, model, u, 8, 8, [0, 0], fused=cluster)
+    b = decode_gpu(zg, idx, model, u, 8, 8, [0, 0], fused=0)
+    check_topk(a[0], a[1], ref, trie, model, u, 1e-4, WINDOW)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
