@@ -63,6 +63,7 @@ WsLayout layout(const Dims& m, bool host_io) {
   for (int s = 1; s <= m.L; ++s) {
     const size_t N = (size_t)m.B * (s == 1 ? 1 : m.beam);
     size_t S = m.S_full;
+    pf = std::max(pf, N * (m.S_full / kChunk));  // full-projection chunk partials
     if (m.constrained) {
       S = std::max<size_t>(S, m.S_sel[s - 1]);
       pf = std::max(pf, N * m.nch_sel[s - 1]);
@@ -215,9 +216,14 @@ StepLaunch make_launch(const Run& r, int s, int variant) {
     a.part = reinterpret_cast<float2*>(r.ws + r.w.part);
   } else {
     a.mode = !r.idx ? kUncon : (r.idx->steps[s - 1].fmt == ZG_FMT_SPARSE ? kFullSparse : kFullDense);
-    a.nch = 0;
     a.S = m.S_full;
-    a.part = nullptr;
+    if (a.mode == kFullSparse) {  // few legal tokens a beam: the select gathers them
+      a.nch = 0;
+      a.part = nullptr;
+    } else {  // the full projection's epilogue writes chunk partials
+      a.nch = m.S_full / kChunk;
+      a.part = reinterpret_cast<float2*>(r.ws + r.w.part);
+    }
   }
   a.zq = (int64_t)a.Wc * a.S;      // contiguous beam rows (the full projection's layout)
   a.pq = (int64_t)a.Wc * a.nch;
@@ -244,11 +250,18 @@ zg_status run_step(const Run& r, int s, int variant, cudaStream_t st, const Step
       e = launch_split_h(H, r.ws + r.w.hhi, r.ws + r.w.hlo, (size_t)M * a.d, a.w_dtype, st);
       if (e != cudaSuccess) return cuda_fail(e, "hidden split launch");
     }
+    FullEpi epi{};
+    epi.part = a.part;
+    if (a.mode == kFullDense) {
+      epi.bitmap = a.tab.bitmap;
+      epi.words = (int)a.tab.words;
+      epi.rows = (s >= 2) ? a.row_in : nullptr;  // beam b = q*beam + k at s >= 2; the root's row 0 at s = 1
+    }
     if (tm) cudaEventRecord(tm->ev[1], st);
     if (a.w_dtype != ZG_F32)
-      e = launch_full_tc(r.ws + r.w.hhi, r.ws + r.w.hlo, a.W, a.Z, M, a.V, a.d, a.S, a.w_dtype, a.status, st);
+      e = launch_full_tc(r.ws + r.w.hhi, r.ws + r.w.hlo, a.W, a.Z, M, a.V, a.d, a.S, a.w_dtype, epi, a.status, st);
     else
-      e = launch_full_simt(a, H, st);
+      e = launch_full_simt(a, H, epi, st);
     if (e != cudaSuccess) return cuda_fail(e, "full projection launch");
   }
   if (tm) cudaEventRecord(tm->ev[2], st);

@@ -42,10 +42,10 @@ constexpr int kClusterPcap = 2048;   // chunk partials and masks held by the ran
 template <int NT, typename SW>
 __device__ int select_large(const StepLaunch& a, int q, BeamTab& bt, SW& sw, uint32_t* buf, int cap,
                             bool tile_z_ready = false) {
-  const bool full = !(a.mode == kSelSparse || a.mode == kSelDense);
+  const bool need_z = (a.part == nullptr);  // tile maxima come from partials when there are any
   int rt, tw;
   tile_layout(a.Wc, a.S, cap, &rt, &tw);
-  if (a.Wc * rt <= cap / 2 && (!full || tile_z_ready)) {
+  if (a.Wc * rt <= cap / 2 && (!need_z || tile_z_ready)) {
     const int nrep = tile_rep_keys<NT>(a, q, bt, buf, rt, tw);
     const int n = cta_select_filtered<NT>(a, q, bt, sw, buf, cap, nrep);
     if (n >= 0) return n;
@@ -224,7 +224,8 @@ __global__ void __launch_bounds__(256) k_gather_add(const __grid_constant__ Step
 // ---------------------------------------------------------------------------
 template <typename WT>
 __global__ void __launch_bounds__(256) k_full_simt(const float* __restrict__ H, const WT* __restrict__ W,
-                                                   float* __restrict__ Z, int M, int V, int d, int ldz) {
+                                                   float* __restrict__ Z, int M, int V, int d, int ldz,
+                                                   const FullEpi epi) {
   constexpr int BM = 64, BN = 64, BK = 16;
   __shared__ float As[BK][BM + 4];
   __shared__ float Bs[BK][BN + 4];
@@ -292,6 +293,30 @@ __global__ void __launch_bounds__(256) k_full_simt(const float* __restrict__ H, 
       if (n < V) Z[(size_t)m * ldz + n] = acc[i][j];
     }
   }
+  if (epi.part) {
+    // legal-only (max, sum exp) of each 32-token chunk: 8 threads (4 tokens
+    // each) share a chunk; lanes tx^1, tx^2, tx^4 hold its other tokens
+    const int chunk = (n0 >> 5) + (tx >> 3);
+    const int sh = (tx & 7) * 4;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int m = m0 + ty * 4 + i;
+      const uint32_t lm = (m < M) ? (epi_legal_mask(epi, m, chunk, V) >> sh) & 0xFu : 0u;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mx = ((lm >> j) & 1u) ? fmaxf(mx, acc[i][j]) : mx;
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+      float sm = 0.f;
+      if (mx != -INFINITY) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sm += ((lm >> j) & 1u) ? expf(acc[i][j] - mx) : 0.f;
+      }
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) sm += __shfl_xor_sync(0xFFFFFFFFu, sm, o);
+      if ((tx & 7) == 0 && m < M && chunk * 32 < V) epi.part[(size_t)m * (ldz >> 5) + chunk] = make_float2(mx, sm);
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -306,9 +331,9 @@ __global__ void __launch_bounds__(kSelThreads) k_select(const __grid_constant__ 
   const bool staged = bt.total <= kSelCap;
   int rt, tw;
   tile_layout(a.Wc, a.S, kSelCap, &rt, &tw);
-  const bool full = !(a.mode == kSelSparse || a.mode == kSelDense);
-  // tile maxima of full scores land in keys[] while the log-sum-exp is computed
-  beam_lse<kSelThreads>(a, q, bt, (!staged && full && a.Wc * rt <= kSelCap / 2) ? keys : nullptr, rt, tw);
+  // without partials (full scores of a sparse step) the tile maxima land in
+  // keys[] while the log-sum-exp is computed
+  beam_lse<kSelThreads>(a, q, bt, (!staged && !a.part && a.Wc * rt <= kSelCap / 2) ? keys : nullptr, rt, tw);
   __syncthreads();
   int n;
   if (staged) {
@@ -491,19 +516,19 @@ cudaError_t launch_gather_add(const StepLaunch& a, float* H, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_full_simt(const StepLaunch& a, const float* H, cudaStream_t st) {
+cudaError_t launch_full_simt(const StepLaunch& a, const float* H, const FullEpi& epi, cudaStream_t st) {
   const int M = a.B * a.Wc;
   dim3 grid((a.V + 63) / 64, (M + 63) / 64);
   switch (a.w_dtype) {
     case ZG_F32:
-      k_full_simt<float><<<grid, 256, 0, st>>>(H, static_cast<const float*>(a.W), a.Z, M, a.V, a.d, a.S);
+      k_full_simt<float><<<grid, 256, 0, st>>>(H, static_cast<const float*>(a.W), a.Z, M, a.V, a.d, a.S, epi);
       break;
     case ZG_BF16:
       k_full_simt<__nv_bfloat16><<<grid, 256, 0, st>>>(H, static_cast<const __nv_bfloat16*>(a.W), a.Z, M, a.V,
-                                                       a.d, a.S);
+                                                       a.d, a.S, epi);
       break;
     default:
-      k_full_simt<__half><<<grid, 256, 0, st>>>(H, static_cast<const __half*>(a.W), a.Z, M, a.V, a.d, a.S);
+      k_full_simt<__half><<<grid, 256, 0, st>>>(H, static_cast<const __half*>(a.W), a.Z, M, a.V, a.d, a.S, epi);
       break;
   }
   return cudaGetLastError();

@@ -124,7 +124,7 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
 __global__ void __launch_bounds__(kThreads, 1)
     k_full_tc(const __grid_constant__ CUtensorMap map_hi, const __grid_constant__ CUtensorMap map_lo,
               const __grid_constant__ CUtensorMap map_w, float* __restrict__ Z, int M, int V, int d, int ldz,
-              uint32_t ab_type, uint32_t* status) {
+              uint32_t ab_type, const FullEpi epi, uint32_t* status) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // stage buffers must sit on 1024-byte boundaries (swizzle atoms)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -217,13 +217,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c0 = 0; c0 < kBN; c0 += 32) {
         float v[32];
         tmem_ld32(lane_addr + (uint32_t)c0, v);
-        if (row < M) {
+        if (row < M && n0 + c0 < V) {
           float* zr = Z + (size_t)row * ldz + n0 + c0;
           if (n0 + c0 + 32 <= V) {
 #pragma unroll
             for (int i = 0; i < 32; i += 4) *reinterpret_cast<float4*>(zr + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
           } else {
             for (int i = 0; i < 32 && n0 + c0 + i < V; ++i) zr[i] = v[i];
+          }
+          if (epi.part) {
+            // legal-only (max, sum exp) of this 32-token chunk
+            const int chunk = (n0 + c0) >> 5;
+            const uint32_t lm = epi_legal_mask(epi, row, chunk, V);
+            float mx = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) mx = ((lm >> i) & 1u) ? fmaxf(mx, v[i]) : mx;
+            float sm = 0.f;
+            if (mx != -INFINITY) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) sm += ((lm >> i) & 1u) ? expf(v[i] - mx) : 0.f;
+            }
+            epi.part[(size_t)row * (ldz >> 5) + chunk] = make_float2(mx, sm);
           }
         }
       }
@@ -315,7 +329,7 @@ cudaError_t launch_split_h(const float* H, void* hi, void* lo, size_t n, int w_d
 }
 
 cudaError_t launch_full_tc(const void* hi, const void* lo, const void* W, float* Z, int M, int V, int d, int ldz,
-                           int w_dtype, uint32_t* status, cudaStream_t st) {
+                           int w_dtype, const FullEpi& epi, uint32_t* status, cudaStream_t st) {
   const bool bf16 = (w_dtype == ZG_BF16);
   CUtensorMap mh, ml, mw;
   if (!make_map(&mh, hi, M, d, kBM, bf16) || !make_map(&ml, lo, M, d, kBM, bf16) ||
@@ -329,7 +343,7 @@ cudaError_t launch_full_tc(const void* hi, const void* lo, const void* W, float*
     attr_done = true;
   }
   dim3 grid((V + kBN - 1) / kBN, (M + kBM - 1) / kBM);
-  k_full_tc<<<grid, kThreads, smem, st>>>(mh, ml, mw, Z, M, V, d, ldz, bf16 ? 1u : 0u, status);
+  k_full_tc<<<grid, kThreads, smem, st>>>(mh, ml, mw, Z, M, V, d, ldz, bf16 ? 1u : 0u, epi, status);
   return cudaGetLastError();
 }
 

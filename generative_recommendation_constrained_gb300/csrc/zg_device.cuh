@@ -436,7 +436,7 @@ __device__ void beam_lse_sel(const StepLaunch& a, int q, BeamTab& bt, const floa
 __host__ __device__ __forceinline__ void tile_layout(int Wc, int S, int cap, int* rt, int* tw) {
   int max_rt = (cap / 2) / (Wc > 0 ? Wc : 1);
   if (max_rt < 1) max_rt = 1;
-  int r = (S + 255) / 256;
+  int r = (S + 31) / 32;
   if (r > max_rt) r = max_rt;
   if (r < 1) r = 1;
   *rt = r;
@@ -451,7 +451,7 @@ __host__ __device__ __forceinline__ void tile_layout(int Wc, int S, int cap, int
 template <int NT>
 __device__ void beam_lse(const StepLaunch& a, int q, BeamTab& bt, uint32_t* rep_z = nullptr, int rt = 0,
                          int tw = 256) {
-  if (a.mode == kSelSparse || a.mode == kSelDense) {
+  if (a.part) {  // selective steps, and full steps whose epilogue wrote chunk partials
     beam_lse_sel<NT>(a, q, bt, nullptr);
     return;
   }
@@ -691,7 +691,7 @@ __device__ int cta_select_filtered(const StepLaunch& a, int q, BeamTab& bt, SW& 
 // representatives (Wc * rt).
 template <int NT>
 __device__ int tile_rep_keys(const StepLaunch& a, int q, const BeamTab& bt, uint32_t* rep, int rt, int tw) {
-  const bool sel = (a.mode == kSelSparse || a.mode == kSelDense);
+  const bool sel = (a.part != nullptr);  // chunk partials exist
   const int n = a.Wc * rt;
   const int cpt = tw / kChunk;  // chunks a tile
   for (int i = threadIdx.x; i < n; i += NT) {

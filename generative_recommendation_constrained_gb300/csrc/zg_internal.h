@@ -84,10 +84,35 @@ struct StepLaunch {
   uint32_t* status;        // device status word
 };
 
+// What the full-projection epilogues write besides the scores: for every
+// 32-token chunk of every beam row, (max, sum exp(z - max)) over the legal
+// tokens of the chunk, the same partials the selective kernels produce.
+struct FullEpi {
+  float2* part;            // [M][ldz/32], or null (no partials)
+  const uint32_t* bitmap;  // dense step's bitmap rows; null: every token < V is legal
+  const uint32_t* rows;    // [M] index row of each beam (kDeadRow: dead); null: row 0
+  int words;               // bitmap words a row
+};
+
+#ifdef __CUDACC__
+// Legal tokens of chunk `chunk` of beam row `m` as a 32-bit mask.
+__device__ __forceinline__ uint32_t epi_legal_mask(const FullEpi& e, int m, int chunk, int V) {
+  uint32_t mask = 0xFFFFFFFFu;
+  if (e.bitmap) {
+    const uint32_t r = e.rows ? e.rows[m] : 0u;
+    if (r == kDeadRow) return 0u;
+    mask = e.bitmap[(size_t)r * e.words + chunk];
+  }
+  const int rem = V - chunk * 32;
+  if (rem < 32) mask &= (rem <= 0) ? 0u : ((1u << rem) - 1u);
+  return mask;
+}
+#endif
+
 // kernels (kernels.cu)
 cudaError_t launch_selective(const StepLaunch& a, cudaStream_t st);
 cudaError_t launch_gather_add(const StepLaunch& a, float* H, cudaStream_t st);
-cudaError_t launch_full_simt(const StepLaunch& a, const float* H, cudaStream_t st);
+cudaError_t launch_full_simt(const StepLaunch& a, const float* H, const FullEpi& epi, cudaStream_t st);
 cudaError_t launch_select(const StepLaunch& a, cudaStream_t st);
 // A device region the fused kernel prefetches into L2 (16-byte aligned).
 struct PrefetchRegion {
@@ -104,7 +129,7 @@ cudaError_t status_word(uint32_t** dev_ptr);   // per-device status word address
 // tensor-core full projection (kernels_tc.cu): H = hi + lo in W's half type
 cudaError_t launch_split_h(const float* H, void* hi, void* lo, size_t n, int w_dtype, cudaStream_t st);
 cudaError_t launch_full_tc(const void* hi, const void* lo, const void* W, float* Z, int M, int V, int d, int ldz,
-                           int w_dtype, uint32_t* status, cudaStream_t st);
+                           int w_dtype, const FullEpi& epi, uint32_t* status, cudaStream_t st);
 // Work counts of the beams entering a step (tracing only): counters[0..3] =
 // live beams, legal slots, chunks, index bytes; mask = V-bit set of touched
 // tokens.  Both must be zeroed by the caller.
