@@ -47,7 +47,7 @@ __device__ int select_large(const StepLaunch& a, int q, BeamTab& bt, SW& sw, uin
   tile_layout(a.Wc, a.S, cap, &rt, &tw);
   if (a.Wc * rt <= cap / 2 && (!need_z || tile_z_ready)) {
     const int nrep = tile_rep_keys<NT>(a, q, bt, buf, rt, tw);
-    const int n = cta_select_filtered<NT>(a, q, bt, sw, buf, cap, nrep);
+    const int n = cta_select_filtered<NT>(a, q, bt, sw, buf, cap, nrep, rt, tw);
     if (n >= 0) return n;
   }
   return cta_select<NT>(a, q, bt, sw, buf, kGlobal);
@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(256) k_full_simt(const float* __restrict__ H, 
       float sm = 0.f;
       if (mx != -INFINITY) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) sm += ((lm >> j) & 1u) ? expf(acc[i][j] - mx) : 0.f;
+        for (int j = 0; j < 4; ++j) sm += ((lm >> j) & 1u) ? __expf(acc[i][j] - mx) : 0.f;
       }
 #pragma unroll
       for (int o = 1; o < 8; o <<= 1) sm += __shfl_xor_sync(0xFFFFFFFFu, sm, o);

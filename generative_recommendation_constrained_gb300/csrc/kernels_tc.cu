@@ -226,7 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32 && n0 + c0 + i < V; ++i) zr[i] = v[i];
           }
           if (epi.part) {
-            // legal-only (max, sum exp) of this 32-token chunk
+            // legal-only (max, sum exp) of this 32-token chunk (the fast
+            // exponential: ~1e-6 relative, far inside the score tolerance)
             const int chunk = (n0 + c0) >> 5;
             const uint32_t lm = epi_legal_mask(epi, row, chunk, V);
             float mx = -INFINITY;
@@ -235,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float sm = 0.f;
             if (mx != -INFINITY) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) sm += ((lm >> i) & 1u) ? expf(v[i] - mx) : 0.f;
+              for (int i = 0; i < 32; ++i) sm += ((lm >> i) & 1u) ? __expf(v[i] - mx) : 0.f;
             }
             epi.part[(size_t)row * (ldz >> 5) + chunk] = make_float2(mx, sm);
           }

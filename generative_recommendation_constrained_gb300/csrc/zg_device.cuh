@@ -489,9 +489,13 @@ __device__ void beam_lse(const StepLaunch& a, int q, BeamTab& bt, uint32_t* rep_
 }
 
 // Key of flat candidate c (0 = illegal slot).
+__device__ __forceinline__ uint32_t cand_key_kj(const StepLaunch& a, const BeamTab& bt, int q, int k, int j);
 __device__ __forceinline__ uint32_t cand_key(const StepLaunch& a, const BeamTab& bt, int q, int c) {
   const int k = upper_find(bt.start, a.Wc, c);
-  const int j = c - bt.start[k];
+  return cand_key_kj(a, bt, q, k, c - bt.start[k]);
+}
+// Key of slot j of beam k (0 = illegal slot).
+__device__ __forceinline__ uint32_t cand_key_kj(const StepLaunch& a, const BeamTab& bt, int q, int k, int j) {
   const size_t zb = (size_t)q * a.zq + (size_t)k * a.S;
   float z;
   switch (a.mode) {
@@ -619,18 +623,18 @@ __device__ uint32_t cta_kth(const uint32_t* keys, int n, int kth, SW& sw) {
 }
 
 // Select when the request's candidates do not fit in shared memory.  rep[0,
-// nrep) holds the keys of true candidates (tile maxima); the keep-th largest
-// of them is a lower bound on the keep-th largest candidate, so one pass over
-// the global slot buffer keeps only candidates at or above it, as
-// (key << 32 | ~flat), in buf after rep; they are bitonic-sorted descending
+// nrep) holds, for tile t (tw slots) of beam k at k*rt + t, the key of the
+// tile's best candidate; the keep-th largest of them is a lower bound on the
+// keep-th largest candidate, so only tiles whose best clears it are read from
+// the global slot buffer, and their candidates at or above it are kept as
+// (key << 32 | ~flat) in buf after rep; they are bitonic-sorted descending
 // and the first keep become the winners.  Returns -1 (nothing written) when
 // more candidates pass than the space holds; the caller then runs the full
 // radix select.
 template <int NT, typename SW>
 __device__ int cta_select_filtered(const StepLaunch& a, int q, BeamTab& bt, SW& sw, uint32_t* buf, int cap,
-                                   int nrep) {
-  const int tid = threadIdx.x;
-  const int total = bt.total;
+                                   int nrep, int rt, int tw) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int keep_n = min(a.keep, bt.nlegal);
   if (keep_n == 0) return 0;
   __syncthreads();
@@ -641,18 +645,18 @@ __device__ int cta_select_filtered(const StepLaunch& a, int q, BeamTab& bt, SW& 
   while (lcap * 2 <= (cap - off) / 2) lcap *= 2;  // power of two, for the sort
   if (tid == 0) sw.nwin = 0;
   __syncthreads();
-  for (int c0 = tid; c0 < total; c0 += 4 * NT) {
-    uint32_t kk[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int c = c0 + u * NT;
-      kk[u] = (c < total) ? cand_key(a, bt, q, c) : 0u;
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      if (kk[u] && kk[u] >= tlb) {
+  // a tile whose best candidate is below the bound holds no winner: only the
+  // tiles at or above it are read (one warp a tile)
+  for (int i = warp; i < nrep; i += NT / 32) {
+    if (buf[i] < tlb || buf[i] == 0u) continue;
+    const int k = i / rt, t = i - k * rt;
+    const int j1 = min((t + 1) * tw, bt.cnt[k]);
+    for (int j = t * tw + lane; j < j1; j += 32) {
+      const uint32_t key = cand_key_kj(a, bt, q, k, j);
+      if (key && key >= tlb) {
         const int pos = atomicAdd(&sw.nwin, 1);
-        if (pos < lcap) list[pos] = ((unsigned long long)kk[u] << 32) | (0xFFFFFFFFu - (uint32_t)(c0 + u * NT));
+        if (pos < lcap)
+          list[pos] = ((unsigned long long)key << 32) | (0xFFFFFFFFu - (uint32_t)(bt.start[k] + j));
       }
     }
   }
