@@ -36,12 +36,20 @@ constexpr int kClusterCap = 11264;   // slot scores / keys held by the cluster k
 constexpr int kClusterPcap = 2048;   // chunk partials and masks held by the rank-0 CTA
 
 // Select when the candidates do not fit in shared memory: filtered select
-// on 256-slot tile maxima when those fit in half the buffer, else the radix
-// select over the global slot buffer.  For full-score steps beam_lse has
-// already stored the tile maxima in buf when tile_z_ready.
+// on the maxima of the scored 32-slot chunks when there are chunk partials
+// and their count fits in half the buffer, else on the maxima of tiles of
+// whole chunks, else the radix select over the global slot buffer.  For
+// full-score steps without chunk partials beam_lse has already stored the
+// tile maxima in buf when tile_z_ready.
 template <int NT, typename SW>
 __device__ int select_large(const StepLaunch& a, int q, BeamTab& bt, SW& sw, uint32_t* buf, int cap,
                             bool tile_z_ready = false) {
+  if (a.part && bt.istart[a.Wc] <= cap / 2) {
+    const int nrep = chunk_rep_keys<NT>(a, q, bt, buf);
+    const int n = cta_select_filtered<NT>(a, q, bt, sw, buf, cap, nrep, 0, kChunk);
+    if (n >= 0) return n;
+    return cta_select<NT>(a, q, bt, sw, buf, kGlobal);
+  }
   const bool need_z = (a.part == nullptr);  // tile maxima come from partials when there are any
   int rt, tw;
   tile_layout(a.Wc, a.S, cap, &rt, &tw);
@@ -171,17 +179,23 @@ __global__ void __launch_bounds__(kClusterThreads, 2) k_decode_cluster(const __g
       int n;
       if (in_smem) {
         beam_lse_sel<NT>(a, q, bt, psm);
-        n = cta_select<NT>(a, q, bt, sw, zsm, kZStaged);  // its first barrier publishes the lse
+        // chunk beams and keys replace the spent partials in place
+        n = cta_select_chunks<NT>(a, q, bt, sw, psm, reinterpret_cast<const float*>(zsm),
+                                  reinterpret_cast<uint32_t*>(psm) + 1, reinterpret_cast<uint32_t*>(psm), 2);
+        if (n < 0) n = cta_select_bins<NT>(a, q, bt, sw, zsm, kZStaged);
         write_survivors<NT>(a, q, bt, sw, n, msm);
       } else {
         beam_lse<NT>(a, q, bt);
         __syncthreads();
-        const bool staged = bt.total <= A.cap;
-        if (staged) {
-          stage_keys_global<NT>(a, q, bt, zsm);
-          n = cta_select<NT>(a, q, bt, sw, zsm, kKeysStaged);
-        } else {
-          n = select_large<NT>(a, q, bt, sw, zsm, A.cap);
+        const int ni = bt.istart[a.Wc];
+        n = (a.part && 2 * ni <= A.cap) ? cta_select_chunks<NT>(a, q, bt, sw, nullptr, nullptr, zsm, zsm + ni, 1) : -1;
+        if (n < 0) {
+          if (bt.total <= A.cap) {
+            stage_keys_global<NT>(a, q, bt, zsm);
+            n = cta_select_bins<NT>(a, q, bt, sw, zsm, kKeysStaged);
+          } else {
+            n = select_large<NT>(a, q, bt, sw, zsm, A.cap);
+          }
         }
         write_survivors<NT>(a, q, bt, sw, n);
       }
@@ -335,12 +349,16 @@ __global__ void __launch_bounds__(kSelThreads) k_select(const __grid_constant__ 
   // keys[] while the log-sum-exp is computed
   beam_lse<kSelThreads>(a, q, bt, (!staged && !a.part && a.Wc * rt <= kSelCap / 2) ? keys : nullptr, rt, tw);
   __syncthreads();
-  int n;
-  if (staged) {
-    stage_keys_global<kSelThreads>(a, q, bt, keys);
-    n = cta_select<kSelThreads>(a, q, bt, sw, keys, kKeysStaged);
-  } else {
-    n = select_large<kSelThreads>(a, q, bt, sw, keys, kSelCap, true);
+  const int ni = bt.istart[a.Wc];
+  int n = (a.part && 2 * ni <= kSelCap)
+              ? cta_select_chunks<kSelThreads>(a, q, bt, sw, nullptr, nullptr, keys, keys + ni, 1) : -1;
+  if (n < 0) {
+    if (staged) {
+      stage_keys_global<kSelThreads>(a, q, bt, keys);
+      n = cta_select_bins<kSelThreads>(a, q, bt, sw, keys, kKeysStaged);
+    } else {
+      n = select_large<kSelThreads>(a, q, bt, sw, keys, kSelCap, true);
+    }
   }
   write_survivors<kSelThreads>(a, q, bt, sw, n);
 }

@@ -301,11 +301,15 @@ struct BeamTab {
   int start[ZG_MAX_BEAM + 1];  // flat candidate prefix
   int istart[ZG_MAX_BEAM + 1]; // chunk prefix
   int total, nlegal;
+  // from the chunk partials (beam_lse_sel): the largest and the smallest
+  // chunk-maximum key and the number of chunks holding a legal candidate
+  uint32_t kceil, kfloor;
+  int nne;
 };
 
 template <int NW>
 struct SelWorkT {
-  uint32_t whist[NW][256];  // private radix histogram of each warp
+  alignas(16) uint32_t whist[NW][256];  // private radix histogram of each warp (or a histogram / list)
   unsigned long long win[ZG_MAX_BEAM];
   int warp_tot[32];
   uint32_t prefix, prefmask;
@@ -394,38 +398,75 @@ __device__ void build_beam_table(const StepLaunch& a, int q, BeamTab& bt) {
       bt.istart[a.Wc] = ii;
       bt.total = ic;
       bt.nlegal = il;
+      bt.kceil = 0u;
+      bt.kfloor = 0xFFFFFFFFu;
+      bt.nne = 0;
     }
   }
   __syncthreads();
 }
 
-// Legal-only log-sum-exp of every live beam from its selective chunk
-// partials (m_c, s_c): lse = M + log(sum_c s_c exp(m_c - M)), M = max_c m_c.
-// Eight lanes a beam (four beams a warp at once), two passes over the
-// partials, width-8 shuffle reductions.  Partials come from shared memory
-// by item (psm) or from the global partial buffer (psm == nullptr).
+// Legal-only log-sum-exp of every live beam from its chunk partials (m_c,
+// s_c): lse = M + log(sum_c s_c exp(m_c - M)), M = max_c m_c.  Eight lanes a
+// beam, eight beams a warp at once (two a lane group, their first partials
+// loaded together and kept for the second pass), width-8 shuffle reductions.
+// Partials come from shared memory by item (psm) or from the global partial
+// buffer (psm == nullptr).  Also folds into bt.kceil / bt.kfloor / bt.nne the
+// keys of each beam's best and weakest non-empty chunk maximum and its
+// number of non-empty chunks.
 template <int NT>
 __device__ void beam_lse_sel(const StepLaunch& a, int q, BeamTab& bt, const float2* psm) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int sub = lane >> 3, sl = lane & 7;
-  for (int k0 = warp * 4; k0 < a.Wc; k0 += (NT / 32) * 4) {
-    const int k = k0 + sub;
-    const bool live = (k < a.Wc) && bt.cnt[k] > 0;
-    const int n = live ? bt.items[k] : 0;
-    const float2* pp = psm ? psm + (live ? bt.istart[k] : 0)
-                           : a.part + (size_t)q * a.pq + (size_t)(live ? k : 0) * a.nch;
-    float m = -INFINITY;
-    for (int c = sl; c < n; c += 8) m = fmaxf(m, pp[c].x);
+  for (int k0 = warp * 8; k0 < a.Wc; k0 += (NT / 32) * 8) {
+    int kb[2], n[2];
+    const float2* pp[2];
+    float2 p0[2];
 #pragma unroll
-    for (int o = 4; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-    float sum = 0.f;
-    for (int c = sl; c < n; c += 8) {
-      const float2 p = pp[c];
-      if (p.y > 0.f) sum += p.y * expf(p.x - m);
+    for (int h = 0; h < 2; ++h) {
+      const int k = k0 + 4 * h + sub;
+      const bool live = (k < a.Wc) && bt.cnt[k] > 0;
+      kb[h] = k;
+      n[h] = live ? bt.items[k] : 0;
+      pp[h] = psm ? psm + (live ? bt.istart[k] : 0) : a.part + (size_t)q * a.pq + (size_t)(live ? k : 0) * a.nch;
+      p0[h] = (sl < n[h]) ? pp[h][sl] : make_float2(-INFINITY, 0.f);
     }
 #pragma unroll
-    for (int o = 4; o; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
-    if (live && sl == 0) bt.lse[k] = m + logf(sum);
+    for (int h = 0; h < 2; ++h) {
+      float m = p0[h].x, mn = (p0[h].y > 0.f) ? p0[h].x : INFINITY;
+      int ne = (p0[h].y > 0.f) ? 1 : 0;  // a chunk with a legal candidate has sum >= 1
+      for (int c = sl + 8; c < n[h]; c += 8) {
+        const float2 p = pp[h][c];
+        m = fmaxf(m, p.x);
+        if (p.y > 0.f) {
+          mn = fminf(mn, p.x);
+          ++ne;
+        }
+      }
+#pragma unroll
+      for (int o = 4; o; o >>= 1) {
+        m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+        mn = fminf(mn, __shfl_xor_sync(kFull, mn, o));
+        ne += __shfl_xor_sync(kFull, ne, o);
+      }
+      float sum = (p0[h].y > 0.f) ? p0[h].y * expf(p0[h].x - m) : 0.f;
+      for (int c = sl + 8; c < n[h]; c += 8) {
+        const float2 p = pp[h][c];
+        if (p.y > 0.f) sum += p.y * expf(p.x - m);
+      }
+#pragma unroll
+      for (int o = 4; o; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
+      const int k = kb[h];
+      if (n[h] > 0 && sl == 0) {
+        const float lse = m + logf(sum);
+        bt.lse[k] = lse;
+        if (ne > 0) {  // keys of the beam's best and of its weakest chunk maximum, as the select computes them
+          atomicMax(&bt.kceil, f2ord(bt.cum[k] + (m - lse)));
+          atomicMin(&bt.kfloor, f2ord(bt.cum[k] + (mn - lse)));
+          atomicAdd(&bt.nne, ne);
+        }
+      }
+    }
   }
 }
 
@@ -514,15 +555,6 @@ __device__ __forceinline__ uint32_t cand_key_kj(const StepLaunch& a, const BeamT
   return f2ord(bt.cum[k] + (z - bt.lse[k]));
 }
 
-// ---------------------------------------------------------------------------
-// CTA-level select of the keep best legal candidates of request q: keys are
-// staged in shared memory when they fit (`cap` entries), then 8-bit radix
-// passes with warp-aggregated histograms narrow the threshold key (stopping
-// as soon as the threshold bin holds exactly the remainder), winners above
-// the threshold are collected, threshold ties go to the lowest flat slot
-// indices, and the winners are bitonic-sorted by (score desc, flat asc).
-// Leaves sw.win[0..n) sorted; returns n = min(keep, legal candidates).
-// ---------------------------------------------------------------------------
 // Stage the keys of every candidate in shared memory (four independent
 // candidates a thread in flight).
 template <int NT>
@@ -555,6 +587,36 @@ __device__ __forceinline__ unsigned long long warp_sort_desc(unsigned long long 
     }
   }
   return v;
+}
+
+// Descending bitonic sort of list[0, P) in shared memory by the CTA (P a
+// power of two).  Entry block [32w', 32w' + 32) is always handled by one
+// warp, so a stage whose pairs stay inside a block, and whose successor does
+// too, needs only that warp's barrier.  Returns after __syncthreads.
+template <int NT>
+__device__ void cta_bitonic_desc(unsigned long long* list, int P) {
+  const int tid = threadIdx.x;
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = tid; i < P; i += NT) {
+        const int jx = i ^ stride;
+        if (jx > i) {
+          const bool desc = ((i & size) == 0);
+          const unsigned long long x = list[i], y = list[jx];
+          if (desc ? (x < y) : (x > y)) {
+            list[i] = y;
+            list[jx] = x;
+          }
+        }
+      }
+      const int next = (stride > 1) ? (stride >> 1) : size;  // stride of the following stage
+      if (stride >= 32 || next >= 32)
+        __syncthreads();
+      else
+        __syncwarp();
+    }
+  }
+  __syncthreads();
 }
 
 // k-th largest (1 <= kth <= n) of the non-zero keys[0..n) in shared memory:
@@ -623,8 +685,9 @@ __device__ uint32_t cta_kth(const uint32_t* keys, int n, int kth, SW& sw) {
 }
 
 // Select when the request's candidates do not fit in shared memory.  rep[0,
-// nrep) holds, for tile t (tw slots) of beam k at k*rt + t, the key of the
-// tile's best candidate; the keep-th largest of them is a lower bound on the
+// nrep) holds, for tile t (tw slots) of beam k at k*rt + t (or, with rt = 0,
+// for the i-th scored 32-slot chunk of the request), the key of the tile's
+// best candidate; the keep-th largest of them is a lower bound on the
 // keep-th largest candidate, so only tiles whose best clears it are read from
 // the global slot buffer, and their candidates at or above it are kept as
 // (key << 32 | ~flat) in buf after rep; they are bitonic-sorted descending
@@ -649,9 +712,16 @@ __device__ int cta_select_filtered(const StepLaunch& a, int q, BeamTab& bt, SW& 
   // tiles at or above it are read (one warp a tile)
   for (int i = warp; i < nrep; i += NT / 32) {
     if (buf[i] < tlb || buf[i] == 0u) continue;
-    const int k = i / rt, t = i - k * rt;
-    const int j1 = min((t + 1) * tw, bt.cnt[k]);
-    for (int j = t * tw + lane; j < j1; j += 32) {
+    int k, j0;
+    if (rt > 0) {
+      k = i / rt;
+      j0 = (i - k * rt) * tw;
+    } else {  // one 32-slot chunk a representative, numbered by the chunk prefix
+      k = upper_find(bt.istart, a.Wc, i);
+      j0 = (i - bt.istart[k]) * kChunk;
+    }
+    const int j1 = min(j0 + tw, bt.cnt[k]);
+    for (int j = j0 + lane; j < j1; j += 32) {
       const uint32_t key = cand_key_kj(a, bt, q, k, j);
       if (key && key >= tlb) {
         const int pos = atomicAdd(&sw.nwin, 1);
@@ -667,22 +737,7 @@ __device__ int cta_select_filtered(const StepLaunch& a, int q, BeamTab& bt, SW& 
   while (P < nl) P <<= 1;
   for (int i = nl + tid; i < P; i += NT) list[i] = 0ull;
   __syncthreads();
-  for (int size = 2; size <= P; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = tid; i < P; i += NT) {
-        const int jx = i ^ stride;
-        if (jx > i) {
-          const bool desc = ((i & size) == 0);
-          const unsigned long long x = list[i], y = list[jx];
-          if (desc ? (x < y) : (x > y)) {
-            list[i] = y;
-            list[jx] = x;
-          }
-        }
-      }
-      __syncthreads();
-    }
-  }
+  cta_bitonic_desc<NT>(list, P);
   for (int i = tid; i < keep_n; i += NT) sw.win[i] = list[i];
   __syncthreads();
   return keep_n;
@@ -714,6 +769,21 @@ __device__ int tile_rep_keys(const StepLaunch& a, int q, const BeamTab& bt, uint
       if (m != -INFINITY) key = f2ord(bt.cum[k] + (m - bt.lse[k]));
     }
     rep[i] = key;
+  }
+  __syncthreads();
+  return n;
+}
+
+// Keys of the scored chunks of a step with chunk partials as representatives
+// for cta_select_filtered (rt = 0): rep[i] for the i-th chunk of the request
+// in beam order, from the chunk's partial maximum.  Returns the chunk count.
+template <int NT>
+__device__ int chunk_rep_keys(const StepLaunch& a, int q, const BeamTab& bt, uint32_t* rep) {
+  const int n = bt.istart[a.Wc];
+  for (int i = threadIdx.x; i < n; i += NT) {
+    const int k = upper_find(bt.istart, a.Wc, i);
+    const float m = a.part[(size_t)q * a.pq + (size_t)k * a.nch + (i - bt.istart[k])].x;
+    rep[i] = (m != -INFINITY) ? f2ord(bt.cum[k] + (m - bt.lse[k])) : 0u;
   }
   __syncthreads();
   return n;
@@ -878,22 +948,307 @@ __device__ int cta_select(const StepLaunch& a, int q, BeamTab& bt, SW& sw, uint3
   while (P < keep_n) P <<= 1;
   for (int i = keep_n + tid; i < P; i += NT) sw.win[i] = 0ull;
   __syncthreads();
-  for (int size = 2; size <= P; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = tid; i < P; i += NT) {
-        const int jx = i ^ stride;
-        if (jx > i) {
-          const bool desc = ((i & size) == 0);
-          const unsigned long long x = sw.win[i], y = sw.win[jx];
-          if (desc ? (x < y) : (x > y)) {
-            sw.win[i] = y;
-            sw.win[jx] = x;
+  cta_bitonic_desc<NT>(sw.win, P);
+  return keep_n;
+}
+
+// ---------------------------------------------------------------------------
+// Histogram-cut selects.  Keys are cut by 2048 bins over a key range [lo, hi]
+// (bin = min((key - lo) >> sh, 2047), sh the smallest shift that maps hi -
+// lo below 2048): the bin where the count from the top reaches the target
+// bounds the winners from below, and every key outside that bin and the bins
+// above it is out.  The bin map is monotone, so the cut is exact.
+// ---------------------------------------------------------------------------
+constexpr int kBins = 2048;
+
+__device__ __forceinline__ int bin_shift(uint32_t lo, uint32_t hi) {
+  const uint32_t R = hi - lo;
+  return (R < (uint32_t)kBins) ? 0 : (32 - __clz(R) - 11);
+}
+__device__ __forceinline__ uint32_t bin_of(uint32_t key, uint32_t lo, int sh) {
+  return min((key - lo) >> sh, (uint32_t)(kBins - 1));
+}
+
+// Cut of a complete histogram (every thread past the barrier that completed
+// it): the bin b where the count of the bins above stays below target and
+// with b reaches it goes to sw.prefix, the count above to sw.cnt_gt, the
+// count in b to sw.cnt_eq, and sw.nwin is zeroed.  Returns the histogram's
+// total (the same in every thread; sw is not written when it is below
+// target).  Thread t scans bins [top - PER, top), top = 2048 - PER * t, from
+// the top.  On return every thread may overwrite the histogram.
+template <int NT, typename SW>
+__device__ uint32_t hist_cut(const uint32_t* hist, SW& sw, uint32_t target) {
+  constexpr int NW = NT / 32;
+  constexpr int PER = kBins / NT;
+  static_assert(PER % 4 == 0, "bins a thread");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int top = kBins - PER * tid;
+  uint32_t cnt[PER];
+#pragma unroll
+  for (int i = 0; i < PER; i += 4) {
+    const uint4 v = *reinterpret_cast<const uint4*>(&hist[top - 4 - i]);
+    cnt[i] = v.w;
+    cnt[i + 1] = v.z;
+    cnt[i + 2] = v.y;
+    cnt[i + 3] = v.x;
+  }
+  uint32_t mine = 0;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) mine += cnt[i];
+  uint32_t incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) sw.warp_tot[warp] = (int)incl;
+  __syncthreads();
+  uint32_t before = 0, all = 0;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    const uint32_t t = (uint32_t)sw.warp_tot[w];
+    before += (w < warp) ? t : 0u;
+    all += t;
+  }
+  const uint32_t excl = before + incl - mine;
+  if (all >= target && excl < target && excl + mine >= target) {
+    uint32_t run = excl;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      if (run + cnt[i] >= target) {
+        sw.prefix = (uint32_t)(top - 1 - i);
+        sw.cnt_gt = (int)run;
+        sw.cnt_eq = (int)cnt[i];
+        break;
+      }
+      run += cnt[i];
+    }
+    sw.nwin = 0;
+  }
+  __syncthreads();
+  return all;
+}
+
+// Append (key << 32 | ~flat) of the lanes with f set to list (warp-wide).
+__device__ __forceinline__ void warp_append(unsigned long long* list, int lcap, int& nwin, bool f, uint32_t key,
+                                            int flat, int lane) {
+  const unsigned bal = __ballot_sync(kFull, f);
+  if (!bal) return;
+  int pos = 0;
+  if (lane == 0) pos = atomicAdd(&nwin, __popc(bal));
+  pos = __shfl_sync(kFull, pos, 0) + __popc(bal & ((1u << lane) - 1u));
+  if (f && pos < lcap) list[pos] = ((unsigned long long)key << 32) | (0xFFFFFFFFu - (uint32_t)flat);
+}
+
+// The keep_n best of nl distinct list entries, in descending order, into
+// sw.win: a warp sort up to 32 entries, else every entry goes to the slot
+// given by the number of entries above it.  Returns after __syncthreads.
+template <int NT, typename SW>
+__device__ void place_winners(const unsigned long long* list, int nl, int keep_n, SW& sw) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (nl <= 32) {
+    if (warp == 0) {
+      const unsigned long long v = warp_sort_desc(lane < nl ? list[lane] : 0ull, lane);
+      if (lane < keep_n) sw.win[lane] = v;
+    }
+  } else if (nl <= NT) {
+    if (tid < nl) {
+      const unsigned long long x = list[tid];
+      int r = 0;
+      for (int j = 0; j < nl; ++j) r += (list[j] > x);
+      if (r < keep_n) sw.win[r] = x;
+    }
+  } else {
+    for (int i0 = tid; i0 < nl; i0 += 2 * NT) {
+      const int i1 = i0 + NT;
+      const unsigned long long x0 = list[i0], x1 = (i1 < nl) ? list[i1] : ~0ull;
+      int r0 = 0, r1 = 0;
+      for (int j = 0; j < nl; ++j) {
+        const unsigned long long y = list[j];
+        r0 += (y > x0);
+        r1 += (y > x1);
+      }
+      if (r0 < keep_n) sw.win[r0] = x0;
+      if (i1 < nl && r1 < keep_n) sw.win[r1] = x1;
+    }
+  }
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// CTA-level select by one histogram pass over keys in shared memory, when
+// the chunk partials gave the key range [kfloor, kceil] (the smallest and the
+// largest chunk-maximum key; kfloor is at most the keep-th largest key when
+// at least keep chunks hold a legal candidate).  One pass makes the keys
+// (from z for kZStaged) and counts them; the cut bounds the winners; one more
+// pass lists every key at or above the cut as (key << 32 | ~flat), whose
+// descending order is the tie order (score desc, flat asc).  Falls back to
+// cta_select when the range is unknown or the list does not fit.  Leaves
+// sw.win[0..n) sorted; returns n = min(keep, legal candidates).
+// ---------------------------------------------------------------------------
+template <int NT, typename SW>
+__device__ int cta_select_bins(const StepLaunch& a, int q, BeamTab& bt, SW& sw, uint32_t* keys, KeySrc src) {
+  constexpr int NW = NT / 32;
+  constexpr int LCAP = NW * 256 / 2;  // u64 list entries in the histogram's space
+  static_assert(NW * 256 >= kBins, "histogram space");
+  uint32_t* hist = &sw.whist[0][0];
+  unsigned long long* list = reinterpret_cast<unsigned long long*>(hist);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int total = bt.total;
+  const int keep_n = min(a.keep, bt.nlegal);
+  if (keep_n == 0 || src == kGlobal) return cta_select<NT>(a, q, bt, sw, keys, src);
+  for (int i = tid; i < kBins; i += NT) hist[i] = 0u;
+  __syncthreads();  // publishes the lse and the key range of beam_lse_sel (and staged keys)
+  const uint32_t lo = bt.kfloor, hi = bt.kceil;
+  if (bt.nne < keep_n || lo > hi) return cta_select<NT>(a, q, bt, sw, keys, src);
+  const int sh = bin_shift(lo, hi);
+  if (src == kZStaged) {
+    int c = tid, k = (c < total) ? upper_find(bt.start, a.Wc, c) : 0;
+    for (; c < total; c += NT) {
+      while (bt.start[k + 1] <= c) ++k;
+      const float z = __uint_as_float(keys[c]);
+      const uint32_t key = (z == -INFINITY) ? 0u : f2ord(bt.cum[k] + (z - bt.lse[k]));
+      keys[c] = key;
+      if (key >= lo) atomicAdd(&hist[bin_of(key, lo, sh)], 1u);
+    }
+  } else {
+    for (int c = tid; c < total; c += NT) {
+      const uint32_t key = keys[c];
+      if (key && key >= lo) atomicAdd(&hist[bin_of(key, lo, sh)], 1u);
+    }
+  }
+  __syncthreads();
+  const uint32_t all = hist_cut<NT>(hist, sw, (uint32_t)keep_n);
+  if (all < (uint32_t)keep_n || sw.cnt_gt + sw.cnt_eq > LCAP)  // uniform: every thread read the same counts
+    return cta_select<NT>(a, q, bt, sw, keys, kKeysStaged);
+  const uint32_t tcut = lo + (sw.prefix << sh);  // smallest key in the cut bin or above
+  const int nl = sw.cnt_gt + sw.cnt_eq;
+  for (int c0 = warp * 32; c0 < total; c0 += NT) {
+    const int c = c0 + lane;
+    const uint32_t key = (c < total) ? keys[c] : 0u;
+    warp_append(list, LCAP, sw.nwin, key && key >= tcut, key, c, lane);
+  }
+  __syncthreads();
+  place_winners<NT>(list, nl, keep_n, sw);
+  return keep_n;
+}
+
+// ---------------------------------------------------------------------------
+// Chunk-filtered select for steps with chunk partials (from shared memory
+// `ps` by chunk item, or the global partial buffer when ps is null), with the
+// slot scores in shared memory (`zs` by flat candidate) or in the global slot
+// buffer (zs null).
+//   1. Every chunk's maximum key goes to ckb[i * st] and its beam to
+//      kb[i * st]; the maxima are cut for keep: at least keep chunk maxima,
+//      all true candidates, lie at or above the cut key tc, so the keep-th
+//      largest candidate does too.
+//   2. The candidates >= tc of the chunks whose maximum reaches tc are cut
+//      again for keep over [tc, kceil]: cut key t2.
+//   3. The candidates >= t2 are listed and placed in descending order.
+// In 2 and 3 each warp tests 32 chunks at once (lane l: chunk i0 + l * NW +
+// warp) and scores the passing ones U at a time.  Returns -1 (caller falls
+// back) when the key range is unknown or the final list would not fit in the
+// histogram's space.
+// ---------------------------------------------------------------------------
+template <int NT, typename SW>
+__device__ int cta_select_chunks(const StepLaunch& a, int q, BeamTab& bt, SW& sw, const float2* ps, const float* zs,
+                                 uint32_t* ckb, uint32_t* kb, int st) {
+  constexpr int NW = NT / 32;
+  constexpr int LCAP = NW * 256 / 2;
+  constexpr int U = 4;  // chunks a warp has in flight
+  static_assert(NW * 256 >= kBins, "histogram space");
+  uint32_t* hist = &sw.whist[0][0];
+  unsigned long long* list = reinterpret_cast<unsigned long long*>(hist);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int keep_n = min(a.keep, bt.nlegal);
+  if (keep_n == 0) return 0;
+  for (int i = tid; i < kBins; i += NT) hist[i] = 0u;
+  __syncthreads();  // publishes the lse and the key range of beam_lse_sel
+  const uint32_t lo = bt.kfloor, hi = bt.kceil;
+  if (bt.nne < keep_n || lo > hi) return -1;
+  const int nitems = bt.istart[a.Wc];
+  const int sh = bin_shift(lo, hi);
+  // 1. chunk maxima (a thread reads and then overwrites its own chunks' entries)
+  for (int i0 = tid; i0 < nitems; i0 += U * NT) {
+    float2 p[U];
+    int kk[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = i0 + u * NT;
+      p[u] = make_float2(-INFINITY, 0.f);
+      kk[u] = 0;
+      if (i < nitems) {
+        kk[u] = upper_find(bt.istart, a.Wc, i);
+        p[u] = ps ? ps[i] : a.part[(size_t)q * a.pq + (size_t)kk[u] * a.nch + (i - bt.istart[kk[u]])];
+      }
+    }
+    asm volatile("" ::: "memory");  // the entries below may overwrite ps[i] in place: reads first
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = i0 + u * NT;
+      if (i >= nitems) continue;
+      const int k = kk[u];
+      const uint32_t ck = (p[u].y > 0.f) ? f2ord(bt.cum[k] + (p[u].x - bt.lse[k])) : 0u;
+      ckb[(size_t)i * st] = ck;
+      kb[(size_t)i * st] = (uint32_t)k;
+      if (ck >= lo) atomicAdd(&hist[bin_of(ck, lo, sh)], 1u);
+    }
+  }
+  __syncthreads();
+  if (hist_cut<NT>(hist, sw, (uint32_t)keep_n) < (uint32_t)keep_n) return -1;
+  const uint32_t tc = lo + (sw.prefix << sh);
+  const int sh2 = bin_shift(tc, hi);
+  for (int i = tid; i < kBins; i += NT) hist[i] = 0u;
+  __syncthreads();
+  for (int pass = 2; pass <= 3; ++pass) {
+    uint32_t t2 = 0u;
+    if (pass == 3) {
+      if (hist_cut<NT>(hist, sw, (uint32_t)keep_n) < (uint32_t)keep_n) return -1;
+      if (sw.cnt_gt + sw.cnt_eq > LCAP) return -1;
+      t2 = tc + (sw.prefix << sh2);
+    }
+    const uint32_t tmin = (pass == 2) ? tc : t2;  // >= lo >= 1
+    for (int i0 = 0; i0 < nitems; i0 += NT) {
+      const int ic = i0 + lane * NW + warp;
+      const bool pass_c = (ic < nitems) && ckb[(size_t)ic * st] >= tmin;
+      const int kl = pass_c ? (int)kb[(size_t)ic * st] : 0;
+      unsigned bal = __ballot_sync(kFull, pass_c);
+      while (bal) {
+        uint32_t key[U];
+        int flat[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          key[u] = 0u;
+          flat[u] = 0;
+          if (bal) {  // warp-uniform
+            const int src = __ffs(bal) - 1;
+            bal &= bal - 1u;
+            const int k = __shfl_sync(kFull, kl, src);
+            const int j = (i0 + src * NW + warp - bt.istart[k]) * kChunk + lane;
+            if (j < bt.cnt[k]) {
+              flat[u] = bt.start[k] + j;
+              if (zs) {
+                const float z = zs[flat[u]];
+                key[u] = (z == -INFINITY) ? 0u : f2ord(bt.cum[k] + (z - bt.lse[k]));
+              } else {
+                key[u] = cand_key_kj(a, bt, q, k, j);
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          if (pass == 2) {
+            if (key[u] >= tc) atomicAdd(&hist[bin_of(key[u], tc, sh2)], 1u);
+          } else {
+            warp_append(list, LCAP, sw.nwin, key[u] >= t2, key[u], flat[u], lane);
           }
         }
       }
-      __syncthreads();
     }
+    __syncthreads();
   }
+  place_winners<NT>(list, sw.cnt_gt + sw.cnt_eq, keep_n, sw);
   return keep_n;
 }
 

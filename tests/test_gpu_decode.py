@@ -414,3 +414,28 @@ def test_fused_hot_prefixes_large_candidate_set(zg, cluster):
     b = decode_gpu(zg, idx, model, u, 8, 8, [0, 0], fused=0)
     check_topk(a[0], a[1], ref, trie, model, u, 1e-4, WINDOW)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("g0", [512, 4096])
+@pytest.mark.parametrize("variants,fused", [([0, 0], 8), ([0, 0], 0), ([1, 1], 0), ([1, 0], 2)])
+def test_exact_ties_follow_the_tie_rule(zg, g0, variants, fused):
+    """Identical weight and embedding rows within token groups make exact
+    score ties inside a beam and, with every first token sharing one child
+    set, across beams: the order must be score desc, parent rank asc, token
+    asc, exactly as the oracle orders them.  With g0 = 4,096 every step-1
+    candidate ties, which overflows the cut lists and reaches the radix
+    select's tie walk."""
+    V, d, beam = 4096, 32, 16
+    T2 = np.arange(0, V, 103)[:40]
+    sids = np.stack(np.meshgrid(np.arange(V), T2, indexing="ij"), -1).reshape(-1, 2).astype(np.int32)
+    model = synth.make_model(2, V, d, "f32", 11)
+    model.W[0][:] = model.W[0][(np.arange(V) // g0) * g0]
+    model.C[0][:] = model.C[0][(np.arange(V) // g0) * g0]
+    model.W[1][:] = model.W[1][(np.arange(V) // 256) * 256]
+    u = synth.make_requests(2, d, 11)
+    idx = zg.zg_index_build(sids, V, stream=_stream())
+    trie = oracle.Trie(sids, 2, V)
+    ref = oracle.decode(trie, model, u, beam, beam)
+    s, sc = decode_gpu(zg, idx, model, u, beam, beam, variants, fused=fused)
+    assert np.array_equal(s, ref.sids)
+    assert np.allclose(sc, ref.scores, atol=1e-4)
