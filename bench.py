@@ -366,7 +366,11 @@ def run_gpu(args, cfg):
         kern.append((avg["ms_select"], [s], "k_select", st["legal_slots"] * 4 + st["live_beams"] * 16, "hbm",
                      None))
     if s0 <= L:
-        fused_kernel_ms = statistics.fmean(t["ms_fused"] for t in traces)
+        if s0 == 1:
+            # the whole decode is this one launch: its duration is the timed step itself
+            fused_kernel_ms = ms
+        else:
+            fused_kernel_ms = statistics.fmean(t["ms_fused"] for t in traces)
         fb = sum(step_bytes(steps_last[s - 1], cfg, s) for s in range(s0, L + 1))
         fu = sum(step_unique_bytes(steps_last[s - 1], cfg, s) for s in range(s0, L + 1))
         kern.append((fused_kernel_ms, list(range(s0, L + 1)), "k_decode_cluster", fb, "hbm", fu))
