@@ -5,11 +5,11 @@ the CPU-baseline leg of ``bench.py``.  It shares no code with the CUDA library.
 """
 from .zerogr_oracle import (DENSE, SPARSE, DecodeResult, StepTable, Trie, brute_force,
                             choose_format, compact_layout, decode, filtered_log_softmax,
-                            keys_to_sids, padded_slot_layout, path_score, serialize_index,
-                            sid_keys, table_row_tokens)
+                            keys_to_sids, padded_slot_layout, path_score, score_first_log_probs,
+                            serialize_index, sid_keys, table_row_tokens)
 
 __all__ = [
     "DENSE", "SPARSE", "DecodeResult", "StepTable", "Trie", "brute_force", "choose_format",
     "compact_layout", "decode", "filtered_log_softmax", "keys_to_sids", "padded_slot_layout",
-    "path_score", "serialize_index", "sid_keys", "table_row_tokens",
+    "path_score", "score_first_log_probs", "serialize_index", "sid_keys", "table_row_tokens",
 ]

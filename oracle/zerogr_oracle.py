@@ -11,7 +11,9 @@ Recommendation" (paper-daily.com digest), sections cited per function:
   [Problem]   "What problem does it solve" - SIDs, beam search, the validity
               filter and the worked example 3-5-1 / 3-5-4 -> {1, 4}.
   [Order]     "Does filtering first change the result" - softmax normalised
-              over the legal tokens only.
+              over the legal tokens only (filter-first); the conventional
+              order normalises over every token and masks afterwards
+              (score-first, the comparison of that section).
   [Pipeline]  "Overall flow" - the four stages of one decoding step.
   [Index]     "Why slice the index by decoding step" - one table per step,
               rows are prefixes, an entry's position is its next-step row,
@@ -240,6 +242,21 @@ def filtered_log_softmax(z_legal: np.ndarray) -> np.ndarray:
     return z - lse
 
 
+def score_first_log_probs(z_all: np.ndarray, T: np.ndarray) -> np.ndarray:
+    """[Order], [Problem]: the conventional order scores every token, takes
+    the log-softmax over the whole codebook and only then masks: the legal
+    tokens T keep lp_t = z_t - lse_V, lse_V = m + log(sum_v exp(z_v - m))
+    over all V tokens, m = max_v z_v.  The probability mass of the illegal
+    tokens is dropped, not redistributed."""
+    z = np.asarray(z_all, dtype=np.float64)
+    m = z.max()
+    lse_all = m + math.log(float(np.exp(z - m).sum()))
+    return z[np.asarray(T, dtype=np.int64)] - lse_all
+
+
+ORDERS = ("filter_first", "score_first")
+
+
 # ---------------------------------------------------------------------------
 # beam search  [Pipeline]
 # ---------------------------------------------------------------------------
@@ -274,7 +291,7 @@ def candidate_order(vals: np.ndarray, flat: np.ndarray) -> np.ndarray:
 
 
 def decode(trie: Trie | None, model, u: np.ndarray, beam: int, K: int,
-           requests=None) -> DecodeResult:
+           requests=None, order: str = "filter_first") -> DecodeResult:
     """Filtering-first constrained beam search, one request at a time.
 
     Per request: one root beam (empty prefix, cumulative score 0, hidden u).
@@ -288,7 +305,12 @@ def decode(trie: Trie | None, model, u: np.ndarray, beam: int, K: int,
     score, then lower parent-beam rank, then lower slot (ascending token).
     A survivor's hidden vector is h_b + C_s[t] (the synthetic model's
     prefix state).  Output rows beyond the number of candidates are -1/-inf.
+    order="score_first" replaces lp_t by the conventional order's
+    score_first_log_probs (every token scored, normaliser over the codebook,
+    then the mask); everything else is unchanged.
     """
+    if order not in ORDERS:
+        raise ValueError(order)
     L, V = model.L, model.V
     u = np.asarray(u)
     B = u.shape[0]
@@ -309,8 +331,10 @@ def decode(trie: Trie | None, model, u: np.ndarray, beam: int, K: int,
             S, slots = padded_slot_layout([t.size for t in legal])
             vals, flat, toks, ranks = [], [], [], []
             for rank, ((p, cum, h), T) in enumerate(zip(beams, legal)):
-                z = step_logits(Wd, s, T, h)
-                lp = filtered_log_softmax(z)
+                if order == "score_first":
+                    lp = score_first_log_probs(step_logits(Wd, s, all_tok, h), T)
+                else:
+                    lp = filtered_log_softmax(step_logits(Wd, s, T, h))
                 vals.append(cum + lp)
                 flat.append(rank * S + slots[rank, :T.size])
                 toks.append(T)
@@ -319,13 +343,13 @@ def decode(trie: Trie | None, model, u: np.ndarray, beam: int, K: int,
             flat = np.concatenate(flat)
             toks = np.concatenate(toks)
             ranks = np.concatenate(ranks)
-            order = candidate_order(vals, flat)
+            best = candidate_order(vals, flat)
             n_cand[q, s - 1] = vals.size
             if vals.size > keep:
-                gaps[q, s - 1] = vals[order[keep - 1]] - vals[order[keep]]
+                gaps[q, s - 1] = vals[best[keep - 1]] - vals[best[keep]]
                 if s == L:
-                    next_score[q] = vals[order[keep]]
-            chosen = order[:keep]
+                    next_score[q] = vals[best[keep]]
+            chosen = best[:keep]
             new = []
             for i in chosen:
                 p, cum, h = beams[ranks[i]]
@@ -339,10 +363,11 @@ def decode(trie: Trie | None, model, u: np.ndarray, beam: int, K: int,
     return DecodeResult(out_sids, out_scores, gaps, n_cand, next_score)
 
 
-def path_score(trie: Trie | None, model, u_q: np.ndarray, sid) -> float:
+def path_score(trie: Trie | None, model, u_q: np.ndarray, sid, order: str = "filter_first") -> float:
     """Filter-first score of one item along its own path: the sum over steps
-    of its token's log-probability among the legal tokens after its prefix.
-    The hidden vector is recomputed from scratch as u + sum_{j<s} C_j[t_j]."""
+    of its token's log-probability among the legal tokens after its prefix
+    (score-first: among all V tokens).  The hidden vector is recomputed from
+    scratch as u + sum_{j<s} C_j[t_j]."""
     L, V = model.L, model.V
     total = 0.0
     for s in range(1, L + 1):
@@ -355,17 +380,22 @@ def path_score(trie: Trie | None, model, u_q: np.ndarray, sid) -> float:
         pos = np.searchsorted(T, t)
         if pos >= T.size or T[pos] != t:
             return -math.inf
-        z = model.W_as_f64(s - 1)[T] @ h
-        total += float(filtered_log_softmax(z)[pos])
+        if order == "score_first":
+            z = model.W_as_f64(s - 1) @ h
+            total += float(z[t] - (z.max() + math.log(float(np.exp(z - z.max()).sum()))))
+        else:
+            z = model.W_as_f64(s - 1)[T] @ h
+            total += float(filtered_log_softmax(z)[pos])
     return total
 
 
-def brute_force(trie: Trie, model, u_q: np.ndarray):
+def brute_force(trie: Trie, model, u_q: np.ndarray, order: str = "filter_first"):
     """Exhaustive enumeration for tiny catalogues: every item with its
     filter-first score, computed as the log of the product of per-step
-    probabilities softmax(z over legal tokens)[token], walking the trie
-    recursively (independent of ``decode``).  Returns (sids [n, L] ordered by
-    score descending then SID ascending, scores)."""
+    probabilities softmax(z over legal tokens)[token] (score-first:
+    softmax(z over all V tokens)[token]), walking the trie recursively
+    (independent of ``decode``).  Returns (sids [n, L] ordered by score
+    descending then SID ascending, scores)."""
     L, V = model.L, model.V
     Wd = _weights_f64(model)
     items, probs = [], []
@@ -376,9 +406,14 @@ def brute_force(trie: Trie, model, u_q: np.ndarray):
             (np.asarray(model.C[j][t], dtype=np.float64) for j, t in enumerate(prefix)),
             np.zeros(model.d))
         T = trie.children(prefix)
-        z = Wd[s - 1][T] @ h
-        e = np.exp(z - z.max())
-        p = e / e.sum()
+        if order == "score_first":
+            z = Wd[s - 1] @ h
+            e = np.exp(z - z.max())
+            p = (e / e.sum())[T]
+        else:
+            z = Wd[s - 1][T] @ h
+            e = np.exp(z - z.max())
+            p = e / e.sum()
         for t, pt in zip(T, p):
             if s == L:
                 items.append(prefix + (int(t),))

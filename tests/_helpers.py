@@ -19,7 +19,7 @@ def golden_catalogue(fx):
     return L, V, sids
 
 
-def check_topk(gpu_sids, gpu_scores, ref, trie, model, u, tol, window, requests=None):
+def check_topk(gpu_sids, gpu_scores, ref, trie, model, u, tol, window, requests=None, order="filter_first"):
     """Compare a decode's top-K output with the oracle's.
 
     Both sides compute the same beam search; floating-point rounding differs
@@ -27,8 +27,8 @@ def check_topk(gpu_sids, gpu_scores, ref, trie, model, u, tol, window, requests=
     within ``window`` of each other may go either way.  For every request:
       * output rows are valid: SIDs in the catalogue (constrained decode),
         distinct, scores non-increasing, padding (-1 / -inf) only at the end;
-      * each returned score equals the exact filter-first path score of its
-        SID within ``tol``;
+      * each returned score equals the exact path score of its SID (in the
+        decode's order: filter-first or score-first) within ``tol``;
       * unless an intermediate beam boundary was a near-tie (gap <= window),
         the same number of outputs is returned, the sorted score lists agree
         within ``tol`` and every oracle item whose score clears the first
@@ -55,7 +55,7 @@ def check_topk(gpu_sids, gpu_scores, ref, trie, model, u, tol, window, requests=
             seen.add(sid)
             if trie is not None:
                 assert trie.contains(sid), f"request {q}: SID {sid} not in catalogue"
-            exact = _path(trie, model, u[q], sid)
+            exact = _path(trie, model, u[q], sid, order)
             assert abs(exact - sc[i]) <= tol, \
                 f"request {q} rank {i}: score {sc[i]} vs exact {exact}"
         if np.any(ref.gaps[q, :L - 1] <= window):
@@ -75,9 +75,9 @@ def check_topk(gpu_sids, gpu_scores, ref, trie, model, u, tol, window, requests=
     return ambiguous
 
 
-def _path(trie, model, u_q, sid):
+def _path(trie, model, u_q, sid, order="filter_first"):
     from oracle import path_score
-    return path_score(trie, model, u_q, sid)
+    return path_score(trie, model, u_q, sid, order)
 
 
 def isclose_inf(a, b, tol):

@@ -144,3 +144,35 @@ def test_mistake_successor_off_by_one(monkeypatch):
             j = int(np.nonzero(toks == t)[0][0])
             row = int(tabs[s].rowptr[row]) + j
         assert list(Z.table_row_tokens(tabs[2], row, V)) == [1, 4]
+
+
+def _score_first_pin_holds():
+    sids = tiny_catalogue(3, 4, 20, 1)
+    m = synth.make_model(3, 4, 5, "bf16", 1)
+    u = synth.make_requests(2, 5, 1)
+    trie = Z.Trie(sids, 3, 4)
+    res = Z.decode(trie, m, u, beam=20, K=20, order="score_first")
+    for q in range(2):
+        bs, bsc = Z.brute_force(trie, m, u[q], order="score_first")
+        if not np.array_equal(res.sids[q], bs) or np.max(np.abs(res.scores[q] - bsc)) > 1e-9:
+            return False
+    return True
+
+
+def test_score_first_pin_holds_on_the_real_oracle():
+    assert _score_first_pin_holds()
+
+
+def test_mistake_score_first_normalised_over_legal(monkeypatch):
+    """A score-first order that (wrongly) renormalises over the legal tokens."""
+    monkeypatch.setattr(Z, "score_first_log_probs", lambda z_all, T: Z.filtered_log_softmax(np.asarray(z_all)[T]))
+    assert not _score_first_pin_holds()
+
+
+def test_mistake_score_first_without_max_shift_sign(monkeypatch):
+    """A normaliser with the wrong sign (z + lse)."""
+    def wrong(z_all, T):
+        z = np.asarray(z_all, dtype=np.float64)
+        return z[T] + (z.max() + np.log(np.exp(z - z.max()).sum()))
+    monkeypatch.setattr(Z, "score_first_log_probs", wrong)
+    assert not _score_first_pin_holds()

@@ -284,3 +284,77 @@ def test_bf16_storage_roundtrip():
     assert y[0] == 1.0 and y[1] == 1.0                  # tie rounds to even
     assert y[2] == np.float32(1.0078125)
     assert abs(y[3] - x[3]) <= abs(x[3]) * 2 ** -8
+
+
+# ------------------------------------------------- score-first order (the conventional baseline)
+
+@pytest.mark.parametrize("seed,L,V,n,dtype", [(0, 2, 5, 9, "f32"), (1, 3, 4, 20, "bf16"),
+                                               (4, 3, 8, 40, "f32")])
+def test_score_first_equals_exhaustive(seed, L, V, n, dtype):
+    """Score-first with beam >= number of items: every item with the log of
+    the product of its tokens' codebook-wide softmax probabilities (the
+    brute-force walk), best first."""
+    sids = tiny_catalogue(L, V, n, seed)
+    m = _model(L, V, 5, dtype, seed)
+    u = synth.make_requests(2, 5, seed)
+    trie = oracle.Trie(sids, L, V)
+    res = oracle.decode(trie, m, u, beam=n, K=n, order="score_first")
+    for q in range(2):
+        bs, bsc = oracle.brute_force(trie, m, u[q], order="score_first")
+        assert np.array_equal(res.sids[q], bs)
+        assert np.max(np.abs(res.scores[q] - bsc)) < 1e-12
+
+
+def test_score_first_is_the_unconstrained_path_probability():
+    """An item's score-first score is its path log-probability under the
+    unconstrained model: the exhaustive unconstrained decode over all V^L
+    sequences (a distribution: total mass 1) gives the same numbers, and the
+    catalogue's score-first mass is the part of that distribution it covers,
+    below 1 when some tokens are illegal."""
+    L, V, n = 2, 5, 9
+    sids = tiny_catalogue(L, V, n, 3)
+    m = _model(L, V, 6, "f32", 3)
+    u = synth.make_requests(2, 6, 3)
+    trie = oracle.Trie(sids, L, V)
+    unc = oracle.decode(None, m, u, beam=V ** L, K=V ** L)
+    sf = oracle.decode(trie, m, u, beam=n, K=n, order="score_first")
+    for q in range(2):
+        assert abs(np.exp(unc.scores[q]).sum() - 1.0) < 1e-9
+        full = {tuple(int(t) for t in s): float(v) for s, v in zip(unc.sids[q], unc.scores[q])}
+        got = [full[tuple(int(t) for t in s)] for s in sf.sids[q]]
+        assert np.max(np.abs(np.array(got) - sf.scores[q])) < 1e-12
+        mass = np.exp(sf.scores[q]).sum()
+        assert mass < 1.0 - 1e-3
+        assert abs(mass - sum(math.exp(full[tuple(int(t) for t in s)]) for s in sids)) < 1e-12
+
+
+def test_score_first_equals_filter_first_on_product_catalogue():
+    """When every SID exists the legal set is the codebook: both orders
+    normalise over the same tokens and agree exactly."""
+    L, V, d = 2, 6, 8
+    sids = synth.product_catalogue(L, V)
+    m = _model(L, V, d)
+    u = synth.make_requests(3, d, 5)
+    trie = oracle.Trie(sids, L, V)
+    a = oracle.decode(trie, m, u, beam=4, K=4)
+    b = oracle.decode(trie, m, u, beam=4, K=4, order="score_first")
+    assert np.array_equal(a.sids, b.sids)
+    assert np.max(np.abs(a.scores - b.scores)) < 1e-12
+
+
+def test_score_first_single_step_closed_form():
+    """One step: score-first = filter-first + log(softmax mass of the legal
+    tokens) with both log-sum-exps from scipy; the order is the same."""
+    V, d = 40, 16
+    m = _model(1, V, d, "f32", 9)
+    u = synth.make_requests(1, d, 9)
+    legal = np.array([2, 5, 11, 17, 23, 31, 38])
+    sids = legal[:, None].astype(np.int32)
+    trie = oracle.Trie(sids, 1, V)
+    a = oracle.decode(trie, m, u, beam=7, K=7)
+    b = oracle.decode(trie, m, u, beam=7, K=7, order="score_first")
+    z = m.W_as_f64(0) @ u[0].astype(np.float64)
+    shift = scipy.special.logsumexp(z[legal]) - scipy.special.logsumexp(z)
+    assert shift < 0
+    assert np.array_equal(a.sids, b.sids)
+    assert np.max(np.abs(b.scores - (a.scores + shift))) < 1e-12
