@@ -340,6 +340,20 @@ def run_gpu(args, cfg):
     utimes = timed(ugraph, max(10, args.steps // 2), 3)
     ums = max_over_ranks(statistics.fmean(utimes), world, dev)
 
+    # score-first order on the same inputs (every token projected, log-softmax
+    # over the codebook, then the mask): the conventional baseline, and the
+    # top-K overlap of the two orders (a mechanism check on random weights)
+    plan_sf = zg.zg_plan_force(idx, B, beam, [1] * cfg.L)
+    zg.zg_plan_set_order(plan_sf, zg.ZG_ORDER_SCORE_FIRST)
+    sdec = Decoder(idx, plan_sf, dm, B, beam, K, dev)
+    sgraph = capture(sdec)
+    stimes = timed(sgraph, max(10, args.steps // 2), 3)
+    sms = max_over_ranks(statistics.fmean(stimes), world, dev)
+    ff_sids = dec(u_dev)[0].cpu().numpy()
+    sf_sids = sdec(u_dev)[0].cpu().numpy()
+    overlap = float(np.mean([len({tuple(x) for x in ff_sids[q]} & {tuple(x) for x in sf_sids[q]}) / K
+                             for q in range(B)]))
+
     # per-kernel times and work counts (traced decode, L2 flushed before each)
     traces = []
     for _ in range(max(5, min(args.steps, 30))):
@@ -450,6 +464,8 @@ def run_gpu(args, cfg):
             "clocks": clocks,
             "unconstrained": {"ms_per_step": ums, "value": B * world / (ums / 1000.0), "unit": UNIT,
                               "constrained_speedup": ums / ms_max},
+            "score_first": {"ms_per_step": sms, "value": B * world / (sms / 1000.0), "unit": UNIT,
+                            "filter_first_speedup": sms / ms_max, "topk_overlap": overlap},
             "kernels": [{"kernel": n, "steps": st, "ms": round(t, 5)} for t, st, n, _, _, _ in kern],
             "work": work,
         }

@@ -24,6 +24,7 @@ ZG_FMT_SPARSE, ZG_FMT_DENSE = 0, 1
 ZG_SELECTIVE, ZG_FULL = 0, 1
 ZG_RESIDENT_DEVICE, ZG_RESIDENT_HOST = 0, 1
 ZG_FORMAT_AUTO, ZG_FORMAT_ALL_SPARSE, ZG_FORMAT_ALL_DENSE = 0, 1, 2
+ZG_ORDER_FILTER_FIRST, ZG_ORDER_SCORE_FIRST = 0, 1
 
 
 class ZgError(RuntimeError):
@@ -84,6 +85,7 @@ def _load():
         "zg_plan_force": [vp, i32, i32, vp, P(vp)],
         "zg_plan_describe": [vp, vp, vp, vp, vp],
         "zg_plan_set_fusion": [vp, i32],
+        "zg_plan_set_order": [vp, i32],
         "zg_decode_workspace_size": [vp, vp, P(zg_model), i32, i32, i32, P(sz)],
         "zg_decode": [vp, vp, P(zg_model), vp, i32, i32, i32, vp, vp, vp, sz, vp],
         "zg_decode_host_workspace_size": [vp, vp, P(zg_model), i32, i32, i32, P(sz)],
@@ -293,6 +295,12 @@ def zg_decode_trace(idx: Index | None, plan: Plan | None, model: zg_model, u, B:
     steps = [{f: getattr(t.step[i], f) for f, _ in zg_step_trace._fields_ if f != "reserved"}
              for i in range(t.L)]
     return {"fused_from": t.fused_from, "ms_fused": t.ms_fused, "ms_total": t.ms_total, "steps": steps}
+
+
+def zg_plan_set_order(plan: Plan, order: int):
+    """ZG_ORDER_FILTER_FIRST (default) or ZG_ORDER_SCORE_FIRST (every step full,
+    log-softmax over the whole codebook, then the mask)."""
+    _check(lib.zg_plan_set_order(plan, int(order)))
 
 
 def zg_plan_set_fusion(plan: Plan, cluster_ctas):

@@ -29,13 +29,15 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 struct Dims {
   int L, V, d, w_dtype, B, beam, K;
   bool constrained;
+  bool score_first;      // ZG_ORDER_SCORE_FIRST plan
   int S_full;            // padded token stride of full scores
   int nch_sel[ZG_MAX_STEPS];
   int S_sel[ZG_MAX_STEPS];
 };
 
 struct WsLayout {
-  size_t tok_hist, par_hist, row[2], cum[2], h[2], hhi, hlo, Z, part, trace, u_stage, o_sids, o_scores, total;
+  size_t tok_hist, par_hist, row[2], cum[2], h[2], hhi, hlo, Z, part, part_all, mask, trace, u_stage, o_sids,
+      o_scores, total;
   size_t trace_bytes;
 };
 
@@ -72,6 +74,10 @@ WsLayout layout(const Dims& m, bool host_io) {
   }
   w.Z = take(zf * 4);
   w.part = take(pf * 8);
+  if (m.score_first) {  // codebook-wide partials and per-beam token bitmaps
+    w.part_all = take(BW * (m.S_full / kChunk) * 8);
+    w.mask = take(BW * (size_t)((m.V + 31) / 32) * 4);
+  }
   w.trace_bytes = 32 + (size_t)((m.V + 31) / 32) * 4;  // 4 counters + token mask
   w.trace = take(w.trace_bytes);
   if (host_io) {
@@ -196,7 +202,7 @@ StepLaunch make_launch(const Run& r, int s, int variant) {
   }
   a.u = r.u;
   a.W = r.model->W[s - 1];
-  const bool full = (variant == ZG_FULL) || !r.idx;
+  const bool full = (variant == ZG_FULL) || !r.idx || m.score_first;
   // hidden of this step's beams: the next step's parents (s < L) and the
   // full projection's input; at step 1 it is u itself
   a.h_out = (s >= 2 && (s < m.L || full)) ? F32(r.w.h[s & 1]) : nullptr;
@@ -214,6 +220,20 @@ StepLaunch make_launch(const Run& r, int s, int variant) {
     a.nch = m.nch_sel[s - 1];
     a.S = m.S_sel[s - 1];
     a.part = reinterpret_cast<float2*>(r.ws + r.w.part);
+  } else if (m.score_first && r.idx) {
+    // project every token, normalise over the codebook, mask, select: token
+    // slots on every step; sparse-format steps expand their legal lists into
+    // per-beam bitmap rows first
+    a.mode = kFullDense;
+    a.S = m.S_full;
+    a.nch = m.S_full / kChunk;
+    a.part = reinterpret_cast<float2*>(r.ws + r.w.part);
+    a.part_all = reinterpret_cast<const float2*>(r.ws + r.w.part_all);
+    if (r.idx->steps[s - 1].fmt == ZG_FMT_SPARSE) {
+      a.mask_by_beam = 1;
+      a.tab.bitmap = U32(r.w.mask);
+      a.tab.words = (uint32_t)((m.V + 31) / 32);
+    }
   } else {
     a.mode = !r.idx ? kUncon : (r.idx->steps[s - 1].fmt == ZG_FMT_SPARSE ? kFullSparse : kFullDense);
     a.S = m.S_full;
@@ -252,10 +272,16 @@ zg_status run_step(const Run& r, int s, int variant, cudaStream_t st, const Step
     }
     FullEpi epi{};
     epi.part = a.part;
+    epi.part_all = const_cast<float2*>(a.part_all);
     if (a.mode == kFullDense) {
       epi.bitmap = a.tab.bitmap;
       epi.words = (int)a.tab.words;
       epi.rows = (s >= 2) ? a.row_in : nullptr;  // beam b = q*beam + k at s >= 2; the root's row 0 at s = 1
+      if (a.mask_by_beam) {
+        e = launch_legal_mask(a, st);
+        if (e != cudaSuccess) return cuda_fail(e, "legal-mask launch");
+        epi.by_m = 1;
+      }
     }
     if (tm) cudaEventRecord(tm->ev[1], st);
     if (a.w_dtype != ZG_F32)
@@ -277,6 +303,7 @@ zg_status prepare(const zg_index* idx, const zg_plan* plan, const zg_model* mode
   zg_status st = check_common(idx, model, B, beam, K, &m);
   if (st != ZG_OK) return st;
   if (plan && plan->L != m.L) return fail(ZG_ERR_INVALID_ARG, "plan has a different number of steps");
+  m.score_first = idx && plan && plan->order == ZG_ORDER_SCORE_FIRST;
   if (!u || !out_sids || !out_scores) return fail(ZG_ERR_INVALID_ARG, "u, out_sids and out_scores must not be NULL");
   if (!host_io && reinterpret_cast<uintptr_t>(u) % 16) return fail(ZG_ERR_INVALID_ARG, "u must be 16-byte aligned");
   if (!ws) return fail(ZG_ERR_INVALID_ARG, "workspace is NULL");
@@ -297,13 +324,13 @@ zg_status prepare(const zg_index* idx, const zg_plan* plan, const zg_model* mode
 constexpr int kClusterCTAs = 8;  // default CTAs of the fused kernel's cluster (one cluster per request)
 
 int variant_of(const Run& r, const zg_plan* plan, int s) {
-  return !r.idx ? ZG_FULL : (plan ? plan->variant[s - 1] : ZG_SELECTIVE);
+  return (!r.idx || r.m.score_first) ? ZG_FULL : (plan ? plan->variant[s - 1] : ZG_SELECTIVE);
 }
 
 // First step of the trailing run of selective steps that zg_decode fuses
 // (L+1: none).
 int fused_from(const Run& r, const zg_plan* plan) {
-  if (!r.idx || (plan && !plan->fused)) return r.m.L + 1;
+  if (!r.idx || r.m.score_first || (plan && !plan->fused)) return r.m.L + 1;
   int s0 = r.m.L + 1;
   while (s0 > 1 && variant_of(r, plan, s0 - 1) == ZG_SELECTIVE) --s0;
   return s0;
@@ -431,24 +458,32 @@ zg_status zg_plan_set_fusion(zg_plan* plan, int32_t cluster_ctas) {
   return ZG_OK;
 }
 
+zg_status zg_plan_set_order(zg_plan* plan, int32_t order) {
+  if (!plan) return fail(ZG_ERR_INVALID_ARG, "zg_plan_set_order: plan is NULL");
+  if (order != ZG_ORDER_FILTER_FIRST && order != ZG_ORDER_SCORE_FIRST)
+    return fail(ZG_ERR_INVALID_ARG, "zg_plan_set_order: order must be ZG_ORDER_FILTER_FIRST or ZG_ORDER_SCORE_FIRST");
+  plan->order = order;
+  return ZG_OK;
+}
+
 zg_status zg_decode_workspace_size(const zg_index* idx, const zg_plan* plan, const zg_model* model, int32_t B,
                                    int32_t beam, int32_t K, size_t* bytes) {
-  (void)plan;
   if (!bytes) return fail(ZG_ERR_INVALID_ARG, "bytes is NULL");
   Dims m;
   zg_status st = check_common(idx, model, B, beam, K, &m);
   if (st != ZG_OK) return st;
+  m.score_first = idx && plan && plan->order == ZG_ORDER_SCORE_FIRST;
   *bytes = layout(m, false).total;
   return ZG_OK;
 }
 
 zg_status zg_decode_host_workspace_size(const zg_index* idx, const zg_plan* plan, const zg_model* model, int32_t B,
                                         int32_t beam, int32_t K, size_t* bytes) {
-  (void)plan;
   if (!bytes) return fail(ZG_ERR_INVALID_ARG, "bytes is NULL");
   Dims m;
   zg_status st = check_common(idx, model, B, beam, K, &m);
   if (st != ZG_OK) return st;
+  m.score_first = idx && plan && plan->order == ZG_ORDER_SCORE_FIRST;
   *bytes = layout(m, true).total;
   return ZG_OK;
 }

@@ -331,6 +331,30 @@ __global__ void __launch_bounds__(256) k_full_simt(const float* __restrict__ H, 
       if ((tx & 7) == 0 && m < M && chunk * 32 < V) epi.part[(size_t)m * (ldz >> 5) + chunk] = make_float2(mx, sm);
     }
   }
+  if (epi.part_all) {
+    // (max, sum exp) over every token of each chunk (score-first normaliser)
+    const int chunk = (n0 >> 5) + (tx >> 3);
+    const int sh = (tx & 7) * 4;
+    const int rem = V - chunk * 32;
+    const uint32_t vm = (rem >= 32 ? 0xFFFFFFFFu : (rem <= 0 ? 0u : ((1u << rem) - 1u))) >> sh & 0xFu;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int m = m0 + ty * 4 + i;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mx = ((vm >> j) & 1u) ? fmaxf(mx, acc[i][j]) : mx;
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+      float sm = 0.f;
+      if (mx != -INFINITY) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sm += ((vm >> j) & 1u) ? __expf(acc[i][j] - mx) : 0.f;
+      }
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) sm += __shfl_xor_sync(0xFFFFFFFFu, sm, o);
+      if ((tx & 7) == 0 && m < M && chunk * 32 < V) epi.part_all[(size_t)m * (ldz >> 5) + chunk] = make_float2(mx, sm);
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -361,6 +385,42 @@ __global__ void __launch_bounds__(kSelThreads) k_select(const __grid_constant__ 
     }
   }
   write_survivors<kSelThreads>(a, q, bt, sw, n);
+}
+
+// ---------------------------------------------------------------------------
+// Score-first order on a sparse-format step: expand every beam's legal list
+// (the index row's column entries) into a token bitmap row of its own,
+// tab.bitmap[b * words] for beam b = q*Wc + k (zeros for a dead beam), so
+// the full projection's epilogue and the select mask tokens as on a dense
+// step.  One warp per beam: clear the row, then set the bits.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_legal_mask(const __grid_constant__ StepLaunch a) {
+  const int lane = threadIdx.x & 31;
+  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  const int N = a.B * a.Wc;
+  uint32_t* mask = const_cast<uint32_t*>(a.tab.bitmap);
+  for (int b = wid; b < N; b += nw) {
+    const int q = b / a.Wc, k = b - q * a.Wc;
+    uint32_t* row = mask + (size_t)b * a.tab.words;
+    for (int w = lane; w < (int)a.tab.words; w += 32) row[w] = 0u;
+    __syncwarp();
+    const BeamState bs = load_beam(a, q, k);
+    if (bs.row == kDeadRow) continue;
+    if (bs.row >= a.tab.rows) {
+      if (lane == 0) flag(a.status, kStatusRow);
+      continue;
+    }
+    const uint32_t rp = a.tab.rowptr[bs.row];
+    const uint32_t F = a.tab.rowptr[bs.row + 1] - rp;
+    for (uint32_t j = lane; j < F; j += 32) {
+      const uint32_t t = a.tab.col[rp + j];
+      if (t < (uint32_t)a.V)
+        atomicOr(&row[t >> 5], 1u << (t & 31));
+      else
+        flag(a.status, kStatusToken);
+    }
+  }
 }
 
 // Tracing: counts of the work a step does, for roofline accounting.
@@ -568,6 +628,13 @@ cudaError_t launch_trace_touch(const StepLaunch& a, unsigned long long* counters
   const int N = a.B * a.Wc;
   const int blocks = std::max(1, std::min((N + 7) / 8, sm_count() * 8));
   k_trace_touch<<<blocks, 256, 0, st>>>(a, counters, mask);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_legal_mask(const StepLaunch& a, cudaStream_t st) {
+  const int N = a.B * a.Wc;
+  const int blocks = std::max(1, std::min((N + 7) / 8, sm_count() * 8));
+  k_legal_mask<<<blocks, 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -240,6 +240,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             epi.part[(size_t)row * (ldz >> 5) + chunk] = make_float2(mx, sm);
           }
+          if (epi.part_all) {
+            // (max, sum exp) over every token of the chunk (score-first normaliser)
+            const int chunk = (n0 + c0) >> 5;
+            const int rem = V - (n0 + c0);
+            const uint32_t vm = rem >= 32 ? 0xFFFFFFFFu : ((1u << rem) - 1u);
+            float mx = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) mx = ((vm >> i) & 1u) ? fmaxf(mx, v[i]) : mx;
+            float sm = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) sm += ((vm >> i) & 1u) ? __expf(v[i] - mx) : 0.f;
+            epi.part_all[(size_t)row * (ldz >> 5) + chunk] = make_float2(mx, sm);
+          }
         }
       }
     }

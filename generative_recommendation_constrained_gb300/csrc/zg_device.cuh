@@ -317,6 +317,12 @@ struct SelWorkT {
   int all_eq;
 };
 
+// Legal-token bitmap row of beam k of request q on a dense-slot full step:
+// the index row's bitmap, or the beam's own expanded row (mask_by_beam).
+__device__ __forceinline__ const uint32_t* legal_bits(const StepLaunch& a, const BeamTab& bt, int q, int k) {
+  return a.tab.bitmap + (a.mask_by_beam ? (size_t)q * a.Wc + k : (size_t)bt.row[k]) * a.tab.words;
+}
+
 // largest k with arr[k] <= c (arr ascending, arr[0] = 0)
 __device__ __forceinline__ int upper_find(const int* arr, int n, int c) {
   int lo = 0, hi = n - 1;
@@ -406,8 +412,9 @@ __device__ void build_beam_table(const StepLaunch& a, int q, BeamTab& bt) {
   __syncthreads();
 }
 
-// Legal-only log-sum-exp of every live beam from its chunk partials (m_c,
-// s_c): lse = M + log(sum_c s_c exp(m_c - M)), M = max_c m_c.  Eight lanes a
+// Log-sum-exp of every live beam from its chunk partials (m_c, s_c): lse =
+// M + log(sum_c s_c exp(m_c - M)), M = max_c m_c, over the legal tokens
+// (filter-first), or over every token from part_all (score-first).  Eight lanes a
 // beam, eight beams a warp at once (two a lane group, their first partials
 // loaded together and kept for the second pass), width-8 shuffle reductions.
 // Partials come from shared memory by item (psm) or from the global partial
@@ -421,15 +428,20 @@ __device__ void beam_lse_sel(const StepLaunch& a, int q, BeamTab& bt, const floa
   for (int k0 = warp * 8; k0 < a.Wc; k0 += (NT / 32) * 8) {
     int kb[2], n[2];
     const float2* pp[2];
-    float2 p0[2];
+    const float2* pa[2];
+    float2 p0[2], a0[2];
+    const bool all_v = (a.part_all != nullptr) && !psm;  // score-first: normaliser over the codebook
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int k = k0 + 4 * h + sub;
       const bool live = (k < a.Wc) && bt.cnt[k] > 0;
       kb[h] = k;
       n[h] = live ? bt.items[k] : 0;
-      pp[h] = psm ? psm + (live ? bt.istart[k] : 0) : a.part + (size_t)q * a.pq + (size_t)(live ? k : 0) * a.nch;
+      const size_t go = (size_t)q * a.pq + (size_t)(live ? k : 0) * a.nch;
+      pp[h] = psm ? psm + (live ? bt.istart[k] : 0) : a.part + go;
+      pa[h] = all_v ? a.part_all + go : pp[h];
       p0[h] = (sl < n[h]) ? pp[h][sl] : make_float2(-INFINITY, 0.f);
+      a0[h] = all_v ? ((sl < n[h]) ? pa[h][sl] : make_float2(-INFINITY, 0.f)) : p0[h];
     }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -443,22 +455,27 @@ __device__ void beam_lse_sel(const StepLaunch& a, int q, BeamTab& bt, const floa
           ++ne;
         }
       }
+      float ma = a0[h].x;  // maximum of the normalised set
+      if (all_v)
+        for (int c = sl + 8; c < n[h]; c += 8) ma = fmaxf(ma, pa[h][c].x);
 #pragma unroll
       for (int o = 4; o; o >>= 1) {
         m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
         mn = fminf(mn, __shfl_xor_sync(kFull, mn, o));
         ne += __shfl_xor_sync(kFull, ne, o);
+        ma = fmaxf(ma, __shfl_xor_sync(kFull, ma, o));
       }
-      float sum = (p0[h].y > 0.f) ? p0[h].y * expf(p0[h].x - m) : 0.f;
+      if (!all_v) ma = m;
+      float sum = (a0[h].y > 0.f) ? a0[h].y * expf(a0[h].x - ma) : 0.f;
       for (int c = sl + 8; c < n[h]; c += 8) {
-        const float2 p = pp[h][c];
-        if (p.y > 0.f) sum += p.y * expf(p.x - m);
+        const float2 p = pa[h][c];
+        if (p.y > 0.f) sum += p.y * expf(p.x - ma);
       }
 #pragma unroll
       for (int o = 4; o; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
       const int k = kb[h];
       if (n[h] > 0 && sl == 0) {
-        const float lse = m + logf(sum);
+        const float lse = ma + logf(sum);
         bt.lse[k] = lse;
         if (ne > 0) {  // keys of the beam's best and of its weakest chunk maximum, as the select computes them
           atomicMax(&bt.kceil, f2ord(bt.cum[k] + (m - lse)));
@@ -504,8 +521,7 @@ __device__ void beam_lse(const StepLaunch& a, int q, BeamTab& bt, uint32_t* rep_
     auto zval = [&](int j) -> float {
       if (a.mode == kFullSparse) return a.Z[zb + a.tab.col[bt.rp[k] + j]];
       if (a.mode == kFullDense)
-        return ((a.tab.bitmap[(size_t)bt.row[k] * a.tab.words + (j >> 5)] >> (j & 31)) & 1u) ? a.Z[zb + j]
-                                                                                          : -INFINITY;
+        return ((legal_bits(a, bt, q, k)[j >> 5] >> (j & 31)) & 1u) ? a.Z[zb + j] : -INFINITY;
       return a.Z[zb + j];
     };
     float m = -INFINITY;
@@ -548,7 +564,7 @@ __device__ __forceinline__ uint32_t cand_key_kj(const StepLaunch& a, const BeamT
       z = a.Z[zb + a.tab.col[bt.rp[k] + j]];
       break;
     default:  // kSelDense, kFullDense
-      if (!((a.tab.bitmap[(size_t)bt.row[k] * a.tab.words + (j >> 5)] >> (j & 31)) & 1u)) return 0u;
+      if (!((legal_bits(a, bt, q, k)[j >> 5] >> (j & 31)) & 1u)) return 0u;
       z = a.Z[zb + j];
       break;
   }
@@ -1285,7 +1301,7 @@ __device__ void write_survivors(const StepLaunch& a, int q, const BeamTab& bt, c
             for (int wd = 0; wd < (t >> 5); ++wd) rank += __popc(mk[wd]);
             rank += __popc(mk[t >> 5] & ((1u << (t & 31)) - 1u));
           } else {
-            const uint32_t* bm = a.tab.bitmap + (size_t)bt.row[k] * a.tab.words;
+            const uint32_t* bm = legal_bits(a, bt, q, k);
             for (int wd = 0; wd < (t >> 5); ++wd) rank += __popc(bm[wd]);
             rank += __popc(bm[t >> 5] & ((1u << (t & 31)) - 1u));
           }

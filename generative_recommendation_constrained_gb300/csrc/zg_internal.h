@@ -73,7 +73,11 @@ struct StepLaunch {
   float* h_out;            // [B*Wc][d] hidden of this step's beams, or NULL
   // scores
   float* Z;                // [B][zq]
-  float2* part;            // [B][pq] (max, sum exp) per chunk, selective only
+  float2* part;            // [B][pq] (max, sum exp) of the legal tokens per chunk
+  const float2* part_all;  // [B][pq] (max, sum exp) of every token per chunk: score-first
+                           // order (log-softmax over the codebook), else NULL
+  int32_t mask_by_beam;    // tab.bitmap holds one row per beam (b = q*Wc + k), not per
+                           // index row: a sparse step's legal lists expanded (score-first)
   // outputs
   uint32_t* row_out;       // [B*beam] (s < L)
   float* cum_out;          // [B*beam]
@@ -89,9 +93,11 @@ struct StepLaunch {
 // tokens of the chunk, the same partials the selective kernels produce.
 struct FullEpi {
   float2* part;            // [M][ldz/32], or null (no partials)
+  float2* part_all;        // [M][ldz/32] (max, sum exp) over every token < V, or null
   const uint32_t* bitmap;  // dense step's bitmap rows; null: every token < V is legal
   const uint32_t* rows;    // [M] index row of each beam (kDeadRow: dead); null: row 0
   int words;               // bitmap words a row
+  int by_m;                // bitmap row m belongs to beam row m (rows unused)
 };
 
 #ifdef __CUDACC__
@@ -99,7 +105,7 @@ struct FullEpi {
 __device__ __forceinline__ uint32_t epi_legal_mask(const FullEpi& e, int m, int chunk, int V) {
   uint32_t mask = 0xFFFFFFFFu;
   if (e.bitmap) {
-    const uint32_t r = e.rows ? e.rows[m] : 0u;
+    const uint32_t r = e.by_m ? (uint32_t)m : (e.rows ? e.rows[m] : 0u);
     if (r == kDeadRow) return 0u;
     mask = e.bitmap[(size_t)r * e.words + chunk];
   }
@@ -114,6 +120,7 @@ cudaError_t launch_selective(const StepLaunch& a, cudaStream_t st);
 cudaError_t launch_gather_add(const StepLaunch& a, float* H, cudaStream_t st);
 cudaError_t launch_full_simt(const StepLaunch& a, const float* H, const FullEpi& epi, cudaStream_t st);
 cudaError_t launch_select(const StepLaunch& a, cudaStream_t st);
+cudaError_t launch_legal_mask(const StepLaunch& a, cudaStream_t st);
 // A device region the fused kernel prefetches into L2 (16-byte aligned).
 struct PrefetchRegion {
   const void* ptr;
@@ -158,6 +165,7 @@ struct zg_index {
 struct zg_plan {
   int32_t L = 0, B = 0, beam = 0;
   int32_t fused = 8;            // CTAs per cluster of the fused kernel; 0 = no fusion
+  int32_t order = 0;            // zg_order
   float fused_ms[5] = {-1, -1, -1, -1, -1};  // tuned decode times with 1, 2, 4, 8, 16 CTAs a cluster
   float plan_ms = -1.f;                      // tuned decode time of the kept plan
   std::vector<uint8_t> variant;  // [L]

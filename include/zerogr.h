@@ -67,6 +67,7 @@ typedef enum { ZG_FMT_SPARSE = 0, ZG_FMT_DENSE = 1 } zg_format;
 typedef enum { ZG_SELECTIVE = 0, ZG_FULL = 1 } zg_variant;
 typedef enum { ZG_RESIDENT_DEVICE = 0, ZG_RESIDENT_HOST = 1 } zg_residency;
 typedef enum { ZG_FORMAT_AUTO = 0, ZG_FORMAT_ALL_SPARSE = 1, ZG_FORMAT_ALL_DENSE = 2 } zg_format_mode;
+typedef enum { ZG_ORDER_FILTER_FIRST = 0, ZG_ORDER_SCORE_FIRST = 1 } zg_order;
 
 typedef struct zg_index zg_index; /* opaque: step tables + host header */
 typedef struct zg_plan zg_plan;   /* opaque: per-step variant choice   */
@@ -189,6 +190,19 @@ ZG_API zg_status zg_plan_set_fusion(zg_plan* plan, int32_t cluster_ctas);
  * schedulable).  Any output may be NULL. */
 ZG_API zg_status zg_plan_describe(const zg_plan* plan, uint8_t* variant, float* step_ms,
                                   int32_t* cluster_ctas, float* fused_ms);
+/* Order of filtering and normalisation (the comparison of [Order]).
+ *   ZG_ORDER_FILTER_FIRST (default): log-softmax over the legal tokens only.
+ *   ZG_ORDER_SCORE_FIRST: the conventional baseline of [Problem] - project
+ *     every token (one dense contraction), normalise the log-softmax over the
+ *     whole codebook, then mask the illegal tokens and select among the legal
+ *     ones.  Every step runs ZG_FULL whatever the plan's variants, unfused;
+ *     sparse-format steps first expand each beam's legal list into a token
+ *     bitmap (workspace), dense-format steps read the index bitmap.  Scores
+ *     are the score-first cumulative log-probabilities (at most the
+ *     filter-first ones: the mass of illegal tokens is not redistributed).
+ * Changes the workspace size: size the workspace after setting the order.
+ * ZG_ERR_INVALID_ARG for another value. */
+ZG_API zg_status zg_plan_set_order(zg_plan* plan, int32_t order);
 ZG_API void zg_plan_free(zg_plan* plan);
 
 /* --------------------------------------------------------------- decode ---
