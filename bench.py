@@ -354,6 +354,10 @@ def run_gpu(args, cfg):
     overlap = float(np.mean([len({tuple(x) for x in ff_sids[q]} & {tuple(x) for x in sf_sids[q]}) / K
                              for q in range(B)]))
 
+    contrast = [step_contrast(zg, idx, dm, cfg, B, u_dev, flush, Decoder)]
+    if B > 1:
+        contrast.append(step_contrast(zg, idx, dm, cfg, 1, u_dev[:1].contiguous(), flush, Decoder))
+
     # per-kernel times and work counts (traced decode, L2 flushed before each)
     traces = []
     for _ in range(max(5, min(args.steps, 30))):
@@ -464,6 +468,7 @@ def run_gpu(args, cfg):
             "clocks": clocks,
             "unconstrained": {"ms_per_step": ums, "value": B * world / (ums / 1000.0), "unit": UNIT,
                               "constrained_speedup": ums / ms_max},
+            "contrast": contrast,
             "score_first": {"ms_per_step": sms, "value": B * world / (sms / 1000.0), "unit": UNIT,
                             "filter_first_speedup": sms / ms_max, "topk_overlap": overlap},
             "kernels": [{"kernel": n, "steps": st, "ms": round(t, 5)} for t, st, n, _, _, _ in kern],
@@ -473,6 +478,129 @@ def run_gpu(args, cfg):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------- scoring-variant contrast
+
+def step_contrast(zg, idx, dm, cfg, B, u_dev, flush, Decoder, reps: int = 5):
+    """The comparison of the pages' compact-list figure at the step with the
+    most legal tokens: the step's kernels (gather-add, projection, select)
+    timed under an all-full, an all-naive (compact list + temporary matrix)
+    and an all-padded-slots (selective, stand-alone) plan; median of `reps`
+    traced decodes, L2 flushed before each."""
+    out = {"batch": B}
+    times = {}
+    for name, v in (("full", 1), ("naive", 2), ("padded", 0)):
+        plan = zg.zg_plan_force(idx, B, cfg.beam, [v] * cfg.L)
+        zg.zg_plan_set_fusion(plan, 0)
+        try:
+            dec = Decoder(idx, plan, dm, B, cfg.beam, cfg.topk, u_dev.device)
+        except zg.ZgError as e:  # the naive temporary matrix does not fit
+            out[name] = str(e)
+            continue
+        runs = []
+        for _ in range(reps):
+            flush.fill_(1.0)
+            runs.append(dec.trace(u_dev))
+        times[name] = runs
+        del dec
+    if "padded" not in times:
+        return out
+    legal = [st["legal_slots"] for st in times["padded"][-1]["steps"]]
+    s = int(np.argmax(legal))
+    out["step"] = s + 1
+    out["legal_slots"] = int(legal[s])
+    out["scores_full"] = int(B * (1 if s == 0 else cfg.beam) * cfg.V)
+    for name, runs in times.items():
+        out[f"{name}_ms"] = statistics.median(
+            r["steps"][s]["ms_gather"] + r["steps"][s]["ms_project"] + r["steps"][s]["ms_select"] for r in runs)
+    if "naive_ms" in out:
+        out["naive_over_full"] = out["naive_ms"] / out["full_ms"]
+        out["naive_over_padded"] = out["naive_ms"] / out["padded_ms"]
+    out["pages"] = {"naive_over_full": 5.1, "naive_over_padded": 8.5}
+    return out
+
+
+# ---------------------------------------------------------------- index rebuild leg
+
+def run_index_rebuild(args, cfg):
+    """Rebuild throughput of the step-sliced index (items/s of zg_index_build:
+    sort + dedup and the two-pass fill on host threads, streamed to HBM
+    through two pinned buffers) and whether a decode served at the same time
+    on the same GPU slows down: the mid-sparse decode graph is replayed on its
+    own stream before and while the index of `cfg` is rebuilt on a host
+    thread, and the median replay times are compared."""
+    import threading
+    import torch
+    import generative_recommendation_constrained_gb300 as zg
+    from generative_recommendation_constrained_gb300.device import Decoder, DeviceModel
+    dev = torch.device("cuda", 0)
+    sids = synth.make_catalogue(cfg, 0)
+    # the decode being served meanwhile: the mid-sparse workload, fused plan
+    scfg = synth.CONFIGS["mid_sparse"]
+    s_sids = synth.make_catalogue(scfg, 0)
+    s_model = synth.make_model(scfg.L, scfg.V, scfg.d, scfg.w_dtype, 0)
+    serve = torch.cuda.Stream(device=dev)
+    s_idx = zg.zg_index_build(s_sids, scfg.V, stream=serve.cuda_stream)
+    dm = DeviceModel(s_model, dev)
+    u = torch.from_numpy(synth.make_requests(scfg.batch, scfg.d, 1000)).to(dev)
+    plan = zg.zg_plan_force(s_idx, scfg.batch, scfg.beam, [0] * scfg.L)
+    dec = Decoder(s_idx, plan, dm, scfg.batch, scfg.beam, scfg.topk, dev)
+    with torch.cuda.stream(serve):
+        dec(u, serve.cuda_stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=serve):
+            dec(u, serve.cuda_stream)
+    torch.cuda.synchronize()
+
+    def replay_times(stop):
+        out = []
+        while not stop():
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(serve):
+                a.record(serve)
+                g.replay()
+                b.record(serve)
+            b.synchronize()
+            out.append(a.elapsed_time(b))
+        return out
+
+    t_end = time.perf_counter() + 2.0
+    alone = replay_times(lambda: time.perf_counter() > t_end)
+    build_stream = torch.cuda.Stream(device=dev)
+    res = {}
+
+    def build():
+        t0 = time.perf_counter()
+        idx = zg.zg_index_build(sids, cfg.V, stream=build_stream.cuda_stream)
+        build_stream.synchronize()
+        res["s"] = time.perf_counter() - t0
+        res["info"] = zg.zg_index_info_get(idx)
+        del idx
+
+    for _ in range(max(1, args.warmup // 10)):  # untimed: pages in the host buffers
+        build()
+    th = threading.Thread(target=build)
+    th.start()
+    during = replay_times(lambda: not th.is_alive())
+    th.join()
+    info = res["info"]
+    n = int(info["n_input"])
+    line = {
+        "metric": "index rebuild items/s (sort + dedup + two-pass fill + H2D)", "value": n / res["s"],
+        "unit": "items/s", "n_gpus": 1, "higher_is_better": True, "data": "synthetic",
+        "config": {"workload": workload_desc(cfg), "items": n, "unique": int(info["n_unique"]),
+                   "index_bytes": int(info["bytes"]), "host_threads": os.cpu_count()},
+        "seconds": res["s"],
+        "phases_ms": {"sort": info["ms_sort"], "count": info["ms_count"], "fill_and_copy": info["ms_fill"],
+                      "total": info["ms_total"]},
+        "concurrent_decode": {"workload": "mid_sparse (fused, 8 CTAs a cluster)",
+                              "ms_alone_median": statistics.median(alone),
+                              "ms_during_rebuild_median": statistics.median(during) if during else None,
+                              "replays_during": len(during),
+                              "slowdown": (statistics.median(during) / statistics.median(alone)) if during else None},
+    }
+    print(json.dumps(line), flush=True)
 
 
 def main(argv=None):
@@ -489,12 +617,16 @@ def main(argv=None):
                     help="tune, capture and replay only (a short command for profilers)")
     ap.add_argument("--plan", default="", help="fixed per-step variants instead of tuning, e.g. sss or fss")
     ap.add_argument("--cluster", type=int, default=8, help="fused cluster size with --plan (0: no fusion)")
+    ap.add_argument("--index-rebuild", action="store_true",
+                    help="rebuild throughput of the workload's index while a decode is served (one JSON line)")
     args = ap.parse_args(argv)
     cfg = synth.CONFIGS[args.workload]
     if args.plan and len(args.plan) != cfg.L:
         ap.error(f"--plan needs {cfg.L} letters (s or f)")
     if args.impl == "reference":
         run_reference(args, cfg)
+    elif args.index_rebuild:
+        run_index_rebuild(args, cfg)
     else:
         run_gpu(args, cfg)
 

@@ -5,7 +5,7 @@ package is its thin binding.  Importing it fails loudly if the library has
 not been built (``__graft_entry__.build()``).
 """
 from ._lib import (DTYPES, LIB_PATH, ZG_BF16, ZG_F16, ZG_F32, ZG_FMT_DENSE, ZG_FMT_SPARSE,
-                   ZG_FORMAT_ALL_DENSE, ZG_FORMAT_ALL_SPARSE, ZG_FORMAT_AUTO, ZG_FULL,
+                   ZG_FORMAT_ALL_DENSE, ZG_FORMAT_ALL_SPARSE, ZG_FORMAT_AUTO, ZG_FULL, ZG_NAIVE,
                    ZG_MAX_BEAM, ZG_ORDER_FILTER_FIRST, ZG_ORDER_SCORE_FIRST, ZG_RESIDENT_DEVICE,
                    ZG_RESIDENT_HOST, ZG_SELECTIVE, Index, Plan, ZgError, make_model, zg_check_device_status, zg_decode, zg_decode_host,
                    zg_decode_host_workspace_size, zg_decode_static, zg_decode_trace,
@@ -16,7 +16,7 @@ from ._lib import (DTYPES, LIB_PATH, ZG_BF16, ZG_F16, ZG_F32, ZG_FMT_DENSE, ZG_F
 
 __all__ = [
     "DTYPES", "LIB_PATH", "ZG_BF16", "ZG_F16", "ZG_F32", "ZG_FMT_DENSE", "ZG_FMT_SPARSE",
-    "ZG_FORMAT_ALL_DENSE", "ZG_FORMAT_ALL_SPARSE", "ZG_FORMAT_AUTO", "ZG_FULL", "ZG_MAX_BEAM",
+    "ZG_FORMAT_ALL_DENSE", "ZG_FORMAT_ALL_SPARSE", "ZG_FORMAT_AUTO", "ZG_FULL", "ZG_MAX_BEAM", "ZG_NAIVE",
     "ZG_ORDER_FILTER_FIRST", "ZG_ORDER_SCORE_FIRST", "ZG_RESIDENT_DEVICE", "ZG_RESIDENT_HOST",
     "ZG_SELECTIVE", "Index", "Plan", "ZgError",
     "make_model", "zg_check_device_status", "zg_decode", "zg_decode_host",

@@ -21,7 +21,7 @@ STATUS_NAMES = {0: "ZG_OK", 1: "ZG_ERR_INVALID_ARG", 2: "ZG_ERR_OUT_OF_MEMORY", 
 ZG_F32, ZG_BF16, ZG_F16 = 0, 1, 2
 DTYPES = {"f32": ZG_F32, "bf16": ZG_BF16, "f16": ZG_F16}
 ZG_FMT_SPARSE, ZG_FMT_DENSE = 0, 1
-ZG_SELECTIVE, ZG_FULL = 0, 1
+ZG_SELECTIVE, ZG_FULL, ZG_NAIVE = 0, 1, 2
 ZG_RESIDENT_DEVICE, ZG_RESIDENT_HOST = 0, 1
 ZG_FORMAT_AUTO, ZG_FORMAT_ALL_SPARSE, ZG_FORMAT_ALL_DENSE = 0, 1, 2
 ZG_ORDER_FILTER_FIRST, ZG_ORDER_SCORE_FIRST = 0, 1

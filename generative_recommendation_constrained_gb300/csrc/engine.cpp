@@ -30,14 +30,17 @@ struct Dims {
   int L, V, d, w_dtype, B, beam, K;
   bool constrained;
   bool score_first;      // ZG_ORDER_SCORE_FIRST plan
+  bool naive[ZG_MAX_STEPS];  // ZG_NAIVE steps of the plan
+  size_t naive_rows;     // listed candidates the naive steps' workspace holds
+  int64_t nnz[ZG_MAX_STEPS];
   int S_full;            // padded token stride of full scores
   int nch_sel[ZG_MAX_STEPS];
   int S_sel[ZG_MAX_STEPS];
 };
 
 struct WsLayout {
-  size_t tok_hist, par_hist, row[2], cum[2], h[2], hhi, hlo, Z, part, part_all, mask, trace, u_stage, o_sids,
-      o_scores, total;
+  size_t tok_hist, par_hist, row[2], cum[2], h[2], hhi, hlo, Z, part, part_all, mask, naive_cnt, naive_off,
+      naive_list, naive_temp, trace, u_stage, o_sids, o_scores, total;
   size_t trace_bytes;
 };
 
@@ -77,6 +80,12 @@ WsLayout layout(const Dims& m, bool host_io) {
   if (m.score_first) {  // codebook-wide partials and per-beam token bitmaps
     w.part_all = take(BW * (m.S_full / kChunk) * 8);
     w.mask = take(BW * (size_t)((m.V + 31) / 32) * 4);
+  }
+  if (m.naive_rows) {  // fan-outs, offsets, compact list, temporary matrix
+    w.naive_cnt = take((BW + 1) * 4);
+    w.naive_off = take((BW + 1) * 4);
+    w.naive_list = take(m.naive_rows * 16);
+    w.naive_temp = take(m.naive_rows * (size_t)m.d * esize(m.w_dtype));
   }
   w.trace_bytes = 32 + (size_t)((m.V + 31) / 32) * 4;  // 4 counters + token mask
   w.trace = take(w.trace_bytes);
@@ -132,8 +141,27 @@ zg_status check_common(const zg_index* idx, const zg_model* model, int B, int be
     }
     d.nch_sel[s - 1] = nch;
     d.S_sel[s - 1] = nch * kChunk;
+    d.nnz[s - 1] = idx ? (int64_t)idx->steps[s - 1].nnz : 0;
   }
   *out = d;
+  return ZG_OK;
+}
+
+// What the plan changes in the decode's shape: the order, and the naive
+// steps' workspace (a request's beams are distinct prefixes, so its listed
+// candidates are at most min(beams * max_fanout, nnz) of the step).
+zg_status apply_plan(Dims& m, const zg_index* idx, const zg_plan* plan) {
+  m.score_first = idx && plan && plan->order == ZG_ORDER_SCORE_FIRST;
+  m.naive_rows = 0;
+  for (int s = 1; s <= m.L; ++s) {
+    m.naive[s - 1] = idx && plan && !m.score_first && plan->variant[s - 1] == ZG_NAIVE;
+    if (!m.naive[s - 1]) continue;
+    const int64_t Wc = (s == 1) ? 1 : m.beam;
+    const int64_t per = std::min<int64_t>(Wc * m.S_sel[s - 1], m.nnz[s - 1]);
+    m.naive_rows = std::max<size_t>(m.naive_rows, (size_t)m.B * (size_t)std::max<int64_t>(per, 1));
+  }
+  if ((double)m.naive_rows * m.d * esize(m.w_dtype) > 16.0 * (1ull << 30))
+    return fail(ZG_ERR_UNSUPPORTED, "naive variant: the temporary matrix would exceed 16 GiB; use a smaller batch");
   return ZG_OK;
 }
 
@@ -203,9 +231,10 @@ StepLaunch make_launch(const Run& r, int s, int variant) {
   a.u = r.u;
   a.W = r.model->W[s - 1];
   const bool full = (variant == ZG_FULL) || !r.idx || m.score_first;
+  const bool naive = !full && variant == ZG_NAIVE;
   // hidden of this step's beams: the next step's parents (s < L) and the
-  // full projection's input; at step 1 it is u itself
-  a.h_out = (s >= 2 && (s < m.L || full)) ? F32(r.w.h[s & 1]) : nullptr;
+  // full projection's (or naive scores') input; at step 1 it is u itself
+  a.h_out = (s >= 2 && (s < m.L || full || naive)) ? F32(r.w.h[s & 1]) : nullptr;
   a.Z = F32(r.w.Z);
   a.row_out = r.idx ? U32(r.w.row[s & 1]) : nullptr;
   a.cum_out = F32(r.w.cum[s & 1]);
@@ -214,7 +243,20 @@ StepLaunch make_launch(const Run& r, int s, int variant) {
   a.out_sids = r.out_sids;
   a.out_scores = r.out_scores;
   a.status = r.status;
-  if (!full) {
+  if (naive) {
+    // scores land in padded slots (sparse: slot = rank, dense: slot = token);
+    // no chunk partials: the select computes its log-sum-exp from the slots
+    if (r.idx->steps[s - 1].fmt == ZG_FMT_SPARSE) {
+      a.mode = kSelSparse;
+      a.nch = m.nch_sel[s - 1];
+      a.S = m.S_sel[s - 1];
+    } else {
+      a.mode = kFullDense;
+      a.nch = m.S_full / kChunk;
+      a.S = m.S_full;
+    }
+    a.part = nullptr;
+  } else if (!full) {
     const StepMeta& sm = r.idx->steps[s - 1];
     a.mode = sm.fmt == ZG_FMT_SPARSE ? kSelSparse : kSelDense;
     a.nch = m.nch_sel[s - 1];
@@ -254,7 +296,23 @@ zg_status run_step(const Run& r, int s, int variant, cudaStream_t st, const Step
   const StepLaunch a = make_launch(r, s, variant);
   cudaError_t e;
   if (tm) cudaEventRecord(tm->ev[0], st);
-  if (a.mode == kSelSparse || a.mode == kSelDense) {
+  if (variant == ZG_NAIVE && r.m.naive[s - 1]) {
+    const float* H = r.u;
+    if (s >= 2) {
+      e = launch_gather_add(a, a.h_out, st);
+      if (e != cudaSuccess) return cuda_fail(e, "gather-add launch");
+      H = a.h_out;
+    }
+    auto* cnt = reinterpret_cast<int32_t*>(r.ws + r.w.naive_cnt);
+    auto* off = reinterpret_cast<int32_t*>(r.ws + r.w.naive_off);
+    auto* list = reinterpret_cast<int4*>(r.ws + r.w.naive_list);
+    void* temp = r.ws + r.w.naive_temp;
+    e = launch_naive_compact(a, cnt, off, list, temp, (int64_t)r.m.naive_rows, st);
+    if (e != cudaSuccess) return cuda_fail(e, "naive compaction launch");
+    if (tm) cudaEventRecord(tm->ev[1], st);
+    e = launch_naive_dot(a, off, list, temp, H, (int64_t)r.m.naive_rows, st);
+    if (e != cudaSuccess) return cuda_fail(e, "naive scoring launch");
+  } else if (a.mode == kSelSparse || a.mode == kSelDense) {
     if (tm) cudaEventRecord(tm->ev[1], st);
     e = launch_selective(a, st);
     if (e != cudaSuccess) return cuda_fail(e, "selective projection launch");
@@ -303,7 +361,7 @@ zg_status prepare(const zg_index* idx, const zg_plan* plan, const zg_model* mode
   zg_status st = check_common(idx, model, B, beam, K, &m);
   if (st != ZG_OK) return st;
   if (plan && plan->L != m.L) return fail(ZG_ERR_INVALID_ARG, "plan has a different number of steps");
-  m.score_first = idx && plan && plan->order == ZG_ORDER_SCORE_FIRST;
+  if ((st = apply_plan(m, idx, plan)) != ZG_OK) return st;
   if (!u || !out_sids || !out_scores) return fail(ZG_ERR_INVALID_ARG, "u, out_sids and out_scores must not be NULL");
   if (!host_io && reinterpret_cast<uintptr_t>(u) % 16) return fail(ZG_ERR_INVALID_ARG, "u must be 16-byte aligned");
   if (!ws) return fail(ZG_ERR_INVALID_ARG, "workspace is NULL");
@@ -425,8 +483,8 @@ zg_status zg_plan_force(const zg_index* idx, int32_t B, int32_t beam, const uint
   *out = nullptr;
   if (!idx || !variant) return fail(ZG_ERR_INVALID_ARG, "zg_plan_force: idx and variant must not be NULL");
   for (int s = 0; s < idx->L; ++s)
-    if (variant[s] != ZG_SELECTIVE && variant[s] != ZG_FULL)
-      return fail(ZG_ERR_INVALID_ARG, "zg_plan_force: variant must be ZG_SELECTIVE or ZG_FULL");
+    if (variant[s] != ZG_SELECTIVE && variant[s] != ZG_FULL && variant[s] != ZG_NAIVE)
+      return fail(ZG_ERR_INVALID_ARG, "zg_plan_force: variant must be ZG_SELECTIVE, ZG_FULL or ZG_NAIVE");
   auto* p = new zg_plan();
   p->L = idx->L;
   p->B = B;
@@ -472,7 +530,8 @@ zg_status zg_decode_workspace_size(const zg_index* idx, const zg_plan* plan, con
   Dims m;
   zg_status st = check_common(idx, model, B, beam, K, &m);
   if (st != ZG_OK) return st;
-  m.score_first = idx && plan && plan->order == ZG_ORDER_SCORE_FIRST;
+  if (plan && plan->L != m.L) return fail(ZG_ERR_INVALID_ARG, "plan has a different number of steps");
+  if ((st = apply_plan(m, idx, plan)) != ZG_OK) return st;
   *bytes = layout(m, false).total;
   return ZG_OK;
 }
@@ -483,7 +542,8 @@ zg_status zg_decode_host_workspace_size(const zg_index* idx, const zg_plan* plan
   Dims m;
   zg_status st = check_common(idx, model, B, beam, K, &m);
   if (st != ZG_OK) return st;
-  m.score_first = idx && plan && plan->order == ZG_ORDER_SCORE_FIRST;
+  if (plan && plan->L != m.L) return fail(ZG_ERR_INVALID_ARG, "plan has a different number of steps");
+  if ((st = apply_plan(m, idx, plan)) != ZG_OK) return st;
   *bytes = layout(m, true).total;
   return ZG_OK;
 }
@@ -729,7 +789,7 @@ zg_status zg_decode_trace(const zg_index* idx, const zg_plan* plan, const zg_mod
     cudaEventElapsedTime(&g, tm.ev[0], tm.ev[1]);
     cudaEventElapsedTime(&pj, tm.ev[1], tm.ev[2]);
     cudaEventElapsedTime(&q, tm.ev[2], tm.ev[3]);
-    t.ms_gather = (v == ZG_FULL && (step >= 2 || r.m.w_dtype != ZG_F32)) ? g : 0.f;
+    t.ms_gather = (v == ZG_NAIVE || (v == ZG_FULL && (step >= 2 || r.m.w_dtype != ZG_F32))) ? g : 0.f;
     t.ms_project = pj;
     t.ms_select = q;
   }

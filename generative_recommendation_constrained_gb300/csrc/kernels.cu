@@ -473,16 +473,6 @@ __global__ void __launch_bounds__(256) k_trace_touch(const __grid_constant__ Ste
   }
 }
 
-int sm_count() {
-  static int n = 0;
-  if (!n) {
-    int dv = 0;
-    cudaGetDevice(&dv);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dv);
-    if (n <= 0) n = 148;
-  }
-  return n;
-}
 
 template <typename WT>
 int vpl_for(int d) {
@@ -550,6 +540,17 @@ cudaError_t launch_cluster_t(const MegaArgs& A, int B, int G, int d, cudaStream_
 }
 
 }  // namespace
+
+int sm_count() {
+  static int n = 0;
+  if (!n) {
+    int dv = 0;
+    cudaGetDevice(&dv);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dv);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
 
 cudaError_t launch_selective(const StepLaunch& a, cudaStream_t st) {
   switch (a.w_dtype) {

@@ -121,6 +121,14 @@ cudaError_t launch_gather_add(const StepLaunch& a, float* H, cudaStream_t st);
 cudaError_t launch_full_simt(const StepLaunch& a, const float* H, const FullEpi& epi, cudaStream_t st);
 cudaError_t launch_select(const StepLaunch& a, cudaStream_t st);
 cudaError_t launch_legal_mask(const StepLaunch& a, cudaStream_t st);
+int sm_count();  // streaming multiprocessors of the current device
+// naive legal-only contrast (naive.cu): compaction + temporary matrix, then the scores
+// (cap: rows the list and the temporary matrix hold; candidates beyond it are
+// dropped and flagged kStatusRow)
+cudaError_t launch_naive_compact(const StepLaunch& a, int32_t* cnt, int32_t* off, int4* list, void* temp,
+                                 int64_t cap, cudaStream_t st);
+cudaError_t launch_naive_dot(const StepLaunch& a, const int32_t* off, const int4* list, const void* temp,
+                             const float* H, int64_t cap, cudaStream_t st);
 // A device region the fused kernel prefetches into L2 (16-byte aligned).
 struct PrefetchRegion {
   const void* ptr;

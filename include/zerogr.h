@@ -64,7 +64,7 @@ typedef enum {
 
 typedef enum { ZG_F32 = 0, ZG_BF16 = 1, ZG_F16 = 2 } zg_dtype;
 typedef enum { ZG_FMT_SPARSE = 0, ZG_FMT_DENSE = 1 } zg_format;
-typedef enum { ZG_SELECTIVE = 0, ZG_FULL = 1 } zg_variant;
+typedef enum { ZG_SELECTIVE = 0, ZG_FULL = 1, ZG_NAIVE = 2 } zg_variant;
 typedef enum { ZG_RESIDENT_DEVICE = 0, ZG_RESIDENT_HOST = 1 } zg_residency;
 typedef enum { ZG_FORMAT_AUTO = 0, ZG_FORMAT_ALL_SPARSE = 1, ZG_FORMAT_ALL_DENSE = 2 } zg_format_mode;
 typedef enum { ZG_ORDER_FILTER_FIRST = 0, ZG_ORDER_SCORE_FIRST = 1 } zg_order;
@@ -168,13 +168,21 @@ ZG_API void zg_index_free(zg_index* idx);
  *                 the step gets max_fanout slots, or V on dense steps).
  *   ZG_FULL:      project every token (a dense contraction), then pick the
  *                 legal ones.
+ *   ZG_NAIVE:     measurement contrast only (never chosen by zg_tune): legal
+ *                 tokens scored the straightforward way of [Speed]'s figure -
+ *                 compact every beam's candidates into one list (count, scan,
+ *                 list), copy their weight rows into a temporary matrix, dot
+ *                 each row with its beam's hidden vector.  Its workspace holds
+ *                 B * min(beams * max_fanout, nnz) listed rows of the step;
+ *                 ZG_ERR_UNSUPPORTED above 16 GiB.
  * zg_tune runs the decode step by step on warm_u (device float32 [B][d]):
  * each variant of step s runs 2 warm-up times and `reps` timed times on the
  * same entering state (CUDA events on `stream`); the faster is kept and
  * advances the state.  Allocates and frees its own workspace.  Synchronous. */
 ZG_API zg_status zg_tune(const zg_index* idx, const zg_model* model, const float* warm_u, int32_t B,
                   int32_t beam, int32_t K, int32_t reps, void* stream, zg_plan** out);
-/* A plan with a fixed variant per step (variant: host uint8 [L]). */
+/* A plan with a fixed variant per step (variant: host uint8 [L], each
+ * ZG_SELECTIVE, ZG_FULL or ZG_NAIVE). */
 ZG_API zg_status zg_plan_force(const zg_index* idx, int32_t B, int32_t beam, const uint8_t* variant,
                         zg_plan** out);
 /* How zg_decode runs the plan's trailing run of ZG_SELECTIVE steps: as one

@@ -188,4 +188,19 @@ def test_plan_force_checks(zg):
     with pytest.raises(zg.ZgError):
         zg.zg_plan_set_fusion(p, 3)
     with pytest.raises(zg.ZgError):
-        zg.zg_plan_force(idx, 2, 4, [0, 2, 0])
+        zg.zg_plan_force(idx, 2, 4, [0, 3, 0])
+
+
+def test_plan_variants_and_order_checked(zg):
+    """zg_plan_force takes ZG_SELECTIVE / ZG_FULL / ZG_NAIVE only; the order
+    setter takes the two orders only (host-side checks, no GPU)."""
+    idx = zg.zg_index_build(tiny_catalogue(3, 16, 50, 2), 16, residency=zg.ZG_RESIDENT_HOST)
+    L = zg.zg_index_info_get(idx)["L"]
+    p = zg.zg_plan_force(idx, 2, 4, [zg.ZG_NAIVE] * L)
+    assert list(zg.zg_plan_describe(p)[0]) == [zg.ZG_NAIVE] * L
+    zg.zg_plan_set_order(p, zg.ZG_ORDER_SCORE_FIRST)
+    zg.zg_plan_set_order(p, zg.ZG_ORDER_FILTER_FIRST)
+    with pytest.raises(zg.ZgError):
+        zg.zg_plan_set_order(p, 2)
+    with pytest.raises(zg.ZgError):
+        zg.zg_plan_force(idx, 2, 4, [3] * L)

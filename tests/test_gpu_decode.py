@@ -500,3 +500,44 @@ def test_score_first_tensor_core_dense_step(zg, mode):
     plan = _score_first_plan(zg, idx, 3, 16, 2)
     s, sc = decode_gpu(zg, idx, model, u, 16, 16, plan=plan)
     check_topk(s, sc, ref, trie, model, u, 2e-2, WINDOW, order="score_first")
+
+
+# ------------------------------------------------------------ naive contrast variant
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("variants", [[2, 2, 2], [2, 0, 1], [1, 2, 0]])
+def test_naive_variant_tiny(zg, mode, variants):
+    """The compact-list contrast (count, scan, list, temporary matrix, dots)
+    scores the same candidates: parity with the oracle in every format mode,
+    mixed with the other variants."""
+    cfg = synth.CONFIGS["tiny"]
+    sids = synth.make_catalogue(cfg)
+    model = synth.make_model(cfg.L, cfg.V, cfg.d, "f32", 2)
+    u = synth.make_requests(4, cfg.d, 2)
+    idx = zg.zg_index_build(sids, cfg.V, format_mode=mode, stream=_stream())
+    trie = oracle.Trie(sids, cfg.L, cfg.V)
+    ref = oracle.decode(trie, model, u, cfg.beam, cfg.topk)
+    s, sc = decode_gpu(zg, idx, model, u, cfg.beam, cfg.topk, variants)
+    check_topk(s, sc, ref, trie, model, u, 1e-4, WINDOW)
+
+
+def test_naive_variant_mid_sparse(zg, mid):
+    cfg, sids, model, u, trie, ref, idx = mid
+    s, sc = decode_gpu(zg, idx, model, u, cfg.beam, cfg.topk, [2, 2, 2])
+    check_topk(s, sc, ref, trie, model, u, 1e-4, WINDOW)
+    a = decode_gpu(zg, idx, model, u, cfg.beam, cfg.topk, [0, 0, 0], fused=0)
+    d = np.nan_to_num(np.abs(sc - a[1]), posinf=0.0)
+    assert np.mean(d < 1e-4) > 0.95
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_naive_variant_half_weights(zg, dtype):
+    cfg = synth.CONFIGS["tiny"]
+    sids = synth.make_catalogue(cfg)
+    model = synth.make_model(cfg.L, cfg.V, cfg.d, dtype, 3)
+    u = synth.make_requests(3, cfg.d, 3)
+    idx = zg.zg_index_build(sids, cfg.V, stream=_stream())
+    trie = oracle.Trie(sids, cfg.L, cfg.V)
+    ref = oracle.decode(trie, model, u, cfg.beam, cfg.topk)
+    s, sc = decode_gpu(zg, idx, model, u, cfg.beam, cfg.topk, [2, 2, 2])
+    check_topk(s, sc, ref, trie, model, u, 2e-2, WINDOW)
