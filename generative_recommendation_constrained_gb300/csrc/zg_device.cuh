@@ -1161,6 +1161,8 @@ __device__ int cta_select_bins(const StepLaunch& a, int q, BeamTab& bt, SW& sw, 
 //   2. The candidates >= tc of the chunks whose maximum reaches tc are cut
 //      again for keep over [tc, kceil]: cut key t2.
 //   3. The candidates >= t2 are listed and placed in descending order.
+// For a small keep (16 * keep within the list space) the candidates >= tc are
+// listed and placed at once, and 2 and 3 run only if that list overflows.
 // In 2 and 3 each warp tests 32 chunks at once (lane l: chunk i0 + l * NW +
 // warp) and scores the passing ones U at a time.  Returns -1 (caller falls
 // back) when the key range is unknown or the final list would not fit in the
@@ -1214,16 +1216,20 @@ __device__ int cta_select_chunks(const StepLaunch& a, int q, BeamTab& bt, SW& sw
   if (hist_cut<NT>(hist, sw, (uint32_t)keep_n) < (uint32_t)keep_n) return -1;
   const uint32_t tc = lo + (sw.prefix << sh);
   const int sh2 = bin_shift(tc, hi);
-  for (int i = tid; i < kBins; i += NT) hist[i] = 0u;
-  __syncthreads();
-  for (int pass = 2; pass <= 3; ++pass) {
-    uint32_t t2 = 0u;
+  // a small keep lists every candidate >= tc at once (pass 1) and cuts again
+  // only when that list overflows; a large keep cuts again first (pass 2)
+  const int first = (keep_n * 16 <= LCAP) ? 1 : 2;
+  if (first == 2) {
+    for (int i = tid; i < kBins; i += NT) hist[i] = 0u;
+    __syncthreads();
+  }
+  for (int pass = first; pass <= 3; ++pass) {
+    uint32_t tmin = tc;  // >= lo >= 1
     if (pass == 3) {
       if (hist_cut<NT>(hist, sw, (uint32_t)keep_n) < (uint32_t)keep_n) return -1;
       if (sw.cnt_gt + sw.cnt_eq > LCAP) return -1;
-      t2 = tc + (sw.prefix << sh2);
+      tmin = tc + (sw.prefix << sh2);
     }
-    const uint32_t tmin = (pass == 2) ? tc : t2;  // >= lo >= 1
     for (int i0 = 0; i0 < nitems; i0 += NT) {
       const int ic = i0 + lane * NW + warp;
       const bool pass_c = (ic < nitems) && ckb[(size_t)ic * st] >= tmin;
@@ -1257,12 +1263,21 @@ __device__ int cta_select_chunks(const StepLaunch& a, int q, BeamTab& bt, SW& sw
           if (pass == 2) {
             if (key[u] >= tc) atomicAdd(&hist[bin_of(key[u], tc, sh2)], 1u);
           } else {
-            warp_append(list, LCAP, sw.nwin, key[u] >= t2, key[u], flat[u], lane);
+            warp_append(list, LCAP, sw.nwin, key[u] >= tmin, key[u], flat[u], lane);
           }
         }
       }
     }
     __syncthreads();
+    if (pass == 1) {
+      const int nl = sw.nwin;  // the same in every thread
+      if (nl <= LCAP) {
+        place_winners<NT>(list, nl, keep_n, sw);
+        return keep_n;
+      }
+      for (int i = tid; i < kBins; i += NT) hist[i] = 0u;  // overflow: cut again
+      __syncthreads();
+    }
   }
   place_winners<NT>(list, sw.cnt_gt + sw.cnt_eq, keep_n, sw);
   return keep_n;
