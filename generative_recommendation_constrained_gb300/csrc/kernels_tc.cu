@@ -16,10 +16,13 @@
 // One CTA computes a 128 x 256 tile: warp 0 issues TMA loads (128-byte
 // swizzled K-major tiles) into a 3-stage shared-memory ring guarded by
 // mbarriers, warp 1 owns the tensor-memory accumulator and issues
-// tcgen05.mma from one thread, warps 2-5 read the accumulator back with
-// tcgen05.ld and store the fp32 scores.  Every wait is bounded; on expiry the
-// kernel records kStatusTimeout, drains its own copies, frees its tensor
-// memory and returns.
+// tcgen05.mma from one thread, warps 2-9 (two per 32-lane quarter of the
+// accumulator, one per 128-column half) read it back with tcgen05.ld, fold
+// the chunk partials, and store the fp32 scores as 32 x 32 blocks staged in
+// the spent ring (128-byte swizzle) and written by TMA stores, so every row
+// segment reaches memory in whole 128-byte lines.  Every wait is bounded; on
+// expiry the kernel records kStatusTimeout, drains its own copies, frees its
+// tensor memory and returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -35,7 +38,7 @@ constexpr int kTileA = kBM * kBK * 2;          // 16 KiB
 constexpr int kTileB = kBN * kBK * 2;          // 32 KiB
 constexpr int kStageBytes = 2 * kTileA + kTileB;
 constexpr int kTmemCols = 256;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // producer, MMA issuer, 8 epilogue warps
 constexpr uint32_t kSpinLimit = 1u << 26;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -93,6 +96,14 @@ __device__ __forceinline__ uint32_t instr_desc(uint32_t ab) {
   return (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
 }
 
+// 2-D TMA store of a 32 x 32 fp32 block from shared memory (bulk group).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(x), "r"(y)
+               : "memory");
+}
+
 __device__ __forceinline__ void mma_f16(uint32_t tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accum) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(
@@ -123,7 +134,8 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
 
 __global__ void __launch_bounds__(kThreads, 1)
     k_full_tc(const __grid_constant__ CUtensorMap map_hi, const __grid_constant__ CUtensorMap map_lo,
-              const __grid_constant__ CUtensorMap map_w, float* __restrict__ Z, int M, int V, int d, int ldz,
+              const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_z, int M, int V,
+              int d, int ldz,
               uint32_t ab_type, const FullEpi epi, uint32_t* status) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // stage buffers must sit on 1024-byte boundaries (swizzle atoms)
@@ -205,56 +217,79 @@ __global__ void __launch_bounds__(kThreads, 1)
     (void)ok;
     mma_commit(&acc_bar);  // arrives once every MMA issued above has completed
   } else if (warp >= 2) {
-    // epilogue: TMEM -> registers -> Z (one row per thread)
+    // epilogue: TMEM -> registers (one row a thread) -> partials, and the
+    // scores through swizzled staging blocks to TMA stores
     const bool got = mbar_wait(&acc_bar, 0);
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     if (!got) {
       if (lane == 0) atomicOr(status, kStatusTimeout);
     } else if (!atomicAdd(&abort_flag, 0)) {
-      const int quarter = warp & 3;
+      const int e = warp - 2;            // 0..7
+      const int quarter = warp & 3;      // the accumulator lanes this warp may read
+      const int half = e >> 2;           // 128-column half of the tile
       const int row = m0 + quarter * 32 + lane;
       const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
-      for (int c0 = 0; c0 < kBN; c0 += 32) {
+      uint32_t brow = 0;                 // legal-bitmap row of this beam row
+      bool dead = false;
+      if (epi.bitmap && row < M) {
+        brow = epi.by_m ? (uint32_t)row : (epi.rows ? epi.rows[row] : 0u);
+        dead = (brow == kDeadRow);
+      }
+      uint8_t* stage = smem + e * 8192;  // two 4 KiB blocks (the ring is spent)
+      int issued = 0;
+      for (int ci = 0; ci < kBN / 64; ++ci) {
+        const int c0 = half * (kBN / 2) + ci * 32;
         float v[32];
         tmem_ld32(lane_addr + (uint32_t)c0, v);
-        if (row < M && n0 + c0 < V) {
-          float* zr = Z + (size_t)row * ldz + n0 + c0;
-          if (n0 + c0 + 32 <= V) {
+        if (n0 + c0 >= V) continue;  // uniform: a block wholly past the codebook
+        const int chunk = (n0 + c0) >> 5;
+        const int rem = V - (n0 + c0);
+        const uint32_t vm = rem >= 32 ? 0xFFFFFFFFu : ((1u << rem) - 1u);
+        if (row < M && epi.part) {
+          // legal-only (max, sum exp) of this 32-token chunk (the fast
+          // exponential: ~1e-6 relative, far inside the score tolerance)
+          const uint32_t lm = dead ? 0u : (epi.bitmap ? epi.bitmap[(size_t)brow * epi.words + chunk] & vm : vm);
+          float mx = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < 32; i += 4) *reinterpret_cast<float4*>(zr + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-          } else {
-            for (int i = 0; i < 32 && n0 + c0 + i < V; ++i) zr[i] = v[i];
+          for (int i = 0; i < 32; ++i) mx = ((lm >> i) & 1u) ? fmaxf(mx, v[i]) : mx;
+          float sm = 0.f;
+          if (mx != -INFINITY) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) sm += ((lm >> i) & 1u) ? __expf(v[i] - mx) : 0.f;
           }
-          if (epi.part) {
-            // legal-only (max, sum exp) of this 32-token chunk (the fast
-            // exponential: ~1e-6 relative, far inside the score tolerance)
-            const int chunk = (n0 + c0) >> 5;
-            const uint32_t lm = epi_legal_mask(epi, row, chunk, V);
-            float mx = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) mx = ((lm >> i) & 1u) ? fmaxf(mx, v[i]) : mx;
-            float sm = 0.f;
-            if (mx != -INFINITY) {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) sm += ((lm >> i) & 1u) ? __expf(v[i] - mx) : 0.f;
-            }
-            epi.part[(size_t)row * (ldz >> 5) + chunk] = make_float2(mx, sm);
-          }
-          if (epi.part_all) {
-            // (max, sum exp) over every token of the chunk (score-first normaliser)
-            const int chunk = (n0 + c0) >> 5;
-            const int rem = V - (n0 + c0);
-            const uint32_t vm = rem >= 32 ? 0xFFFFFFFFu : ((1u << rem) - 1u);
-            float mx = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) mx = ((vm >> i) & 1u) ? fmaxf(mx, v[i]) : mx;
-            float sm = 0.f;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) sm += ((vm >> i) & 1u) ? __expf(v[i] - mx) : 0.f;
-            epi.part_all[(size_t)row * (ldz >> 5) + chunk] = make_float2(mx, sm);
-          }
+          epi.part[(size_t)row * (ldz >> 5) + chunk] = make_float2(mx, sm);
         }
+        if (row < M && epi.part_all) {
+          // (max, sum exp) over every token of the chunk (score-first normaliser)
+          float mx = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mx = ((vm >> i) & 1u) ? fmaxf(mx, v[i]) : mx;
+          float sm = 0.f;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) sm += ((vm >> i) & 1u) ? __expf(v[i] - mx) : 0.f;
+          epi.part_all[(size_t)row * (ldz >> 5) + chunk] = make_float2(mx, sm);
+        }
+        // stage the 32 x 32 block (row = lane; 16-byte piece j of a row at
+        // j ^ (row & 7): the 128-byte swizzle of the store map), then store
+        uint8_t* buf = stage + (issued & 1) * 4096;
+        if (issued >= 2) {
+          if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+          __syncwarp();
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<float4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+              make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&map_z, buf, n0 + c0, m0 + quarter * 32);
+          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+        ++issued;
       }
+      if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+      __syncwarp();
     }
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -342,12 +377,25 @@ cudaError_t launch_split_h(const float* H, void* hi, void* lo, size_t n, int w_d
   return cudaGetLastError();
 }
 
+// Store map of the scores: fp32 [rows][ldz], 32 x 32 boxes, 128B swizzle.
+bool make_store_map(CUtensorMap* m, float* Z, int rows, int ldz) {
+  EncodeFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)ldz, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ldz * 4};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, Z, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 cudaError_t launch_full_tc(const void* hi, const void* lo, const void* W, float* Z, int M, int V, int d, int ldz,
                            int w_dtype, const FullEpi& epi, uint32_t* status, cudaStream_t st) {
   const bool bf16 = (w_dtype == ZG_BF16);
-  CUtensorMap mh, ml, mw;
-  if (!make_map(&mh, hi, M, d, kBM, bf16) || !make_map(&ml, lo, M, d, kBM, bf16) ||
-      !make_map(&mw, W, V, d, kBN, bf16))
+  CUtensorMap mh, ml, mw, mz;
+  if (ldz % 32 != 0 || !make_map(&mh, hi, M, d, kBM, bf16) || !make_map(&ml, lo, M, d, kBM, bf16) ||
+      !make_map(&mw, W, V, d, kBN, bf16) || !make_store_map(&mz, Z, M, ldz))
     return cudaErrorInvalidValue;
   static bool attr_done = false;
   const size_t smem = full_tc_smem_bytes();
@@ -357,7 +405,7 @@ cudaError_t launch_full_tc(const void* hi, const void* lo, const void* W, float*
     attr_done = true;
   }
   dim3 grid((V + kBN - 1) / kBN, (M + kBM - 1) / kBM);
-  k_full_tc<<<grid, kThreads, smem, st>>>(mh, ml, mw, Z, M, V, d, ldz, bf16 ? 1u : 0u, epi, status);
+  k_full_tc<<<grid, kThreads, smem, st>>>(mh, ml, mw, mz, M, V, d, ldz, bf16 ? 1u : 0u, epi, status);
   return cudaGetLastError();
 }
 
