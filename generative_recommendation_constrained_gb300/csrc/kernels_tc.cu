@@ -13,14 +13,15 @@
 // fp32 selective projection to ~1e-6 instead of the ~1e-3 a single rounding
 // of H would give.
 //
-// One CTA computes a 128 x 256 tile: warp 0 issues TMA loads (128-byte
-// swizzled K-major tiles) into a 3-stage shared-memory ring guarded by
-// mbarriers, warp 1 owns the tensor-memory accumulator and issues
-// tcgen05.mma from one thread, warps 2-9 (two per 32-lane quarter of the
-// accumulator, one per 128-column half) read it back with tcgen05.ld, fold
-// the chunk partials, and store the fp32 scores as 32 x 32 blocks staged in
-// the spent ring (128-byte swizzle) and written by TMA stores, so every row
-// segment reaches memory in whole 128-byte lines.  Every wait is bounded; on
+// Persistent CTAs (one per SM) walk 128 x 256 tiles: warp 0 issues TMA loads
+// (128-byte swizzled K-major tiles) into a 3-stage shared-memory ring guarded
+// by mbarriers, running ahead into the next tile; warp 1 owns two
+// tensor-memory accumulators and issues tcgen05.mma from one thread into the
+// one the epilogue has released; warps 2-9 (two per 32-lane quarter of the
+// accumulator, one per 128-column half) read the other back with tcgen05.ld,
+// fold the chunk partials, and store the fp32 scores as 32 x 32 blocks staged
+// with the 128-byte swizzle and written by TMA stores (whole 128-byte lines),
+// so a tile's epilogue overlaps the next tile's loads and MMAs.  Every wait is bounded; on
 // expiry the kernel records kStatusTimeout, drains its own copies, frees its
 // tensor memory and returns.
 #include <cuda.h>
@@ -38,7 +39,8 @@ constexpr int kTileA = kBM * kBK * 2;          // 16 KiB
 constexpr int kTileB = kBN * kBK * 2;          // 32 KiB
 constexpr int kStageBytes = 2 * kTileA + kTileB;
 constexpr int kTmemCols = 256;
-constexpr int kThreads = 320;  // producer, MMA issuer, 8 epilogue warps
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer, MMA issuer, epilogue warps
 constexpr uint32_t kSpinLimit = 1u << 26;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -135,30 +137,35 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
 __global__ void __launch_bounds__(kThreads, 1)
     k_full_tc(const __grid_constant__ CUtensorMap map_hi, const __grid_constant__ CUtensorMap map_lo,
               const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_z, int M, int V,
-              int d, int ldz,
-              uint32_t ab_type, const FullEpi epi, uint32_t* status) {
+              int d, int ldz, uint32_t ab_type, const FullEpi epi, uint32_t* status) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // stage buffers must sit on 1024-byte boundaries (swizzle atoms)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t full_bar[kStages], empty_bar[kStages], acc_bar;
+  uint8_t* staging = smem + kStages * kStageBytes;  // one 4 KiB block per epilogue warp
+  __shared__ uint64_t full_bar[kStages], empty_bar[kStages], tfull_bar[2], tempty_bar[2];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * kBN, m0 = blockIdx.y * kBM;
   const int nk = (d + kBK - 1) / kBK;
+  const int ntn = (V + kBN - 1) / kBN;
+  const int ntiles = ntn * ((M + kBM - 1) / kBM);
+  // tiles of this CTA: blockIdx.x, + gridDim.x, ...; tile t = (m-tile t / ntn, n-tile t % ntn)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&full_bar[i], 1);
       mbar_init(&empty_bar[i], 1);
     }
-    mbar_init(&acc_bar, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull_bar[i], 1);
+      mbar_init(&tempty_bar[i], kEpiWarps);
+    }
     abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base)),
-                 "r"(kTmemCols)
+                 "r"(2 * kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -168,75 +175,93 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = tmem_base;
 
   if (warp == 0 && lane == 0) {
-    // producer: TMA ring
-    int issued = 0;
-    for (int kb = 0; kb < nk; ++kb) {
-      const int st = kb % kStages;
-      if (kb >= kStages && !mbar_wait(&empty_bar[st], ((kb / kStages) - 1) & 1)) {
-        atomicOr(status, kStatusTimeout);
-        atomicExch(&abort_flag, 1);
-        break;
+    // producer: TMA ring, running ahead across tiles
+    int kg = 0;  // k-blocks issued by this CTA
+    for (int t = blockIdx.x; t < ntiles && !atomicAdd(&abort_flag, 0); t += gridDim.x) {
+      const int m0 = (t / ntn) * kBM, n0 = (t % ntn) * kBN;
+      for (int kb = 0; kb < nk; ++kb, ++kg) {
+        const int st = kg % kStages;
+        if (kg >= kStages && !mbar_wait(&empty_bar[st], ((kg / kStages) - 1) & 1)) {
+          atomicOr(status, kStatusTimeout);
+          atomicExch(&abort_flag, 1);
+          break;
+        }
+        uint8_t* sa_hi = smem + st * kStageBytes;
+        uint8_t* sa_lo = sa_hi + kTileA;
+        uint8_t* sb = sa_lo + kTileA;
+        mbar_expect_tx(&full_bar[st], kStageBytes);
+        tma_load_2d(sa_hi, &map_hi, &full_bar[st], kb * kBK, m0);
+        tma_load_2d(sa_lo, &map_lo, &full_bar[st], kb * kBK, m0);
+        tma_load_2d(sb, &map_w, &full_bar[st], kb * kBK, n0);
       }
-      if (atomicAdd(&abort_flag, 0)) break;
-      uint8_t* sa_hi = smem + st * kStageBytes;
-      uint8_t* sa_lo = sa_hi + kTileA;
-      uint8_t* sb = sa_lo + kTileA;
-      mbar_expect_tx(&full_bar[st], kStageBytes);
-      tma_load_2d(sa_hi, &map_hi, &full_bar[st], kb * kBK, m0);
-      tma_load_2d(sa_lo, &map_lo, &full_bar[st], kb * kBK, m0);
-      tma_load_2d(sb, &map_w, &full_bar[st], kb * kBK, n0);
-      ++issued;
     }
     // drain: every issued stage must have landed before the CTA may exit
-    for (int kb = (issued > kStages ? issued - kStages : 0); kb < issued; ++kb)
-      mbar_wait(&full_bar[kb % kStages], (kb / kStages) & 1);
+    for (int k = (kg > kStages ? kg - kStages : 0); k < kg; ++k) mbar_wait(&full_bar[k % kStages], (k / kStages) & 1);
   } else if (warp == 1 && lane == 0) {
-    // MMA issuer
+    // MMA issuer: accumulator buffer (i & 1) for the i-th tile of this CTA
     const uint32_t idesc = instr_desc(ab_type);
-    bool ok = true;
-    for (int kb = 0; kb < nk; ++kb) {
-      const int st = kb % kStages;
-      if (!mbar_wait(&full_bar[st], (kb / kStages) & 1) || atomicAdd(&abort_flag, 0)) {
+    int kg = 0, i = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+      const int b = i & 1;
+      if (atomicAdd(&abort_flag, 0) || (i >= 2 && !mbar_wait(&tempty_bar[b], ((i >> 1) - 1) & 1))) {
         atomicOr(status, kStatusTimeout);
         atomicExch(&abort_flag, 1);
-        ok = false;
         break;
       }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const uint8_t* sa_hi = smem + st * kStageBytes;
-      const uint8_t* sa_lo = sa_hi + kTileA;
-      const uint8_t* sb = sa_lo + kTileA;
+      const uint32_t acc = tmem + (uint32_t)(b * kTmemCols);
+      bool ok = true;
+      for (int kb = 0; kb < nk; ++kb, ++kg) {
+        const int st = kg % kStages;
+        if (!mbar_wait(&full_bar[st], (kg / kStages) & 1) || atomicAdd(&abort_flag, 0)) {
+          atomicOr(status, kStatusTimeout);
+          atomicExch(&abort_flag, 1);
+          ok = false;
+          break;
+        }
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint8_t* sa_hi = smem + st * kStageBytes;
+        const uint8_t* sa_lo = sa_hi + kTileA;
+        const uint8_t* sb = sa_lo + kTileA;
 #pragma unroll
-      for (int kk = 0; kk < kBK / 16; ++kk) {
-        const uint64_t bd = smem_desc(sb + kk * 32);
-        mma_f16(tmem, smem_desc(sa_hi + kk * 32), bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-        mma_f16(tmem, smem_desc(sa_lo + kk * 32), bd, idesc, 1u);
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          const uint64_t bd = smem_desc(sb + kk * 32);
+          mma_f16(acc, smem_desc(sa_hi + kk * 32), bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          mma_f16(acc, smem_desc(sa_lo + kk * 32), bd, idesc, 1u);
+        }
+        mma_commit(&empty_bar[st]);  // stage free once these MMAs have read it
       }
-      mma_commit(&empty_bar[st]);  // stage free once these MMAs have read it
+      mma_commit(&tfull_bar[b]);  // arrives once every MMA issued above has completed
+      if (!ok) break;
     }
-    (void)ok;
-    mma_commit(&acc_bar);  // arrives once every MMA issued above has completed
   } else if (warp >= 2) {
     // epilogue: TMEM -> registers (one row a thread) -> partials, and the
-    // scores through swizzled staging blocks to TMA stores
-    const bool got = mbar_wait(&acc_bar, 0);
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    if (!got) {
-      if (lane == 0) atomicOr(status, kStatusTimeout);
-    } else if (!atomicAdd(&abort_flag, 0)) {
-      const int e = warp - 2;            // 0..7
-      const int quarter = warp & 3;      // the accumulator lanes this warp may read
-      const int half = e >> 2;           // 128-column half of the tile
+    // scores through a swizzled staging block to TMA stores
+    const int e = warp - 2;            // 0..7
+    const int quarter = warp & 3;      // the accumulator lanes this warp may read
+    const int half = e >> 2;           // 128-column half of the tile
+    uint8_t* buf = staging + e * 4096;
+    int issued = 0, i = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+      const int b = i & 1;
+      const int m0 = (t / ntn) * kBM, n0 = (t % ntn) * kBN;
+      const bool got = mbar_wait(&tfull_bar[b], (i >> 1) & 1);
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      if (!got || atomicAdd(&abort_flag, 0)) {
+        if (lane == 0) {
+          atomicOr(status, kStatusTimeout);
+          atomicExch(&abort_flag, 1);
+        }
+        break;
+      }
       const int row = m0 + quarter * 32 + lane;
-      const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
-      uint32_t brow = 0;                 // legal-bitmap row of this beam row
+      const uint32_t lane_addr = tmem + (uint32_t)(b * kTmemCols) + ((uint32_t)(quarter * 32) << 16);
+      uint32_t brow = 0;  // legal-bitmap row of this beam row
       bool dead = false;
       if (epi.bitmap && row < M) {
         brow = epi.by_m ? (uint32_t)row : (epi.rows ? epi.rows[row] : 0u);
         dead = (brow == kDeadRow);
       }
-      uint8_t* stage = smem + e * 8192;  // two 4 KiB blocks (the ring is spent)
-      int issued = 0;
       for (int ci = 0; ci < kBN / 64; ++ci) {
         const int c0 = half * (kBN / 2) + ci * 32;
         float v[32];
@@ -251,11 +276,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t lm = dead ? 0u : (epi.bitmap ? epi.bitmap[(size_t)brow * epi.words + chunk] & vm : vm);
           float mx = -INFINITY;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mx = ((lm >> i) & 1u) ? fmaxf(mx, v[i]) : mx;
+          for (int j = 0; j < 32; ++j) mx = ((lm >> j) & 1u) ? fmaxf(mx, v[j]) : mx;
           float sm = 0.f;
           if (mx != -INFINITY) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) sm += ((lm >> i) & 1u) ? __expf(v[i] - mx) : 0.f;
+            for (int j = 0; j < 32; ++j) sm += ((lm >> j) & 1u) ? __expf(v[j] - mx) : 0.f;
           }
           epi.part[(size_t)row * (ldz >> 5) + chunk] = make_float2(mx, sm);
         }
@@ -263,17 +288,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           // (max, sum exp) over every token of the chunk (score-first normaliser)
           float mx = -INFINITY;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mx = ((vm >> i) & 1u) ? fmaxf(mx, v[i]) : mx;
+          for (int j = 0; j < 32; ++j) mx = ((vm >> j) & 1u) ? fmaxf(mx, v[j]) : mx;
           float sm = 0.f;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) sm += ((vm >> i) & 1u) ? __expf(v[i] - mx) : 0.f;
+          for (int j = 0; j < 32; ++j) sm += ((vm >> j) & 1u) ? __expf(v[j] - mx) : 0.f;
           epi.part_all[(size_t)row * (ldz >> 5) + chunk] = make_float2(mx, sm);
         }
         // stage the 32 x 32 block (row = lane; 16-byte piece j of a row at
         // j ^ (row & 7): the 128-byte swizzle of the store map), then store
-        uint8_t* buf = stage + (issued & 1) * 4096;
-        if (issued >= 2) {
-          if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        if (issued > 0) {
+          if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
           __syncwarp();
         }
 #pragma unroll
@@ -288,15 +312,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++issued;
       }
-      if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+      // this warp's part of accumulator b is read: let the MMA issuer reuse it
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&tempty_bar[b])) : "memory");
     }
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+    __syncwarp();
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   if (warp == 1) {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * kTmemCols) : "memory");
   }
 }
 
@@ -365,7 +393,7 @@ bool make_map(CUtensorMap* m, const void* base, int rows, int d, int box_rows, b
 
 }  // namespace
 
-size_t full_tc_smem_bytes() { return (size_t)kStages * kStageBytes + 1024; }
+size_t full_tc_smem_bytes() { return (size_t)kStages * kStageBytes + kEpiWarps * 4096 + 1024; }
 
 cudaError_t launch_split_h(const float* H, void* hi, void* lo, size_t n, int w_dtype, cudaStream_t st) {
   const int blocks = (int)std::min<size_t>((n + 255) / 256, 4096);
@@ -404,7 +432,9 @@ cudaError_t launch_full_tc(const void* hi, const void* lo, const void* W, float*
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  dim3 grid((V + kBN - 1) / kBN, (M + kBM - 1) / kBM);
+  // persistent: one CTA per SM (shared memory admits one), tiles strided over the CTAs
+  const int ntiles = ((V + kBN - 1) / kBN) * ((M + kBM - 1) / kBM);
+  const int grid = std::max(1, std::min(ntiles, sm_count()));
   k_full_tc<<<grid, kThreads, smem, st>>>(mh, ml, mw, mz, M, V, d, ldz, bf16 ? 1u : 0u, epi, status);
   return cudaGetLastError();
 }
