@@ -990,23 +990,28 @@ __device__ __forceinline__ uint32_t bin_of(uint32_t key, uint32_t lo, int sh) {
 // with b reaches it goes to sw.prefix, the count above to sw.cnt_gt, the
 // count in b to sw.cnt_eq, and sw.nwin is zeroed.  Returns the histogram's
 // total (the same in every thread; sw is not written when it is below
-// target).  Thread t scans bins [top - PER, top), top = 2048 - PER * t, from
+// target).  Thread t scans bins [top - PER, top), top = NB - PER * t, from
 // the top.  On return every thread may overwrite the histogram.
-template <int NT, typename SW>
+template <int NT, typename SW, int NB = kBins>
 __device__ uint32_t hist_cut(const uint32_t* hist, SW& sw, uint32_t target) {
   constexpr int NW = NT / 32;
-  constexpr int PER = kBins / NT;
-  static_assert(PER % 4 == 0, "bins a thread");
+  constexpr int PER = NB / NT;
+  static_assert(PER >= 1 && NB % NT == 0, "bins a thread");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int top = kBins - PER * tid;
+  const int top = NB - PER * tid;
   uint32_t cnt[PER];
+  if constexpr (PER % 4 == 0) {
 #pragma unroll
-  for (int i = 0; i < PER; i += 4) {
-    const uint4 v = *reinterpret_cast<const uint4*>(&hist[top - 4 - i]);
-    cnt[i] = v.w;
-    cnt[i + 1] = v.z;
-    cnt[i + 2] = v.y;
-    cnt[i + 3] = v.x;
+    for (int i = 0; i < PER; i += 4) {
+      const uint4 v = *reinterpret_cast<const uint4*>(&hist[top - 4 - i]);
+      cnt[i] = v.w;
+      cnt[i + 1] = v.z;
+      cnt[i + 2] = v.y;
+      cnt[i + 3] = v.x;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < PER; ++i) cnt[i] = hist[top - 1 - i];
   }
   uint32_t mine = 0;
 #pragma unroll
@@ -1272,6 +1277,32 @@ __device__ int cta_select_chunks(const StepLaunch& a, int q, BeamTab& bt, SW& sw
     if (pass == 1) {
       const int nl = sw.nwin;  // the same in every thread
       if (nl <= LCAP) {
+        if (nl > 2 * keep_n && nl > 64) {
+          // a long list: cut it once more by a 1,024-bin histogram over
+          // [tc, kceil] (in sw.win, spare until the placement), keep the
+          // entries at or above the cut and place those
+          constexpr int NB3 = 1024, EPT = (LCAP + NT - 1) / NT;
+          uint32_t* h3 = reinterpret_cast<uint32_t*>(sw.win);
+          const int sh3 = (hi - tc < (uint32_t)NB3) ? 0 : (32 - __clz(hi - tc) - 10);
+          for (int i = tid; i < NB3; i += NT) h3[i] = 0u;
+          unsigned long long mine[EPT];
+#pragma unroll
+          for (int u = 0; u < EPT; ++u) mine[u] = (tid + u * NT < nl) ? list[tid + u * NT] : 0ull;
+          __syncthreads();
+#pragma unroll
+          for (int u = 0; u < EPT; ++u)
+            if (mine[u]) atomicAdd(&h3[min(((uint32_t)(mine[u] >> 32) - tc) >> sh3, (uint32_t)(NB3 - 1))], 1u);
+          __syncthreads();
+          hist_cut<NT, SW, NB3>(h3, sw, (uint32_t)keep_n);  // total nl >= keep_n
+          const uint32_t t3 = tc + (sw.prefix << sh3);
+#pragma unroll
+          for (int u = 0; u < EPT; ++u)
+            warp_append(list, LCAP, sw.nwin, mine[u] && (uint32_t)(mine[u] >> 32) >= t3, (uint32_t)(mine[u] >> 32),
+                        (int)(0xFFFFFFFFu - (uint32_t)(mine[u] & 0xFFFFFFFFu)), lane);
+          __syncthreads();
+          place_winners<NT>(list, sw.nwin, keep_n, sw);
+          return keep_n;
+        }
         place_winners<NT>(list, nl, keep_n, sw);
         return keep_n;
       }
