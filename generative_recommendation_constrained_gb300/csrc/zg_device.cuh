@@ -415,8 +415,9 @@ __device__ void build_beam_table(const StepLaunch& a, int q, BeamTab& bt) {
 // Log-sum-exp of every live beam from its chunk partials (m_c, s_c): lse =
 // M + log(sum_c s_c exp(m_c - M)), M = max_c m_c, over the legal tokens
 // (filter-first), or over every token from part_all (score-first).  Eight lanes a
-// beam, eight beams a warp at once (two a lane group, their first partials
-// loaded together and kept for the second pass), width-8 shuffle reductions.
+// beam; each 8-lane group of the CTA takes up to two beams at once (their
+// first partials loaded together and kept for the second pass), so every
+// group has a beam before any has two; width-8 shuffle reductions.
 // Partials come from shared memory by item (psm) or from the global partial
 // buffer (psm == nullptr).  Also folds into bt.kceil / bt.kfloor / bt.nne the
 // keys of each beam's best and weakest non-empty chunk maximum and its
@@ -425,7 +426,9 @@ template <int NT>
 __device__ void beam_lse_sel(const StepLaunch& a, int q, BeamTab& bt, const float2* psm) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int sub = lane >> 3, sl = lane & 7;
-  for (int k0 = warp * 8; k0 < a.Wc; k0 += (NT / 32) * 8) {
+  constexpr int NG = (NT / 32) * 4;  // 8-lane groups of the CTA
+  const int g = warp * 4 + sub;
+  for (int k0 = 0; k0 < a.Wc; k0 += 2 * NG) {
     int kb[2], n[2];
     const float2* pp[2];
     const float2* pa[2];
@@ -433,7 +436,7 @@ __device__ void beam_lse_sel(const StepLaunch& a, int q, BeamTab& bt, const floa
     const bool all_v = (a.part_all != nullptr) && !psm;  // score-first: normaliser over the codebook
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const int k = k0 + 4 * h + sub;
+      const int k = k0 + h * NG + g;  // every group takes a beam before any takes a second
       const bool live = (k < a.Wc) && bt.cnt[k] > 0;
       kb[h] = k;
       n[h] = live ? bt.items[k] : 0;
