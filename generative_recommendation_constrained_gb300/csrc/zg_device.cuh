@@ -425,6 +425,56 @@ __device__ void build_beam_table(const StepLaunch& a, int q, BeamTab& bt) {
 template <int NT>
 __device__ void beam_lse_sel(const StepLaunch& a, int q, BeamTab& bt, const float2* psm) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  static_assert(NT >= 256, "eight warps at least");
+  if (a.Wc <= 8) {
+    // few beams (the first step's root beam): all 32 lanes of a warp on one
+    // beam, width-32 reductions (the same threshold in every kernel keeps
+    // the fused and stand-alone selects bit-identical)
+    const int k = warp;
+    const bool live = (k < a.Wc) && bt.cnt[k] > 0;
+    if (!live) return;
+    const int n = bt.items[k];
+    const size_t go = (size_t)q * a.pq + (size_t)k * a.nch;
+    const float2* pp = psm ? psm + bt.istart[k] : a.part + go;
+    const bool all_v = (a.part_all != nullptr) && !psm;
+    const float2* pa = all_v ? a.part_all + go : pp;
+    float m = -INFINITY, mn = INFINITY, ma = -INFINITY;
+    int ne = 0;
+    for (int c = lane; c < n; c += 32) {
+      const float2 p = pp[c];
+      m = fmaxf(m, p.x);
+      if (p.y > 0.f) {
+        mn = fminf(mn, p.x);
+        ++ne;
+      }
+      if (all_v) ma = fmaxf(ma, pa[c].x);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+      mn = fminf(mn, __shfl_xor_sync(kFull, mn, o));
+      ne += __shfl_xor_sync(kFull, ne, o);
+      ma = fmaxf(ma, __shfl_xor_sync(kFull, ma, o));
+    }
+    if (!all_v) ma = m;
+    float sum = 0.f;
+    for (int c = lane; c < n; c += 32) {
+      const float2 p = pa[c];
+      if (p.y > 0.f) sum += p.y * expf(p.x - ma);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
+    if (lane == 0) {
+      const float lse = ma + logf(sum);
+      bt.lse[k] = lse;
+      if (ne > 0) {
+        atomicMax(&bt.kceil, f2ord(bt.cum[k] + (m - lse)));
+        atomicMin(&bt.kfloor, f2ord(bt.cum[k] + (mn - lse)));
+        atomicAdd(&bt.nne, ne);
+      }
+    }
+    return;
+  }
   const int sub = lane >> 3, sl = lane & 7;
   constexpr int NG = (NT / 32) * 4;  // 8-lane groups of the CTA
   const int g = warp * 4 + sub;
