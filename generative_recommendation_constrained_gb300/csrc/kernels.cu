@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(kClusterThreads, 2) k_decode_cluster(const __g
       if (in_smem) {
         beam_lse_sel<NT>(a, q, bt, psm);
         // chunk beams and keys replace the spent partials in place
-        n = cta_select_chunks<NT>(a, q, bt, sw, psm, reinterpret_cast<const float*>(zsm),
+        n = cta_select_chunks<NT, true>(a, q, bt, sw, psm, reinterpret_cast<const float*>(zsm),
                                   reinterpret_cast<uint32_t*>(psm) + 1, reinterpret_cast<uint32_t*>(psm), 2);
         if (n < 0) n = cta_select_bins<NT>(a, q, bt, sw, zsm, kZStaged);
         write_survivors<NT>(a, q, bt, sw, n, msm);
@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(kClusterThreads, 2) k_decode_cluster(const __g
         beam_lse<NT>(a, q, bt);
         __syncthreads();
         const int ni = bt.istart[a.Wc];
-        n = (a.part && 2 * ni <= A.cap) ? cta_select_chunks<NT>(a, q, bt, sw, nullptr, nullptr, zsm, zsm + ni, 1) : -1;
+        n = (a.part && 2 * ni <= A.cap) ? cta_select_chunks<NT, false>(a, q, bt, sw, nullptr, nullptr, zsm, zsm + ni, 1) : -1;
         if (n < 0) {
           if (bt.total <= A.cap) {
             stage_keys_global<NT>(a, q, bt, zsm);
@@ -375,7 +375,7 @@ __global__ void __launch_bounds__(kSelThreads) k_select(const __grid_constant__ 
   __syncthreads();
   const int ni = bt.istart[a.Wc];
   int n = (a.part && 2 * ni <= kSelCap)
-              ? cta_select_chunks<kSelThreads>(a, q, bt, sw, nullptr, nullptr, keys, keys + ni, 1) : -1;
+              ? cta_select_chunks<kSelThreads, false>(a, q, bt, sw, nullptr, nullptr, keys, keys + ni, 1) : -1;
   if (n < 0) {
     if (staged) {
       stage_keys_global<kSelThreads>(a, q, bt, keys);

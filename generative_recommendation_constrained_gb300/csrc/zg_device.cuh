@@ -1210,8 +1210,8 @@ __device__ int cta_select_bins(const StepLaunch& a, int q, BeamTab& bt, SW& sw, 
 // ---------------------------------------------------------------------------
 // Chunk-filtered select for steps with chunk partials (from shared memory
 // `ps` by chunk item, or the global partial buffer when ps is null), with the
-// slot scores in shared memory (`zs` by flat candidate) or in the global slot
-// buffer (zs null).
+// slot scores in shared memory (kSmemZ: `zs` by flat candidate) or in the
+// global slot buffer.
 //   1. Every chunk's maximum key goes to ckb[i * st] and its beam to
 //      kb[i * st]; the maxima are cut for keep: at least keep chunk maxima,
 //      all true candidates, lie at or above the cut key tc, so the keep-th
@@ -1226,7 +1226,7 @@ __device__ int cta_select_bins(const StepLaunch& a, int q, BeamTab& bt, SW& sw, 
 // back) when the key range is unknown or the final list would not fit in the
 // histogram's space.
 // ---------------------------------------------------------------------------
-template <int NT, typename SW>
+template <int NT, bool kSmemZ, typename SW>
 __device__ int cta_select_chunks(const StepLaunch& a, int q, BeamTab& bt, SW& sw, const float2* ps, const float* zs,
                                  uint32_t* ckb, uint32_t* kb, int st) {
   constexpr int NW = NT / 32;
@@ -1307,7 +1307,7 @@ __device__ int cta_select_chunks(const StepLaunch& a, int q, BeamTab& bt, SW& sw
             const int j = (i0 + src * NW + warp - bt.istart[k]) * kChunk + lane;
             if (j < bt.cnt[k]) {
               flat[u] = bt.start[k] + j;
-              if (zs) {
+              if constexpr (kSmemZ) {
                 const float z = zs[flat[u]];
                 key[u] = (z == -INFINITY) ? 0u : f2ord(bt.cum[k] + (z - bt.lse[k]));
               } else {
