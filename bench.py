@@ -237,8 +237,8 @@ def run_reference(args, cfg):
         "impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": workload_desc(cfg), "global_batch": per_step,
-                   "sample": f"{per_step} requests of the batch per step"},
+        "config": {"workload": workload_desc(cfg), "global_batch": cfg.batch, "beam": cfg.beam, "topk": cfg.topk,
+                   "sample": f"each step decodes {per_step} requests of the batch (bounded CPU sample)"},
         "cpu_baseline": {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"{per_step} requests per step x {args.steps} steps, fp64 numpy oracle"},
         "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
