@@ -358,3 +358,21 @@ def test_score_first_single_step_closed_form():
     assert shift < 0
     assert np.array_equal(a.sids, b.sids)
     assert np.max(np.abs(b.scores - (a.scores + shift))) < 1e-12
+
+
+@pytest.mark.parametrize("order", ["filter_first", "score_first"])
+def test_path_score_matches_exhaustive_walk(order):
+    """The per-item path score (hidden vector rebuilt from scratch for every
+    prefix) equals the brute-force walk's product of per-step softmax
+    probabilities for every item of a tiny catalogue, in both orders."""
+    sids = tiny_catalogue(3, 6, 40, 12)
+    m = _model(3, 6, 5, "bf16", 12)
+    u = synth.make_requests(1, 5, 12)
+    trie = oracle.Trie(sids, 3, 6)
+    bs, bsc = oracle.brute_force(trie, m, u[0], order=order)
+    for sid, sc in zip(bs, bsc):
+        assert abs(oracle.path_score(trie, m, u[0], sid, order) - sc) < 1e-12
+    # an item outside the catalogue has no path
+    missing = next(t for t in ((a, b, c) for a in range(6) for b in range(6) for c in range(6))
+                   if not trie.contains(t))
+    assert oracle.path_score(trie, m, u[0], missing, order) == -math.inf
