@@ -245,6 +245,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
       const int b = i & 1;
       const int m0 = (t / ntn) * kBM, n0 = (t % ntn) * kBN;
+      const int row = m0 + quarter * 32 + lane;
+      // this row's legal-bitmap words for its four chunks, fetched while the
+      // tile's MMAs run (they do not depend on the accumulator)
+      uint32_t lmw[kBN / 64];
+      bool dead = false;
+#pragma unroll
+      for (int ci = 0; ci < kBN / 64; ++ci) lmw[ci] = 0xFFFFFFFFu;
+      if (epi.bitmap && row < M) {
+        const uint32_t brow = epi.by_m ? (uint32_t)row : (epi.rows ? epi.rows[row] : 0u);
+        dead = (brow == kDeadRow);
+        if (!dead) {
+#pragma unroll
+          for (int ci = 0; ci < kBN / 64; ++ci) {
+            const int c0 = half * (kBN / 2) + ci * 32;
+            if (n0 + c0 < V) lmw[ci] = epi.bitmap[(size_t)brow * epi.words + ((n0 + c0) >> 5)];
+          }
+        }
+      }
       const bool got = mbar_wait(&tfull_bar[b], (i >> 1) & 1);
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       if (!got || atomicAdd(&abort_flag, 0)) {
@@ -254,14 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         break;
       }
-      const int row = m0 + quarter * 32 + lane;
       const uint32_t lane_addr = tmem + (uint32_t)(b * kTmemCols) + ((uint32_t)(quarter * 32) << 16);
-      uint32_t brow = 0;  // legal-bitmap row of this beam row
-      bool dead = false;
-      if (epi.bitmap && row < M) {
-        brow = epi.by_m ? (uint32_t)row : (epi.rows ? epi.rows[row] : 0u);
-        dead = (brow == kDeadRow);
-      }
+#pragma unroll
       for (int ci = 0; ci < kBN / 64; ++ci) {
         const int c0 = half * (kBN / 2) + ci * 32;
         float v[32];
@@ -273,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (row < M && epi.part) {
           // legal-only (max, sum exp) of this 32-token chunk (the fast
           // exponential: ~1e-6 relative, far inside the score tolerance)
-          const uint32_t lm = dead ? 0u : (epi.bitmap ? epi.bitmap[(size_t)brow * epi.words + chunk] & vm : vm);
+          const uint32_t lm = dead ? 0u : (lmw[ci] & vm);
           float mx = -INFINITY;
 #pragma unroll
           for (int j = 0; j < 32; ++j) mx = ((lm >> j) & 1u) ? fmaxf(mx, v[j]) : mx;
