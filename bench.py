@@ -24,6 +24,7 @@ for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -612,6 +613,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["zerogr", "reference"], default="zerogr")
     ap.add_argument("--workload", default="mid_sparse", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--batch", type=int, default=0, help="requests per batch (0: the workload's own)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-requests", type=int, default=2)
@@ -623,6 +625,8 @@ def main(argv=None):
                     help="rebuild throughput of the workload's index while a decode is served (one JSON line)")
     args = ap.parse_args(argv)
     cfg = synth.CONFIGS[args.workload]
+    if args.batch:
+        cfg = dataclasses.replace(cfg, batch=args.batch)
     if args.plan and len(args.plan) != cfg.L:
         ap.error(f"--plan needs {cfg.L} letters (s or f)")
     if args.impl == "reference":

@@ -176,3 +176,39 @@ def test_mistake_score_first_without_max_shift_sign(monkeypatch):
         return z[T] + (z.max() + np.log(np.exp(z - z.max()).sum()))
     monkeypatch.setattr(Z, "score_first_log_probs", wrong)
     assert not _score_first_pin_holds()
+
+
+def _trie_pin_holds():
+    from test_oracle_pins import trie_children_match_recount
+    return trie_children_match_recount()
+
+
+def test_trie_pin_holds_on_the_real_oracle():
+    assert _trie_pin_holds()
+
+
+@pytest.mark.parametrize("delta", [1, -1])
+def test_mistake_trie_range_span_off_by_one_power(monkeypatch, delta):
+    """A key range under a prefix whose span is V**(L-s+delta) instead of V**(L-s)."""
+    def wrong_range(self, prefix):
+        s = len(prefix)
+        p = 0
+        for t in prefix:
+            p = p * self.V + int(t)
+        span = self.V ** max(self.L - s + delta, 0)
+        lo = int(np.searchsorted(self.keys, p * span, side="left"))
+        hi = int(np.searchsorted(self.keys, (p + 1) * span, side="left"))
+        return lo, hi
+    monkeypatch.setattr(Z.Trie, "_range", wrong_range)
+    assert not _trie_pin_holds()
+
+
+def test_mistake_trie_children_wrong_digit(monkeypatch):
+    """children() reading the token one step too deep (the digit after the next one)."""
+    def wrong_children(self, prefix):
+        prefix = tuple(int(t) for t in prefix)
+        lo, hi = self._range(prefix)
+        div = self.V ** max(self.L - len(prefix) - 2, 0)
+        return np.unique((self.keys[lo:hi] // div) % self.V)
+    monkeypatch.setattr(Z.Trie, "children", wrong_children)
+    assert not _trie_pin_holds()

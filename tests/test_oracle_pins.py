@@ -81,6 +81,47 @@ def test_index_brute_force_recount(seed, L, V, n, fmt):
                 assert pre[s][e] == p + (int(t),)
 
 
+TRIE_CASES = [(0, 3, 8, 60), (1, 2, 40, 300), (2, 4, 5, 200), (3, 1, 33, 20), (4, 3, 64, 500)]
+
+
+def trie_children_match_recount(cases=TRIE_CASES) -> bool:
+    """Trie.children at every prefix of every length (and at absent prefixes)
+    equals the distinct next tokens recounted with Python sets over the raw
+    SID rows; Trie.contains is true exactly for catalogue items."""
+    for seed, L, V, n in cases:
+        sids = tiny_catalogue(L, V, n, seed)
+        trie = oracle.Trie(sids, L, V)
+        items = {tuple(int(x) for x in r) for r in sids}
+        for s in range(L):
+            nxt = {}
+            for it in items:
+                nxt.setdefault(it[:s], set()).add(it[s])
+            for p, toks in nxt.items():
+                if list(trie.children(p)) != sorted(toks):
+                    return False
+            rng = np.random.default_rng(seed + 10 * s)
+            for _ in range(20):          # prefixes that no item starts with
+                p = tuple(int(x) for x in rng.integers(0, V, size=s))
+                if p not in nxt and trie.children(p).size != 0:
+                    return False
+        for it in list(items)[:50]:
+            if not trie.contains(it):
+                return False
+        rng = np.random.default_rng(seed)
+        for _ in range(50):
+            it = tuple(int(x) for x in rng.integers(0, V, size=L))
+            if trie.contains(it) != (it in items):
+                return False
+    return True
+
+
+def test_trie_children_brute_force_recount():
+    """[Problem]: a token is legal after a prefix iff prefix + token starts a
+    catalogue SID - checked at every prefix of every length, not only at the
+    worked example's."""
+    assert trie_children_match_recount()
+
+
 def test_format_rule_closed_form():
     """Dense iff 4*rows*ceil(V/32) < 2*nnz, evaluated by hand."""
     assert oracle.choose_format(1, 256, 256) == oracle.DENSE      # 32 < 512
