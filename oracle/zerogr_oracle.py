@@ -65,6 +65,19 @@ def sid_keys(sids: np.ndarray, V: int) -> np.ndarray:
     return k
 
 
+def distinct_sorted(x: np.ndarray) -> np.ndarray:
+    """The distinct values of x in ascending order: a library sort, then every
+    value equal to its predecessor dropped (the definition of a set's sorted
+    listing; np.unique computes the same but is far slower on 10^8 keys)."""
+    x = np.sort(np.asarray(x).ravel())
+    if x.size == 0:
+        return x
+    keep = np.empty(x.size, dtype=bool)
+    keep[0] = True
+    np.not_equal(x[1:], x[:-1], out=keep[1:])
+    return x[keep]
+
+
 def keys_to_sids(keys: np.ndarray, L: int, V: int) -> np.ndarray:
     out = np.empty((keys.size, L), dtype=np.int64)
     k = keys.copy()
@@ -89,10 +102,22 @@ class Trie:
             raise ValueError("token out of range")
         self.L, self.V = L, V
         raw = sid_keys(sids, V)
-        self.keys = np.unique(raw)
+        self.keys = distinct_sorted(raw)
         self.n_input = int(raw.size)
         self.n_unique = int(self.keys.size)
         self._cache = {}
+
+    @classmethod
+    def from_keys(cls, keys: np.ndarray, L: int, V: int) -> "Trie":
+        """A trie over keys that are already the distinct ascending base-V SID
+        keys of a catalogue (another Trie's ``keys``, e.g. memory-mapped in a
+        worker process), without sorting again."""
+        t = cls.__new__(cls)
+        t.L, t.V = L, V
+        t.keys = keys
+        t.n_input = t.n_unique = int(keys.size)
+        t._cache = {}
+        return t
 
     def _range(self, prefix) -> tuple[int, int]:
         s = len(prefix)
@@ -112,7 +137,7 @@ class Trie:
             lo, hi = self._range(prefix)
             s = len(prefix)
             div = self.V ** (self.L - s - 1)
-            got = np.unique((self.keys[lo:hi] // div) % self.V)
+            got = distinct_sorted((self.keys[lo:hi] // div) % self.V)
             self._cache[prefix] = got
         return got
 
@@ -168,13 +193,13 @@ def serialize_index(sids: np.ndarray, L: int, V: int, force_format: int = -1) ->
     entries of step s in order, entry e extends to the prefix that is row e of
     step s+1, so no successor array is stored; rowptr[r] is the position of
     row r's first entry."""
-    keys = np.unique(sid_keys(sids, V))
+    keys = distinct_sorted(sid_keys(sids, V))
     words = (V + 31) // 32
     tables = []
     for s in range(1, L + 1):
-        ent = np.unique(keys // (V ** (L - s)))       # distinct s-prefixes, sorted
+        ent = distinct_sorted(keys // (V ** (L - s)))  # distinct s-prefixes, sorted
         parent = ent // V                              # their (s-1)-prefixes
-        rows_val = np.unique(parent)
+        rows_val = distinct_sorted(parent)
         rowidx = np.searchsorted(rows_val, parent)
         F = np.bincount(rowidx, minlength=rows_val.size).astype(np.int64)
         rowptr = np.zeros(rows_val.size + 1, dtype=np.int64)
@@ -363,12 +388,16 @@ def decode(trie: Trie | None, model, u: np.ndarray, beam: int, K: int,
     return DecodeResult(out_sids, out_scores, gaps, n_cand, next_score)
 
 
-def path_score(trie: Trie | None, model, u_q: np.ndarray, sid, order: str = "filter_first") -> float:
+def path_score(trie: Trie | None, model, u_q: np.ndarray, sid, order: str = "filter_first",
+               Wd=None) -> float:
     """Filter-first score of one item along its own path: the sum over steps
     of its token's log-probability among the legal tokens after its prefix
     (score-first: among all V tokens).  The hidden vector is recomputed from
-    scratch as u + sum_{j<s} C_j[t_j]."""
+    scratch as u + sum_{j<s} C_j[t_j].  Wd: the stored weights already widened
+    to float64 (model.W_as_f64 of every step), to spare repeated widening."""
     L, V = model.L, model.V
+    if Wd is None:
+        Wd = _weights_f64(model)
     total = 0.0
     for s in range(1, L + 1):
         prefix = tuple(int(t) for t in sid[:s - 1])
@@ -381,10 +410,10 @@ def path_score(trie: Trie | None, model, u_q: np.ndarray, sid, order: str = "fil
         if pos >= T.size or T[pos] != t:
             return -math.inf
         if order == "score_first":
-            z = model.W_as_f64(s - 1) @ h
+            z = Wd[s - 1] @ h
             total += float(z[t] - (z.max() + math.log(float(np.exp(z - z.max()).sum()))))
         else:
-            z = model.W_as_f64(s - 1)[T] @ h
+            z = Wd[s - 1][T] @ h
             total += float(filtered_log_softmax(z)[pos])
     return total
 

@@ -39,6 +39,7 @@ def check_topk(gpu_sids, gpu_scores, ref, trie, model, u, tol, window, requests=
     B, K, L = gpu_sids.shape
     req = range(B) if requests is None else list(requests)
     ambiguous = 0
+    Wd = [model.W_as_f64(s) for s in range(model.L)]
     for q in req:
         valid = gpu_sids[q, :, 0] >= 0
         nv = int(valid.sum())
@@ -55,7 +56,7 @@ def check_topk(gpu_sids, gpu_scores, ref, trie, model, u, tol, window, requests=
             seen.add(sid)
             if trie is not None:
                 assert trie.contains(sid), f"request {q}: SID {sid} not in catalogue"
-            exact = _path(trie, model, u[q], sid, order)
+            exact = _path(trie, model, u[q], sid, order, Wd)
             assert abs(exact - sc[i]) <= tol, \
                 f"request {q} rank {i}: score {sc[i]} vs exact {exact}"
         if np.any(ref.gaps[q, :L - 1] <= window):
@@ -75,9 +76,9 @@ def check_topk(gpu_sids, gpu_scores, ref, trie, model, u, tol, window, requests=
     return ambiguous
 
 
-def _path(trie, model, u_q, sid, order="filter_first"):
+def _path(trie, model, u_q, sid, order="filter_first", Wd=None):
     from oracle import path_score
-    return path_score(trie, model, u_q, sid, order)
+    return path_score(trie, model, u_q, sid, order, Wd)
 
 
 def isclose_inf(a, b, tol):

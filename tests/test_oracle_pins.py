@@ -11,6 +11,7 @@ import pytest
 import scipy.special
 
 import oracle
+import oracle.zerogr_oracle as Z
 import synth
 from _helpers import golden_catalogue, tiny_catalogue
 from conftest import read_golden
@@ -113,6 +114,22 @@ def trie_children_match_recount(cases=TRIE_CASES) -> bool:
             if trie.contains(it) != (it in items):
                 return False
     return True
+
+
+def test_distinct_sorted_is_the_sorted_set():
+    rng = np.random.default_rng(5)
+    for n, hi in [(0, 3), (1, 3), (50, 4), (1000, 50), (5000, 1 << 40)]:
+        x = rng.integers(0, hi, size=n)
+        assert list(Z.distinct_sorted(x)) == sorted(set(int(v) for v in x))
+
+
+def test_trie_from_keys_equals_trie():
+    sids = tiny_catalogue(3, 16, 300, 7)
+    a = oracle.Trie(sids, 3, 16)
+    b = Z.Trie.from_keys(a.keys, 3, 16)
+    for p in [(), (int(sids[0, 0]),), tuple(int(x) for x in sids[1, :2])]:
+        assert list(a.children(p)) == list(b.children(p))
+    assert b.contains(sids[3]) and b.n_unique == a.n_unique
 
 
 def test_trie_children_brute_force_recount():
