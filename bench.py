@@ -5,8 +5,10 @@ One step = one full L-step constrained beam decode of one request batch,
 all kernels of the CUDA library (index lookup, gather-add, selective or full
 projection, masked log-softmax, cumulative add, top-K select, emit), replayed
 from a CUDA graph with inputs resident in HBM and L2 flushed (a 256 MiB
-write) before every timed step.  Default workload: the mid-sparse catalogue
-(L=3, V=2048, 1M items, d=256, fp32 weights, batch 32, beam 32, top-K 32).
+write) before every timed step.  Default workload: the large catalogue
+(L=4, V=8192, 100M items with Zipf(1.05) first tokens and geometric fan-out
+decay, d=512, bf16 weights, batch 64, beam 256, top-K 256), the largest
+configuration; its batch sweep (1, 8, 32, 64) is reported beside the line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl zerogr|reference]
 
@@ -19,7 +21,7 @@ from __future__ import annotations
 
 import os
 
-# the CPU oracle leg is timed on one host thread; keep numpy's BLAS single-threaded
+# the CPU oracle is timed per process (one a core); keep numpy's BLAS single-threaded
 for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
@@ -195,43 +197,115 @@ def load_peaks() -> dict:
 
 # ---------------------------------------------------------------- CPU oracle leg
 
-def oracle_rate(cfg, sids, model, u, budget_s: float):
-    """Requests/s of the CPU oracle (as it stands, one host thread) on a
-    bounded sample: requests decoded one at a time until budget_s elapses."""
+_ORACLE_CTX = {}
+
+
+def host_cpu_model() -> str:
+    """The host CPU's model name (/proc/cpuinfo, else lscpu, else platform)."""
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def _oracle_requests(wid: int, n_workers: int, budget_s: float):
+    """Decode requests wid, wid + n_workers, ... of the batch one at a time
+    until budget_s elapses; returns (requests decoded, seconds)."""
     import oracle
-    t0 = time.perf_counter()
-    trie = oracle.Trie(sids, cfg.L, cfg.V)
-    t_trie = time.perf_counter() - t0
+    c = _ORACLE_CTX
+    B = c["u"].shape[0]
     done = 0
     t0 = time.perf_counter()
     while True:
-        oracle.decode(trie, model, u[done % u.shape[0]: done % u.shape[0] + 1], cfg.beam, cfg.topk)
+        q = (wid + done * n_workers) % B
+        oracle.decode(c["trie"], c["model"], c["u"][q:q + 1], c["beam"], c["topk"])
         done += 1
         if time.perf_counter() - t0 >= budget_s:
             break
-    dt = time.perf_counter() - t0
-    return done / dt, done, dt, t_trie
+    return done, time.perf_counter() - t0
+
+
+def _oracle_batch(sel):
+    """Decode the requests `sel` one at a time; returns seconds."""
+    import oracle
+    c = _ORACLE_CTX
+    t0 = time.perf_counter()
+    for q in sel:
+        oracle.decode(c["trie"], c["model"], c["u"][q:q + 1], c["beam"], c["topk"])
+    return time.perf_counter() - t0
+
+
+def oracle_setup(cfg, sids, model, u):
+    """Build the oracle's trie once (timed) and keep what the workers read.
+    Worker pools are forked from this process, so this and the pools must run
+    before the first CUDA call of the process."""
+    import oracle
+    t0 = time.perf_counter()
+    trie = oracle.Trie(sids, cfg.L, cfg.V)
+    _ORACLE_CTX.update(trie=trie, model=model, u=u, beam=cfg.beam, topk=cfg.topk)
+    return time.perf_counter() - t0
+
+
+def oracle_rates(cfg, sids, model, u, budget_s: float) -> dict:
+    """Requests/s of the CPU oracle as it stands (fp64 numpy, requests decoded
+    one at a time): on one host thread, then on every host core (one forked
+    worker process per core, requests dealt round-robin, each worker decoding
+    for budget_s).  Must run before the first CUDA call of the process."""
+    import multiprocessing as mp
+    t_trie = oracle_setup(cfg, sids, model, u)
+    _oracle_requests(0, 1, 0.0)          # warms the trie's lookups of the first step
+    done1, dt1 = _oracle_requests(0, 1, budget_s)
+    cores = os.cpu_count() or 1
+    with mp.get_context("fork").Pool(cores) as pool:
+        res = pool.starmap(_oracle_requests, [(w, cores, budget_s) for w in range(cores)])
+    rate_all = sum(d / t for d, t in res)
+    done_all = sum(d for d, _ in res)
+    return {"value": rate_all, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "cpu_model": host_cpu_model(), "one_thread": done1 / dt1,
+            "sample": f"requests of the workload decoded one at a time for {budget_s:.0f} s: {done1} on 1 thread, "
+                      f"{done_all} on {cores} worker processes (one a core); trie build {t_trie:.1f} s excluded; "
+                      f"fp64 numpy oracle"}
 
 
 def run_reference(args, cfg):
+    """The oracle (this method exists only as web pages of text; there is no
+    installable reference implementation) timed as it stands on every host
+    core: each step decodes one request per core (the requests of the batch
+    in turn), in a pool of forked worker processes, one a core."""
+    import multiprocessing as mp
     rank, world, _ = dist_env()
     if rank != 0:
         return
     sids = synth.make_catalogue(cfg, 0)
     model = synth.make_model(cfg.L, cfg.V, cfg.d, cfg.w_dtype, 0)
     u = synth.make_requests(cfg.batch, cfg.d, request_seed(0))
-    import oracle
-    trie = oracle.Trie(sids, cfg.L, cfg.V)
-    per_step = max(1, min(cfg.batch, args.ref_requests))
-    for i in range(args.warmup):
-        oracle.decode(trie, model, u[:1], cfg.beam, cfg.topk)
+    t_trie = oracle_setup(cfg, sids, model, u)
+    cores = os.cpu_count() or 1
+    per_step = max(1, min(cfg.batch, args.ref_requests or cores))
     times = []
-    for i in range(args.steps):
-        lo = (i * per_step) % cfg.batch
-        sel = np.arange(lo, lo + per_step) % cfg.batch
-        t0 = time.perf_counter()
-        oracle.decode(trie, model, u[sel], cfg.beam, cfg.topk)
-        times.append(time.perf_counter() - t0)
+    with mp.get_context("fork").Pool(cores) as pool:
+        def step(i):
+            lo = (i * per_step) % cfg.batch
+            sel = (np.arange(lo, lo + per_step) % cfg.batch).tolist()
+            chunks = [sel[w::cores] for w in range(cores) if sel[w::cores]]
+            t0 = time.perf_counter()
+            pool.map(_oracle_batch, chunks)
+            return time.perf_counter() - t0
+        for i in range(args.warmup):
+            step(i)
+        for i in range(args.steps):
+            times.append(step(i))
     ms = 1000.0 * sum(times) / len(times)
     val = per_step / (ms / 1000.0)
     line = {
@@ -240,8 +314,9 @@ def run_reference(args, cfg):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": workload_desc(cfg), "global_batch": cfg.batch, "beam": cfg.beam, "topk": cfg.topk,
                    "sample": f"each step decodes {per_step} requests of the batch (bounded CPU sample)"},
-        "cpu_baseline": {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"{per_step} requests per step x {args.steps} steps, fp64 numpy oracle"},
+        "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle", "cpu_model": host_cpu_model(),
+                         "sample": f"{per_step} requests per step x {args.steps} steps on {cores} worker processes, "
+                                   f"fp64 numpy oracle; trie build {t_trie:.1f} s excluded"},
         "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -252,6 +327,14 @@ def run_reference(args, cfg):
 def run_gpu(args, cfg):
     import torch
     rank, world, local = dist_env()
+    sids = synth.make_catalogue(cfg, 0)
+    model = synth.make_model(cfg.L, cfg.V, cfg.d, cfg.w_dtype, 0)
+    u = synth.make_requests(cfg.batch, cfg.d, request_seed(rank))
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        # before any CUDA call: the oracle's worker pool is forked from this process
+        cpu = oracle_rates(cfg, sids, model, u, args.cpu_seconds)
+        _ORACLE_CTX.clear()
     torch.cuda.set_device(local)
     if world > 1:
         import torch.distributed as dist
@@ -261,9 +344,6 @@ def run_gpu(args, cfg):
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream().cuda_stream
 
-    sids = synth.make_catalogue(cfg, 0)
-    model = synth.make_model(cfg.L, cfg.V, cfg.d, cfg.w_dtype, 0)
-    u = synth.make_requests(cfg.batch, cfg.d, request_seed(rank))
     warm_u = synth.make_requests(cfg.batch, cfg.d, 99)
     B, beam, K = cfg.batch, cfg.beam, cfg.topk
 
@@ -280,15 +360,16 @@ def run_gpu(args, cfg):
     dec = Decoder(idx, plan, dm, B, beam, K, dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
-    def capture(d):
-        d(u_dev)
+    def capture(d, x=None):
+        x = u_dev if x is None else x
+        d(x)
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         side = torch.cuda.Stream(device=dev)
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(side):
             with torch.cuda.graph(g, stream=side):
-                d(u_dev)
+                d(x)
         torch.cuda.current_stream().wait_stream(side)
         torch.cuda.synchronize()
         return g
@@ -435,15 +516,12 @@ def run_gpu(args, cfg):
     e2e_ms = e2e_s * 1000.0 / e2e_steps
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
 
+    sweep = None
+    if cfg.name == "large" and not args.no_sweep:
+        sweep = batch_sweep(zg, idx, dm, cfg, u, warm_u, flush, capture, timed, Decoder, dev, stream, world)
+
     launches_per_step = sum(2 if v == 0 else (2 if s == 0 else 3) for s, v in enumerate(variants[:s0 - 1]))
     launches_per_step += 1 if s0 <= L else 0
-
-    cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
-        rate, done, dt, t_trie = oracle_rate(cfg, sids, model, u, args.cpu_seconds)
-        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{done} requests of the workload decoded one at a time in {dt:.1f} s "
-                         f"(trie build {t_trie:.1f} s excluded), fp64 numpy, 1 thread"}
 
     if rank == 0:
         line = {
@@ -458,7 +536,8 @@ def run_gpu(args, cfg):
                        "tune_fused_ms": [round(float(x), 4) for x in fused_ms],
                        "l2": "flushed by a 256 MiB write before every timed step",
                        "parallelism": f"replicas x{world}: requests sharded, index replicated, no collective",
-                       "index_bytes": info["bytes"], "dense_trie_bytes": info["dense_trie_bytes"]},
+                       "index_bytes": info["bytes"], "dense_trie_bytes": info["dense_trie_bytes"],
+                       "index_gb": info["bytes"] / 1e9, "dense_trie_gb": info["dense_trie_bytes"] / 1e9},
             "p10_ms": float(np.percentile(times, 10)), "p50_ms": float(np.percentile(times, 50)),
             "p90_ms": float(np.percentile(times, 90)),
             "e2e": {"value": B * world / (e2e_ms / 1000.0), "unit": UNIT,
@@ -475,12 +554,43 @@ def run_gpu(args, cfg):
             "score_first": {"ms_per_step": sms, "value": B * world / (sms / 1000.0), "unit": UNIT,
                             "filter_first_speedup": sms / ms_max, "topk_overlap": overlap},
             "kernels": [{"kernel": n, "steps": st, "ms": round(t, 5)} for t, st, n, _, _, _ in kern],
+            "batch_sweep": sweep,
             "work": work,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------- batch sweep
+
+def batch_sweep(zg, idx, dm, cfg, u, warm_u, flush, capture, timed, Decoder, dev, stream, world,
+                batches=(1, 8, 32, 64), steps: int = 30):
+    """Constrained and unconstrained decode latency at each batch size of the
+    large catalogue's sweep: requests 0..B-1 of the workload, the plan tuned
+    at that batch, graph replays with L2 flushed before each (CUDA events)."""
+    import torch
+    out = []
+    for B in batches:
+        if B > u.shape[0]:
+            continue
+        ub = torch.from_numpy(np.ascontiguousarray(u[:B])).to(dev)
+        plan = zg.zg_tune(idx, dm.struct, torch.from_numpy(np.ascontiguousarray(warm_u[:B])).to(dev), B,
+                          cfg.beam, cfg.topk, 10, stream)
+        variants, _, cluster_ctas, _ = zg.zg_plan_describe(plan)
+        dec = Decoder(idx, plan, dm, B, cfg.beam, cfg.topk, dev)
+        t = timed(capture(dec, ub), steps, 3)
+        udec = Decoder(None, None, dm, B, cfg.beam, cfg.topk, dev)
+        ut = timed(capture(udec, ub), steps, 3)
+        ms = max_over_ranks(statistics.fmean(t), world, dev)
+        ums = max_over_ranks(statistics.fmean(ut), world, dev)
+        out.append({"batch": B, "ms_per_batch": ms, "requests_per_s": B * world / (ms / 1000.0),
+                    "p10_ms": float(np.percentile(t, 10)), "p90_ms": float(np.percentile(t, 90)),
+                    "unconstrained_ms": ums, "constrained_speedup": ums / ms,
+                    "plan": "".join("f" if v else "s" for v in variants), "cluster_ctas": int(cluster_ctas)})
+        del dec, udec
+    return out
 
 
 # ---------------------------------------------------------------- scoring-variant contrast
@@ -612,11 +722,12 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["zerogr", "reference"], default="zerogr")
-    ap.add_argument("--workload", default="mid_sparse", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--workload", default="large", choices=sorted(synth.CONFIGS))
     ap.add_argument("--batch", type=int, default=0, help="requests per batch (0: the workload's own)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--ref-requests", type=int, default=2)
+    ap.add_argument("--no-sweep", action="store_true", help="skip the large catalogue's batch sweep")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-requests", type=int, default=0, help="requests a reference-arm step (0: one per core)")
     ap.add_argument("--quick", action="store_true",
                     help="tune, capture and replay only (a short command for profilers)")
     ap.add_argument("--plan", default="", help="fixed per-step variants instead of tuning, e.g. sss or fss")

@@ -106,6 +106,10 @@ def _load():
     lib.zg_last_error.restype = C.c_char_p
     lib.zg_version.argtypes = []
     lib.zg_version.restype = C.c_char_p
+    lib.zg_static_scratch_bytes.argtypes = []
+    lib.zg_static_scratch_bytes.restype = C.c_size_t
+    lib.zg_debug_set_wait_limit.argtypes = [C.c_uint32]
+    lib.zg_debug_set_wait_limit.restype = None
     return lib
 
 
@@ -271,7 +275,7 @@ def zg_decode_host(idx: Index | None, plan: Plan | None, model: zg_model, u_host
                               _ptr(out_scores_host), _ptr(workspace), ws_bytes, stream or None))
 
 
-ZG_STATIC_SCRATCH_BYTES = 16 << 20
+ZG_STATIC_SCRATCH_BYTES = int(lib.zg_static_scratch_bytes())   # as compiled into the library
 
 
 def zg_decode_static(idx: Index | None, plan: Plan | None, model: zg_model, u, B: int, beam: int, K: int,
@@ -279,6 +283,11 @@ def zg_decode_static(idx: Index | None, plan: Plan | None, model: zg_model, u, B
     """zg_decode without a workspace: scratch from the library's static device array."""
     _check(lib.zg_decode_static(idx, plan, C.byref(model), _ptr(u), B, beam, K, _ptr(out_sids),
                                 _ptr(out_scores), stream or None))
+
+
+def zg_debug_set_wait_limit(polls: int = 0):
+    """Polls before a tensor-core pipeline wait gives up (0: the default)."""
+    lib.zg_debug_set_wait_limit(int(polls))
 
 
 def zg_check_device_status(stream: int = 0):

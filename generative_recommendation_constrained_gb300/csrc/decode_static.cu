@@ -24,6 +24,7 @@ static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBy
 
 std::mutex g_static_mu;
 void* g_static_ptr[64] = {};
+unsigned long long g_static_ctx[64] = {};  // context the cached address belongs to
 
 }  // namespace
 
@@ -43,14 +44,20 @@ extern "C" zg_status zg_decode_static(const zg_index* idx, const zg_plan* plan, 
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return zg::cuda_fail(e, "zg_decode_static: cudaGetDevice");
   if (dev < 0 || dev >= 64) return zg::fail(ZG_ERR_UNSUPPORTED, "zg_decode_static: device ordinal >= 64");
+  unsigned long long ctx = 0;
+  e = zg::current_context_id(&ctx);
+  if (e != cudaSuccess) return zg::cuda_fail(e, "zg_decode_static: current context");
   void* scratch = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_static_mu);
-    if (!g_static_ptr[dev]) {
+    // looked up once per device and context: a context created after
+    // cudaDeviceReset holds a new copy of the array at a new address
+    if (!g_static_ptr[dev] || g_static_ctx[dev] != ctx) {
       void* p = nullptr;
       e = cudaGetSymbolAddress(&p, g_static_scratch);
       if (e != cudaSuccess) return zg::cuda_fail(e, "zg_decode_static: cudaGetSymbolAddress of the static scratch");
       g_static_ptr[dev] = p;
+      g_static_ctx[dev] = ctx;
     }
     scratch = g_static_ptr[dev];
   }
@@ -58,3 +65,5 @@ extern "C" zg_status zg_decode_static(const zg_index* idx, const zg_plan* plan, 
   // needs no clearing between calls.
   return zg_decode(idx, plan, model, u, B, beam, K, out_sids, out_scores, scratch, kStaticScratchBytes, stream);
 }
+
+extern "C" size_t zg_static_scratch_bytes(void) { return kStaticScratchBytes; }

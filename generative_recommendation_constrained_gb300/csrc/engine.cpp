@@ -167,16 +167,20 @@ zg_status apply_plan(Dims& m, const zg_index* idx, const zg_plan* plan) {
 
 std::mutex g_status_mu;
 uint32_t* g_status_ptr[64] = {};
+unsigned long long g_status_ctx[64] = {};
 
 zg_status get_status_ptr(uint32_t** p) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= 64) return fail(ZG_ERR_UNSUPPORTED, "device ordinal >= 64");
+  unsigned long long ctx = 0;
+  if ((e = current_context_id(&ctx)) != cudaSuccess) return cuda_fail(e, "current context id");
   std::lock_guard<std::mutex> lk(g_status_mu);
-  if (!g_status_ptr[dev]) {
+  if (!g_status_ptr[dev] || g_status_ctx[dev] != ctx) {  // first use, or a new context (device reset)
     e = status_word(&g_status_ptr[dev]);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status word)");
+    g_status_ctx[dev] = ctx;
   }
   *p = g_status_ptr[dev];
   return ZG_OK;
@@ -335,10 +339,13 @@ zg_status run_step(const Run& r, int s, int variant, cudaStream_t st, const Step
       epi.bitmap = a.tab.bitmap;
       epi.words = (int)a.tab.words;
       epi.rows = (s >= 2) ? a.row_in : nullptr;  // beam b = q*beam + k at s >= 2; the root's row 0 at s = 1
+      epi.nrows = a.tab.rows;
+      epi.status = a.status;
       if (a.mask_by_beam) {
         e = launch_legal_mask(a, st);
         if (e != cudaSuccess) return cuda_fail(e, "legal-mask launch");
         epi.by_m = 1;
+        epi.nrows = (uint32_t)M;
       }
     }
     if (tm) cudaEventRecord(tm->ev[1], st);
@@ -458,6 +465,36 @@ zg_status decode_steps(const Run& r, const zg_plan* plan, cudaStream_t st, cudaE
 }
 
 }  // namespace
+
+cudaError_t current_context_id(unsigned long long* id) {
+  using GetCurrent = int (*)(void**);                      // cuCtxGetCurrent(CUcontext*)
+  using GetId = int (*)(void*, unsigned long long*);       // cuCtxGetId(CUcontext, unsigned long long*)
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(p);
+  });
+  if (!get_current || !get_id) return cudaErrorNotSupported;
+  // make the runtime's primary context of the current device current on this
+  // thread (cudaSetDevice initialises it; nothing is allocated)
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaSetDevice(dev);
+  if (e != cudaSuccess) return e;
+  void* ctx = nullptr;
+  if (get_current(&ctx) != 0 || !ctx) return cudaErrorDeviceUninitialized;
+  if (get_id(ctx, id) != 0) return cudaErrorDeviceUninitialized;
+  return cudaSuccess;
+}
 
 zg_status fail(zg_status code, const std::string& msg) {
   g_err = msg;
@@ -796,6 +833,8 @@ zg_status zg_decode_trace(const zg_index* idx, const zg_plan* plan, const zg_mod
   cleanup();
   return st;
 }
+
+void zg_debug_set_wait_limit(uint32_t polls) { set_wait_limit(polls); }
 
 zg_status zg_check_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));

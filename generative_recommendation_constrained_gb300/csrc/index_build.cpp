@@ -658,6 +658,57 @@ zg_status zg_index_save(const zg_index* idx, const char* path) {
   return ZG_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// Structural check of a loaded image before anything reads it on the device:
+// the invariants of the step-sliced index ("Why slice the index by decoding
+// step": one row per (s-1)-prefix, a row's legal tokens ascending, entry e of
+// step s is row e of step s+1).  Any table that passes keeps every kernel
+// read in bounds: rowptr is non-decreasing from 0 to nnz, every token is
+// below V, and every next-step row (an entry position) is below the next
+// step's row count.
+bool tables_valid(const zg_index& idx, const std::vector<uint8_t>& img) {
+  const int L = idx.L;
+  const uint32_t V = (uint32_t)idx.V;
+  const uint32_t words = (V + 31) / 32;
+  for (int s = 1; s <= L; ++s) {
+    const StepMeta& m = idx.steps[s - 1];
+    if (m.words != words) return false;
+    if (s == 1 && m.rows != 1) return false;
+    if (s < L && idx.steps[s].rows != m.nnz) return false;
+    const uint64_t want_pay = (m.fmt == ZG_FMT_SPARSE) ? (uint64_t)m.nnz * 2 : (uint64_t)m.rows * words * 4;
+    if (m.bytes_payload != want_pay || m.off_rowptr % 4 || m.off_payload % 4) return false;
+    const uint32_t* rp = reinterpret_cast<const uint32_t*>(img.data() + m.off_rowptr);
+    if (rp[0] != 0 || rp[m.rows] != m.nnz) return false;
+    uint32_t mf = 0;
+    for (uint32_t r = 0; r < m.rows; ++r) {
+      if (rp[r + 1] < rp[r]) return false;
+      const uint32_t F = rp[r + 1] - rp[r];
+      if (F > V) return false;
+      mf = std::max(mf, F);
+      if (m.fmt == ZG_FMT_SPARSE) {
+        const uint16_t* col = reinterpret_cast<const uint16_t*>(img.data() + m.off_payload) + rp[r];
+        for (uint32_t j = 0; j < F; ++j)
+          if (col[j] >= V || (j > 0 && col[j] <= col[j - 1])) return false;
+      } else {
+        const uint32_t* bm = reinterpret_cast<const uint32_t*>(img.data() + m.off_payload) + (uint64_t)r * words;
+        uint32_t pc = 0;
+        for (uint32_t w = 0; w < words; ++w) pc += (uint32_t)__builtin_popcount(bm[w]);
+        if (V % 32 && (bm[words - 1] >> (V % 32))) return false;  // no bit at a token >= V
+        if (pc != F) return false;
+      }
+    }
+    if (mf != m.max_fanout) return false;
+  }
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
 zg_status zg_index_load(const char* path, int32_t residency, void* stream, zg_index** out) {
   if (!path || !out) return fail(ZG_ERR_INVALID_ARG, "zg_index_load: NULL argument");
   *out = nullptr;
@@ -706,6 +757,7 @@ zg_status zg_index_load(const char* path, int32_t residency, void* stream, zg_in
     uint64_t h = 0;
     ok = std::fread(img.data(), 1, tot, f) == tot && std::fread(&h, 8, 1, f) == 1 && h == fnv1a(img.data(), tot);
   }
+  ok = ok && tables_valid(*idx, img);
   std::fclose(f);
   if (!ok) return fail(ZG_ERR_IO, std::string("zg_index_load: short, corrupt or foreign file ") + path);
   idx->residency = residency;

@@ -24,6 +24,8 @@
 // so a tile's epilogue overlaps the next tile's loads and MMAs.  Every wait is bounded; on
 // expiry the kernel records kStatusTimeout, drains its own copies, frees its
 // tensor memory and returns.
+#include <atomic>
+
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -41,7 +43,7 @@ constexpr int kStageBytes = 2 * kTileA + kTileB;
 constexpr int kTmemCols = 256;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer, MMA issuer, epilogue warps
-constexpr uint32_t kSpinLimit = 1u << 26;
+constexpr uint32_t kSpinLimit = 1u << 26;  // default polls of a wait (seconds at most)
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -56,10 +58,10 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
                : "memory");
 }
 
-// Bounded wait for the phase with the given parity; false on expiry.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Bounded wait (`limit` polls) for the phase with the given parity; false on expiry.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit) {
   const uint32_t a = smem_u32(bar);
-  for (uint32_t it = 0; it < kSpinLimit; ++it) {
+  for (uint32_t it = 0; it < limit; ++it) {
     uint32_t done;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
@@ -137,12 +139,12 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
 __global__ void __launch_bounds__(kThreads, 1)
     k_full_tc(const __grid_constant__ CUtensorMap map_hi, const __grid_constant__ CUtensorMap map_lo,
               const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_z, int M, int V,
-              int d, int ldz, uint32_t ab_type, const FullEpi epi, uint32_t* status) {
+              int d, int ldz, uint32_t ab_type, const FullEpi epi, uint32_t* status, uint32_t spin) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // stage buffers must sit on 1024-byte boundaries (swizzle atoms)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* staging = smem + kStages * kStageBytes;  // one 4 KiB block per epilogue warp
-  __shared__ uint64_t full_bar[kStages], empty_bar[kStages], tfull_bar[2], tempty_bar[2];
+  __shared__ uint64_t full_bar[kStages], empty_bar[kStages], tfull_bar[2], tempty_bar[2], drain_bar;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -160,6 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&tfull_bar[i], 1);
       mbar_init(&tempty_bar[i], kEpiWarps);
     }
+    mbar_init(&drain_bar, 1);
     abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -181,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int m0 = (t / ntn) * kBM, n0 = (t % ntn) * kBN;
       for (int kb = 0; kb < nk; ++kb, ++kg) {
         const int st = kg % kStages;
-        if (kg >= kStages && !mbar_wait(&empty_bar[st], ((kg / kStages) - 1) & 1)) {
+        if (kg >= kStages && !mbar_wait(&empty_bar[st], ((kg / kStages) - 1) & 1, spin)) {
           atomicOr(status, kStatusTimeout);
           atomicExch(&abort_flag, 1);
           break;
@@ -196,14 +199,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     // drain: every issued stage must have landed before the CTA may exit
-    for (int k = (kg > kStages ? kg - kStages : 0); k < kg; ++k) mbar_wait(&full_bar[k % kStages], (k / kStages) & 1);
+    // (always the default limit, whatever the pipeline waits were given)
+    for (int k = (kg > kStages ? kg - kStages : 0); k < kg; ++k)
+      if (!mbar_wait(&full_bar[k % kStages], (k / kStages) & 1, kSpinLimit)) atomicOr(status, kStatusTimeout);
   } else if (warp == 1 && lane == 0) {
     // MMA issuer: accumulator buffer (i & 1) for the i-th tile of this CTA
     const uint32_t idesc = instr_desc(ab_type);
     int kg = 0, i = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
       const int b = i & 1;
-      if (atomicAdd(&abort_flag, 0) || (i >= 2 && !mbar_wait(&tempty_bar[b], ((i >> 1) - 1) & 1))) {
+      if (atomicAdd(&abort_flag, 0) || (i >= 2 && !mbar_wait(&tempty_bar[b], ((i >> 1) - 1) & 1, spin))) {
         atomicOr(status, kStatusTimeout);
         atomicExch(&abort_flag, 1);
         break;
@@ -213,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int kb = 0; kb < nk; ++kb, ++kg) {
         const int st = kg % kStages;
-        if (!mbar_wait(&full_bar[st], (kg / kStages) & 1) || atomicAdd(&abort_flag, 0)) {
+        if (!mbar_wait(&full_bar[st], (kg / kStages) & 1, spin) || atomicAdd(&abort_flag, 0)) {
           atomicOr(status, kStatusTimeout);
           atomicExch(&abort_flag, 1);
           ok = false;
@@ -234,6 +239,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&tfull_bar[b]);  // arrives once every MMA issued above has completed
       if (!ok) break;
     }
+    // drain: every MMA this thread issued has finished with tensor memory and
+    // the stage buffers before the accumulators are freed (default limit)
+    mma_commit(&drain_bar);
+    if (!mbar_wait(&drain_bar, 0, kSpinLimit)) atomicOr(status, kStatusTimeout);
   } else if (warp >= 2) {
     // epilogue: TMEM -> registers (one row a thread) -> partials, and the
     // scores through a swizzled staging block to TMA stores
@@ -255,6 +264,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (epi.bitmap && row < M) {
         const uint32_t brow = epi.by_m ? (uint32_t)row : (epi.rows ? epi.rows[row] : 0u);
         dead = (brow == kDeadRow);
+        if (!dead && brow >= epi.nrows) {  // never read past the table: flag, treat as dead
+          atomicOr(status, kStatusRow);
+          dead = true;
+        }
         if (!dead) {
 #pragma unroll
           for (int ci = 0; ci < kBN / 64; ++ci) {
@@ -263,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      const bool got = mbar_wait(&tfull_bar[b], (i >> 1) & 1);
+      const bool got = mbar_wait(&tfull_bar[b], (i >> 1) & 1, spin);
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       if (!got || atomicAdd(&abort_flag, 0)) {
         if (lane == 0) {
@@ -403,6 +416,8 @@ bool make_map(CUtensorMap* m, const void* base, int rows, int d, int box_rows, b
   return r == CUDA_SUCCESS;
 }
 
+std::atomic<uint32_t> g_wait_limit{kSpinLimit};
+
 }  // namespace
 
 size_t full_tc_smem_bytes() { return (size_t)kStages * kStageBytes + kEpiWarps * 4096 + 1024; }
@@ -447,8 +462,11 @@ cudaError_t launch_full_tc(const void* hi, const void* lo, const void* W, float*
   // persistent: one CTA per SM (shared memory admits one), tiles strided over the CTAs
   const int ntiles = ((V + kBN - 1) / kBN) * ((M + kBM - 1) / kBM);
   const int grid = std::max(1, std::min(ntiles, sm_count()));
-  k_full_tc<<<grid, kThreads, smem, st>>>(mh, ml, mw, mz, M, V, d, ldz, bf16 ? 1u : 0u, epi, status);
+  k_full_tc<<<grid, kThreads, smem, st>>>(mh, ml, mw, mz, M, V, d, ldz, bf16 ? 1u : 0u, epi, status,
+                                          g_wait_limit.load(std::memory_order_relaxed));
   return cudaGetLastError();
 }
+
+void set_wait_limit(uint32_t polls) { g_wait_limit.store(polls ? polls : kSpinLimit, std::memory_order_relaxed); }
 
 }  // namespace zg

@@ -98,6 +98,9 @@ struct FullEpi {
   const uint32_t* rows;    // [M] index row of each beam (kDeadRow: dead); null: row 0
   int words;               // bitmap words a row
   int by_m;                // bitmap row m belongs to beam row m (rows unused)
+  uint32_t nrows;          // bitmap rows: an index row at or beyond it is flagged kStatusRow
+                           // and treated as dead (never read)
+  uint32_t* status;        // device status word (for that flag)
 };
 
 #ifdef __CUDACC__
@@ -107,6 +110,10 @@ __device__ __forceinline__ uint32_t epi_legal_mask(const FullEpi& e, int m, int 
   if (e.bitmap) {
     const uint32_t r = e.by_m ? (uint32_t)m : (e.rows ? e.rows[m] : 0u);
     if (r == kDeadRow) return 0u;
+    if (r >= e.nrows) {
+      atomicOr(e.status, kStatusRow);
+      return 0u;
+    }
     mask = e.bitmap[(size_t)r * e.words + chunk];
   }
   const int rem = V - chunk * 32;
@@ -145,6 +152,13 @@ cudaError_t status_word(uint32_t** dev_ptr);   // per-device status word address
 cudaError_t launch_split_h(const float* H, void* hi, void* lo, size_t n, int w_dtype, cudaStream_t st);
 cudaError_t launch_full_tc(const void* hi, const void* lo, const void* W, float* Z, int M, int V, int d, int ldz,
                            int w_dtype, const FullEpi& epi, uint32_t* status, cudaStream_t st);
+// polls of an mbarrier before a pipeline wait of the tensor-core kernel gives
+// up (0: the default); the drain waits before exit always use the default
+void set_wait_limit(uint32_t polls);
+// Unique id of the calling thread's current CUDA context (the driver's
+// cuCtxGetId; a context created after cudaDeviceReset gets a new id).  Device
+// addresses of __device__ variables are cached per context under this id.
+cudaError_t current_context_id(unsigned long long* id);
 // Work counts of the beams entering a step (tracing only): counters[0..3] =
 // live beams, legal slots, chunks, index bytes; mask = V-bit set of touched
 // tokens.  Both must be zeroed by the caller.

@@ -309,7 +309,9 @@ ZG_API zg_status zg_decode_trace(const zg_index* idx, const zg_plan* plan, const
  * rejected with ZG_ERR_INVALID_ARG before anything runs.  It calls no
  * cudaMalloc, cudaFree or other allocating routine.  The first call on a
  * device looks up the array's device address (cudaGetSymbolAddress) with
- * that device current; make that first call before any stream capture.
+ * that device current; make that first call before any stream capture.  The
+ * address is cached per device and CUDA context: after cudaDeviceReset the
+ * next call (again outside any capture) looks it up in the new context.
  * Every call on a device shares the one array and it keeps the previous
  * call's contents (the decode writes every scratch word before reading it,
  * so nothing needs clearing): calls whose executions can overlap on the GPU
@@ -317,6 +319,19 @@ ZG_API zg_status zg_decode_trace(const zg_index* idx, const zg_plan* plan, const
 ZG_API zg_status zg_decode_static(const zg_index* idx, const zg_plan* plan, const zg_model* model,
                                   const float* u, int32_t B, int32_t beam, int32_t K,
                                   int32_t* out_sids, float* out_scores, void* stream);
+
+/* ZG_STATIC_SCRATCH_BYTES as compiled into the library (for bindings that
+ * cannot read the header). */
+ZG_API size_t zg_static_scratch_bytes(void);
+
+/* Test and diagnosis hook, no counterpart in the paper: the number of polls
+ * after which a pipeline wait (an mbarrier) of the tensor-core full
+ * projection gives up, records bit 2 in the device status word and ends the
+ * kernel early (its copies and tensor-core operations drained, tensor memory
+ * freed).  0 restores the default (2^26 polls, about a second).  Applies to
+ * launches issued after the call, process-wide.  A limit too small for the
+ * work makes decodes fail with ZG_ERR_DEVICE_STATUS. */
+ZG_API void zg_debug_set_wait_limit(uint32_t polls);
 
 /* Synchronises `stream`, then reports and clears the device status word that
  * kernels set instead of trapping (bit 0: row out of range, bit 1: token out

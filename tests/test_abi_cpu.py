@@ -204,3 +204,87 @@ def test_plan_variants_and_order_checked(zg):
         zg.zg_plan_set_order(p, 2)
     with pytest.raises(zg.ZgError):
         zg.zg_plan_force(idx, 2, 4, [3] * L)
+
+
+def _fnv1a(b: bytes) -> int:
+    h = 1469598103934665603
+    for x in b:
+        h = ((h ^ x) * 1099511628211) & 0xFFFFFFFFFFFFFFFF
+    return h
+
+
+def _parse_index_file(raw: bytes):
+    """Header fields and per-step metadata of a saved index, and where the
+    table image starts (the layout zg_index_save writes)."""
+    L, V = np.frombuffer(raw[8:16], "<i4")
+    off = 8 + 8 + 16 + 8
+    steps = []
+    for _ in range(int(L)):
+        fmt = int(np.frombuffer(raw[off:off + 4], "<i4")[0])
+        rows, nnz, words, mf = (int(x) for x in np.frombuffer(raw[off + 4:off + 20], "<u4"))
+        o_rp, o_pay, b_rp, b_pay = (int(x) for x in np.frombuffer(raw[off + 20:off + 52], "<u8"))
+        steps.append(dict(fmt=fmt, rows=rows, nnz=nnz, words=words, mf=mf, o_rp=o_rp, o_pay=o_pay))
+        off += 52
+    return int(L), int(V), steps, off
+
+
+@pytest.mark.parametrize("damage", ["rowptr_decreasing", "rowptr_end", "token_ge_v", "tokens_unsorted",
+                                    "bitmap_extra_bit", "max_fanout"])
+def test_load_rejects_inconsistent_tables(zg, tmp_path, damage):
+    """A file whose checksum is intact but whose tables break the index's
+    invariants (rowptr from 0 to nnz, non-decreasing; tokens below V and
+    ascending in a row; a dense row's popcount = its fan-out; the stored
+    largest fan-out) is refused on load, so no kernel can be pointed out of
+    the tables' bounds by a loaded file."""
+    L, V, sids = 3, 64, tiny_catalogue(3, 64, 500, 9)
+    idx = zg.zg_index_build(sids, V, residency=zg.ZG_RESIDENT_HOST, format_mode=zg.ZG_FORMAT_AUTO)
+    p = str(tmp_path / "i.zgidx")
+    zg.zg_index_save(idx, p)
+    raw = bytearray(open(p, "rb").read())
+    L, V, steps, img0 = _parse_index_file(bytes(raw))
+    assert [st["fmt"] for st in steps] == [1, 1, 0]    # dense, dense, sparse under the automatic rule
+    dense, sparse = steps[1], steps[2]
+
+    def u32(at, val=None):
+        o = img0 + at
+        if val is None:
+            return int(np.frombuffer(raw[o:o + 4], "<u4")[0])
+        raw[o:o + 4] = np.array([val], "<u4").tobytes()
+
+    def u16(at, val=None):
+        o = img0 + at
+        if val is None:
+            return int(np.frombuffer(raw[o:o + 2], "<u2")[0])
+        raw[o:o + 2] = np.array([val], "<u2").tobytes()
+
+    if damage == "rowptr_decreasing":
+        u32(sparse["o_rp"] + 4 * 2, u32(sparse["o_rp"] + 4 * 1) - 1 if u32(sparse["o_rp"] + 4) else 5)
+    elif damage == "rowptr_end":
+        u32(sparse["o_rp"] + 4 * sparse["rows"], sparse["nnz"] + 3)
+    elif damage == "token_ge_v":
+        u16(sparse["o_pay"], V + 5)
+    elif damage == "tokens_unsorted":
+        r = next(r for r in range(sparse["rows"]) if u32(sparse["o_rp"] + 4 * (r + 1)) - u32(sparse["o_rp"] + 4 * r) >= 2)
+        e = u32(sparse["o_rp"] + 4 * r)
+        a, b = u16(sparse["o_pay"] + 2 * e), u16(sparse["o_pay"] + 2 * (e + 1))
+        u16(sparse["o_pay"] + 2 * e, b)
+        u16(sparse["o_pay"] + 2 * (e + 1), a)
+    elif damage == "bitmap_extra_bit":
+        w = u32(dense["o_pay"])
+        bit = next(i for i in range(32) if not (w >> i) & 1)
+        u32(dense["o_pay"], w | (1 << bit))
+    elif damage == "max_fanout":
+        o = 8 + 8 + 16 + 8 + 2 * 52 + 16          # step 3's stored max fan-out field
+        raw[o:o + 4] = np.array([sparse["mf"] + 1], "<u4").tobytes()
+    tot = len(raw) - img0 - 8
+    raw[-8:] = np.array([_fnv1a(bytes(raw[img0:img0 + tot]))], "<u8").tobytes()
+    open(p, "wb").write(bytes(raw))
+    with pytest.raises(zg.ZgError) as e:
+        zg.zg_index_load(p, zg.ZG_RESIDENT_HOST)
+    assert e.value.status == 7
+
+
+def test_static_scratch_size_matches_header(zg):
+    txt = open(os.path.join(ROOT, "include", "zerogr.h")).read()
+    m = re.search(r"#define ZG_STATIC_SCRATCH_BYTES \((\d+)u << (\d+)\)", txt)
+    assert m and zg._lib.ZG_STATIC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))

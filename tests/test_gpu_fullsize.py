@@ -1,10 +1,20 @@
-"""Full-size configurations (10M-100M items) on the GPU, checked against the
-oracle on sampled requests: the codebook sweep (V = 2,048 .. 16,384, bf16),
-the dense-early catalogue (50M items, fp16) and the large catalogue (100M
-items, bf16, beam 256).  Index tables are compared bit-exact (10M items) or on
-sampled rows (50M/100M items); decodes run the whole batch in the tuned plan
-and in forced all-selective / all-full plans, and the oracle decodes the
-first and last request of the batch."""
+"""Full-size configurations (10M-100M items) on the GPU against the oracle:
+the codebook sweep (V = 2,048 .. 16,384, bf16), the dense-early catalogue
+(50M items, fp16) and the large catalogue (100M items, bf16, beam 256) at
+batch 64 and at the batch sweep's 1, 8 and 32.
+
+  * Index: every step table of every configuration bit-exact against the
+    oracle's serialisation.
+  * Decode: the whole batch in the tuned plan and in forced all-selective and
+    all-full plans; every request of the batch is checked against the
+    oracle's beam search (check_topk: SIDs in the catalogue, each score equal
+    to the exact path score within the tolerance, the same top-K set wherever
+    no intermediate beam boundary is a near-tie).  The number of requests
+    with such a near-tie is reported and bounded.
+  * Unconstrained decode: eight requests against the oracle.
+"""
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -17,7 +27,9 @@ torch = pytest.importorskip("torch")
 
 TOL = 2e-2        # bf16/fp16 weights, fp32 accumulation
 WINDOW = 1e-4     # the fp32-accumulated paths decide near-ties to ~1e-6
-CONFIGS = ["sweep_v2048", "sweep_v4096", "sweep_v8192", "sweep_v16384", "dense_early", "large"]
+CASES = [("sweep_v2048", 0), ("sweep_v4096", 0), ("sweep_v8192", 0), ("sweep_v16384", 0),
+         ("dense_early", 0), ("large", 0), ("large", 1), ("large", 8), ("large", 32)]
+_DATA = {}        # the last configuration's inputs, trie and oracle results (one entry)
 
 
 @pytest.fixture(scope="module")
@@ -30,17 +42,41 @@ def zg():
     return zg
 
 
-@pytest.fixture(scope="module", params=CONFIGS)
+def _inputs(name):
+    """Catalogue, model, the full batch's requests, trie and the oracle's
+    decode of every request of the full batch (cached across batch sizes)."""
+    if name not in _DATA:
+        _DATA.clear()
+        cfg = synth.CONFIGS[name]
+        sids = synth.make_catalogue(cfg, 0)
+        model = synth.make_model(cfg.L, cfg.V, cfg.d, cfg.w_dtype, 0)
+        u = synth.make_requests(cfg.batch, cfg.d, 1000)
+        trie = oracle.Trie(sids, cfg.L, cfg.V)
+        ref = oracle.decode(trie, model, u, cfg.beam, cfg.topk)
+        _DATA[name] = (sids, model, u, trie, ref)
+    return _DATA[name]
+
+
+def _head(ref, B):
+    """The oracle's results of the first B requests."""
+    return oracle.DecodeResult(ref.sids[:B], ref.scores[:B], ref.gaps[:B], ref.n_cand[:B], ref.next_score[:B])
+
+
+@pytest.fixture(scope="module", params=CASES, ids=[f"{n}-b{b}" if b else n for n, b in CASES])
 def full(request, zg):
-    cfg = synth.CONFIGS[request.param]
-    sids = synth.make_catalogue(cfg, 0)
-    model = synth.make_model(cfg.L, cfg.V, cfg.d, cfg.w_dtype, 0)
-    u = synth.make_requests(cfg.batch, cfg.d, 1000)
+    name, B = request.param
+    cfg = synth.CONFIGS[name]
+    sids, model, u, trie, ref = _inputs(name)
+    if B:
+        # requests 0..B-1 of the same seeded stream: the first B rows of the full batch
+        cfg = dataclasses.replace(cfg, batch=B)
+        u = synth.make_requests(B, cfg.d, 1000)
+        assert np.array_equal(u, _DATA[name][2][:B])
+        ref = _head(ref, B)
     stream = torch.cuda.current_stream().cuda_stream
     idx = zg.zg_index_build(sids, cfg.V, stream=stream)
-    trie = oracle.Trie(sids, cfg.L, cfg.V)
-    yield cfg, sids, model, u, idx, trie
-    del idx, trie, sids
+    yield cfg, sids, model, u, idx, trie, ref, B
+    del idx
 
 
 def _decode(zg, cfg, idx, dm, u, plan):
@@ -53,37 +89,18 @@ def _decode(zg, cfg, idx, dm, u, plan):
 
 
 def test_fullsize_index(zg, full):
-    cfg, sids, model, u, idx, trie = full
+    cfg, sids, model, u, idx, trie, ref, B = full
+    if B:
+        pytest.skip("index checked once per catalogue")
     info = zg.zg_index_info_get(idx)
     assert info["n_unique"] == trie.n_unique
-    if cfg.n_items <= 10_000_000:
-        tabs = oracle.serialize_index(sids, cfg.L, cfg.V)
-        for s in range(1, cfg.L + 1):
-            assert zg.zg_index_export(idx, s) == tabs[s - 1].export_bytes(), f"step {s}"
-        return
-    # sampled rows: the r-th row of step s is the r-th distinct (s-1)-prefix
-    rng = np.random.default_rng(0)
+    tabs = oracle.serialize_index(sids, cfg.L, cfg.V)
     for s in range(1, cfg.L + 1):
-        raw = zg.zg_index_export(idx, s)
-        fmt, rows, nnz, words = np.frombuffer(raw[:16], "<u4")
-        rowptr = np.frombuffer(raw[16:16 + 4 * (rows + 1)], "<u4")
-        pay = raw[16 + 4 * (rows + 1):]
-        prefixes = np.unique(trie.keys // (cfg.V ** (cfg.L - s + 1)))
-        assert prefixes.size == rows and rowptr[-1] == nnz
-        for r in rng.integers(0, rows, size=min(rows, 300)):
-            p = int(prefixes[r])
-            pre = tuple(int(x) for x in oracle.keys_to_sids(np.array([p]), s - 1, cfg.V)[0]) if s > 1 else ()
-            want = trie.children(pre)
-            if fmt == 0:
-                got = np.frombuffer(pay, "<u2")[rowptr[r]:rowptr[r + 1]].astype(np.int64)
-            else:
-                bm = np.frombuffer(pay, "<u4")[r * words:(r + 1) * words]
-                got = np.nonzero(np.unpackbits(bm.view(np.uint8), bitorder="little"))[0]
-            assert np.array_equal(got, want), f"step {s} row {r}"
+        assert zg.zg_index_export(idx, s) == tabs[s - 1].export_bytes(), f"step {s}"
 
 
 def test_fullsize_decode_plans(zg, full):
-    cfg, sids, model, u, idx, trie = full
+    cfg, sids, model, u, idx, trie, ref, B = full
     from generative_recommendation_constrained_gb300.device import DeviceModel
     dm = DeviceModel(model)
     stream = torch.cuda.current_stream().cuda_stream
@@ -92,23 +109,35 @@ def test_fullsize_decode_plans(zg, full):
     plans = {"tuned": tuned,
              "selective": zg.zg_plan_force(idx, cfg.batch, cfg.beam, [0] * cfg.L),
              "full": zg.zg_plan_force(idx, cfg.batch, cfg.beam, [1] * cfg.L)}
-    sample = [0, cfg.batch - 1]
-    ref = oracle.decode(trie, model, u, cfg.beam, cfg.topk, requests=sample)
+    amb = {}
     outs = {}
     for name, plan in plans.items():
         s, sc = _decode(zg, cfg, idx, dm, u, plan)
-        check_topk(s, sc, ref, trie, model, u, TOL, WINDOW, requests=sample)
+        amb[name] = check_topk(s, sc, ref, trie, model, u, TOL, WINDOW)
         outs[name] = sc
-    # every plan scores the whole batch alike (rounding aside)
-    d = np.nan_to_num(np.abs(outs["selective"] - outs["full"]), posinf=0.0)
-    assert np.mean(d < 1e-3) > 0.9
+    print(f"{cfg.name} batch {cfg.batch}: requests with an intermediate near-tie (set check skipped): {amb}")
+    # every request is checked for validity and exact path scores; the set check
+    # may be skipped only where the oracle's own beam boundary is a near-tie
+    near = int(np.sum(np.any(ref.gaps[:, :cfg.L - 1] <= WINDOW, axis=1)))
+    assert all(a == near for a in amb.values())
+    assert near <= max(1, cfg.batch // 8), f"{near} of {cfg.batch} requests have near-ties"
+    # where no beam boundary is a near-tie, every plan returns the same scores
+    clean = ~np.any(ref.gaps[:, :cfg.L - 1] <= WINDOW, axis=1)
+    for name in ("selective", "full"):
+        a, b = outs["tuned"][clean], outs[name][clean]
+        fin = np.isfinite(a)
+        assert np.array_equal(fin, np.isfinite(b))
+        assert np.max(np.abs(a[fin] - b[fin]), initial=0.0) <= TOL
 
 
 def test_fullsize_unconstrained(zg, full):
-    cfg, sids, model, u, idx, trie = full
+    cfg, sids, model, u, idx, trie, ref, B = full
+    if B:
+        pytest.skip("unconstrained decode checked once per catalogue")
     from generative_recommendation_constrained_gb300.device import DeviceModel
     dm = DeviceModel(model)
-    uu = u[:4]
+    uu = np.ascontiguousarray(u[:8])
     s, sc = _decode(zg, cfg, None, dm, uu, None)
-    ref = oracle.decode(None, model, uu, cfg.beam, cfg.topk, requests=[0])
-    check_topk(s, sc, ref, None, model, uu, TOL, WINDOW, requests=[0])
+    uref = oracle.decode(None, model, uu, cfg.beam, cfg.topk)
+    amb = check_topk(s, sc, uref, None, model, uu, TOL, WINDOW)
+    assert amb <= 2
