@@ -7,6 +7,8 @@ import numpy as np
 
 import synth
 
+LAST_MAX_ERR = 0.0
+
 
 def tiny_catalogue(L: int, V: int, n: int, seed: int) -> np.ndarray:
     return synth.catalogue_uniform(L, V, n, seed)
@@ -33,12 +35,15 @@ def check_topk(gpu_sids, gpu_scores, ref, trie, model, u, tol, window, requests=
         the same number of outputs is returned, the sorted score lists agree
         within ``tol`` and every oracle item whose score clears the first
         dropped candidate by more than ``window`` is returned.
-    Returns the number of requests that had only the first two checks."""
+    Returns the number of requests that had only the first two checks; the
+    largest |score - exact path score| seen is left in LAST_MAX_ERR."""
+    global LAST_MAX_ERR
     gpu_sids = np.asarray(gpu_sids)
     gpu_scores = np.asarray(gpu_scores, dtype=np.float64)
     B, K, L = gpu_sids.shape
     req = range(B) if requests is None else list(requests)
     ambiguous = 0
+    max_err = 0.0
     Wd = [model.W_as_f64(s) for s in range(model.L)]
     for q in req:
         valid = gpu_sids[q, :, 0] >= 0
@@ -57,6 +62,8 @@ def check_topk(gpu_sids, gpu_scores, ref, trie, model, u, tol, window, requests=
             if trie is not None:
                 assert trie.contains(sid), f"request {q}: SID {sid} not in catalogue"
             exact = _path(trie, model, u[q], sid, order, Wd)
+            max_err = max(max_err, abs(exact - sc[i]))
+            LAST_MAX_ERR = max_err
             assert abs(exact - sc[i]) <= tol, \
                 f"request {q} rank {i}: score {sc[i]} vs exact {exact}"
         if np.any(ref.gaps[q, :L - 1] <= window):

@@ -11,6 +11,7 @@ import pytest
 
 import oracle
 import synth
+import _helpers as _h
 from _helpers import check_topk, golden_catalogue, tiny_catalogue
 from conftest import read_golden
 
@@ -127,7 +128,11 @@ def test_mid_sparse_parity(zg, mid, variants, fused):
     cfg, sids, model, u, trie, ref, idx = mid
     s, sc = decode_gpu(zg, idx, model, u, cfg.beam, cfg.topk, variants, fused=fused)
     amb = check_topk(s, sc, ref, trie, model, u, 1e-4, WINDOW)
-    assert amb <= cfg.batch // 4
+    # the set check is skipped only for requests whose oracle beam boundary is
+    # a near-tie (2 of the 32 requests of this seeded batch at this window)
+    near = int(np.sum(np.any(ref.gaps[:, :cfg.L - 1] <= WINDOW, axis=1)))
+    print(f"mid sparse {variants} fused={fused}: near-tie requests {amb}, max score error {_h.LAST_MAX_ERR:.2e}")
+    assert amb == near <= 2
 
 
 def test_mid_sparse_tuned_plan(zg, mid):

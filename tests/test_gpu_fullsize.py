@@ -20,13 +20,19 @@ import pytest
 
 import oracle
 import synth
+import _helpers as _h
 from _helpers import check_topk
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 torch = pytest.importorskip("torch")
 
 TOL = 2e-2        # bf16/fp16 weights, fp32 accumulation
-WINDOW = 1e-4     # the fp32-accumulated paths decide near-ties to ~1e-6
+# Decision window: every GPU path accumulates in fp32 (the tensor-core path
+# with the hidden split into two halves), so candidate scores agree with the
+# fp64 oracle to ~1e-6 and a beam boundary can only flip where the oracle's
+# own gap is below ~1e-5.  With beam 256 such near-ties are not rare (6 of the
+# 64 large-catalogue requests, 3 of 128 dense-early, none of the sweep's).
+WINDOW = 1e-5
 CASES = [("sweep_v2048", 0), ("sweep_v4096", 0), ("sweep_v8192", 0), ("sweep_v16384", 0),
          ("dense_early", 0), ("large", 0), ("large", 1), ("large", 8), ("large", 32)]
 _DATA = {}        # the last configuration's inputs, trie and oracle results (one entry)
@@ -114,13 +120,14 @@ def test_fullsize_decode_plans(zg, full):
     for name, plan in plans.items():
         s, sc = _decode(zg, cfg, idx, dm, u, plan)
         amb[name] = check_topk(s, sc, ref, trie, model, u, TOL, WINDOW)
+        amb[name + "_max_err"] = _h.LAST_MAX_ERR
         outs[name] = sc
-    print(f"{cfg.name} batch {cfg.batch}: requests with an intermediate near-tie (set check skipped): {amb}")
+    print(f"{cfg.name} batch {cfg.batch}: near-tie requests (set check skipped) and max |score - exact|: {amb}")
     # every request is checked for validity and exact path scores; the set check
     # may be skipped only where the oracle's own beam boundary is a near-tie
     near = int(np.sum(np.any(ref.gaps[:, :cfg.L - 1] <= WINDOW, axis=1)))
-    assert all(a == near for a in amb.values())
-    assert near <= max(1, cfg.batch // 8), f"{near} of {cfg.batch} requests have near-ties"
+    assert all(amb[n] == near for n in plans)
+    assert near <= max(2, cfg.batch // 8), f"{near} of {cfg.batch} requests have near-ties"
     # where no beam boundary is a near-tie, every plan returns the same scores
     clean = ~np.any(ref.gaps[:, :cfg.L - 1] <= WINDOW, axis=1)
     for name in ("selective", "full"):
