@@ -93,6 +93,8 @@ def _load():
         "zg_decode_trace": [vp, vp, P(zg_model), vp, i32, i32, i32, vp, vp, vp, sz, vp, P(zg_trace)],
         "zg_decode_static": [vp, vp, P(zg_model), vp, i32, i32, i32, vp, vp, vp],
         "zg_check_device_status": [vp],
+        "zg_plan_save": [vp, C.c_char_p],
+        "zg_plan_load": [C.c_char_p, P(vp)],
     }
     for name, args in sigs.items():
         f = getattr(lib, name)
@@ -110,6 +112,8 @@ def _load():
     lib.zg_static_scratch_bytes.restype = C.c_size_t
     lib.zg_debug_set_wait_limit.argtypes = [C.c_uint32]
     lib.zg_debug_set_wait_limit.restype = None
+    lib.zg_debug_inject_build_failure.argtypes = [C.c_int32, C.c_int32]
+    lib.zg_debug_inject_build_failure.restype = None
     return lib
 
 
@@ -283,6 +287,26 @@ def zg_decode_static(idx: Index | None, plan: Plan | None, model: zg_model, u, B
     """zg_decode without a workspace: scratch from the library's static device array."""
     _check(lib.zg_decode_static(idx, plan, C.byref(model), _ptr(u), B, beam, K, _ptr(out_sids),
                                 _ptr(out_scores), stream or None))
+
+
+ZG_INJECT_PINNED_ALLOC, ZG_INJECT_COPY = 1, 2
+
+
+def zg_debug_inject_build_failure(point: int = 0, after: int = 0):
+    """Make the index builder's (after+1)-th next pinned allocation or copy fail once (0: disarm)."""
+    lib.zg_debug_inject_build_failure(int(point), int(after))
+
+
+def zg_plan_save(plan: Plan, path: str):
+    _check(lib.zg_plan_save(plan, path.encode()))
+
+
+def zg_plan_load(path: str) -> Plan:
+    h = C.c_void_p()
+    _check(lib.zg_plan_load(path.encode(), C.byref(h)))
+    with open(path, "rb") as f:                 # steps: the int32 after the 8-byte magic
+        L = int.from_bytes(f.read(12)[8:12], "little")
+    return Plan(h.value, L)
 
 
 def zg_debug_set_wait_limit(polls: int = 0):

@@ -11,10 +11,14 @@
 //     token at every step and serves as the speed reference.
 #include <algorithm>
 #include <cmath>
-#include <vector>
+#include <cstdio>
 #include <cstring>
+#include <memory>
 #include <mutex>
 #include <string>
+#include <vector>
+
+#include <nvtx3/nvToolsExt.h>
 
 #include "zg_internal.h"
 
@@ -443,14 +447,34 @@ int prefetch_set(const Run& r, int s0, PrefetchRegion* pf) {
   return n;
 }
 
+// An NVTX range for the host-side span of a call (profiler timelines); a
+// no-op unless a tool is attached.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
+
+const char* step_range_name(int s, int variant) {
+  static const char* names[ZG_MAX_STEPS][3] = {
+      {"zg step 1 selective", "zg step 1 full", "zg step 1 naive"}, {"zg step 2 selective", "zg step 2 full", "zg step 2 naive"},
+      {"zg step 3 selective", "zg step 3 full", "zg step 3 naive"}, {"zg step 4 selective", "zg step 4 full", "zg step 4 naive"},
+      {"zg step 5 selective", "zg step 5 full", "zg step 5 naive"}, {"zg step 6 selective", "zg step 6 full", "zg step 6 naive"},
+      {"zg step 7 selective", "zg step 7 full", "zg step 7 naive"}, {"zg step 8 selective", "zg step 8 full", "zg step 8 naive"}};
+  return names[s - 1][variant];
+}
+
 // zg_decode's launch sequence: stand-alone steps, then the fused suffix.
 zg_status decode_steps(const Run& r, const zg_plan* plan, cudaStream_t st, cudaEvent_t* fuse_ev = nullptr) {
+  NvtxRange whole("zg_decode");
   const int s0 = fused_from(r, plan);
   for (int s = 1; s < s0; ++s) {
-    zg_status e = run_step(r, s, variant_of(r, plan, s), st);
+    const int v = variant_of(r, plan, s);
+    NvtxRange step(step_range_name(s, v));
+    zg_status e = run_step(r, s, v, st);
     if (e != ZG_OK) return e;
   }
   if (s0 <= r.m.L) {
+    NvtxRange fused("zg fused selective steps");
     StepLaunch steps[ZG_MAX_STEPS];
     fused_launches(r, s0, steps);
     PrefetchRegion pf[kMaxPrefetch];
@@ -544,6 +568,94 @@ zg_status zg_plan_describe(const zg_plan* plan, uint8_t* variant, float* step_ms
 
 void zg_plan_free(zg_plan* plan) { delete plan; }
 
+}  // extern "C"
+
+namespace {
+const char kPlanMagic[8] = {'Z', 'G', 'P', 'L', 'A', 'N', 0, 1};
+
+uint64_t plan_fnv1a(const std::vector<uint8_t>& b) {
+  uint64_t h = 1469598103934665603ull;
+  for (uint8_t x : b) {
+    h ^= x;
+    h *= 1099511628211ull;
+  }
+  return h;
+}
+
+template <typename T>
+void put(std::vector<uint8_t>& b, const T& v) {
+  const uint8_t* p = reinterpret_cast<const uint8_t*>(&v);
+  b.insert(b.end(), p, p + sizeof(T));
+}
+
+template <typename T>
+bool get(const std::vector<uint8_t>& b, size_t& at, T* v) {
+  if (at + sizeof(T) > b.size()) return false;
+  std::memcpy(v, b.data() + at, sizeof(T));
+  at += sizeof(T);
+  return true;
+}
+}  // namespace
+
+extern "C" {
+
+zg_status zg_plan_save(const zg_plan* plan, const char* path) {
+  if (!plan || !path) return fail(ZG_ERR_INVALID_ARG, "zg_plan_save: NULL argument");
+  std::vector<uint8_t> body;
+  put(body, plan->L);
+  put(body, plan->B);
+  put(body, plan->beam);
+  put(body, plan->fused);
+  put(body, plan->order);
+  put(body, plan->plan_ms);
+  for (float x : plan->fused_ms) put(body, x);
+  for (uint8_t v : plan->variant) put(body, v);
+  for (float x : plan->step_ms) put(body, x);
+  const uint64_t h = plan_fnv1a(body);
+  FILE* f = std::fopen(path, "wb");
+  if (!f) return fail(ZG_ERR_IO, std::string("zg_plan_save: cannot open ") + path);
+  bool ok = std::fwrite(kPlanMagic, 1, 8, f) == 8 && std::fwrite(body.data(), 1, body.size(), f) == body.size() &&
+            std::fwrite(&h, 8, 1, f) == 1;
+  ok = (std::fclose(f) == 0) && ok;
+  if (!ok) return fail(ZG_ERR_IO, std::string("zg_plan_save: write failed for ") + path);
+  return ZG_OK;
+}
+
+zg_status zg_plan_load(const char* path, zg_plan** out) {
+  if (!path || !out) return fail(ZG_ERR_INVALID_ARG, "zg_plan_load: NULL argument");
+  *out = nullptr;
+  FILE* f = std::fopen(path, "rb");
+  if (!f) return fail(ZG_ERR_IO, std::string("zg_plan_load: cannot open ") + path);
+  std::vector<uint8_t> raw;
+  uint8_t buf[4096];
+  size_t n;
+  while ((n = std::fread(buf, 1, sizeof buf, f)) > 0 && raw.size() < (1u << 20)) raw.insert(raw.end(), buf, buf + n);
+  std::fclose(f);
+  auto bad = [&]() { return fail(ZG_ERR_IO, std::string("zg_plan_load: short, corrupt or foreign file ") + path); };
+  if (raw.size() < 16 || std::memcmp(raw.data(), kPlanMagic, 8) != 0) return bad();
+  std::vector<uint8_t> body(raw.begin() + 8, raw.end() - 8);
+  uint64_t h = 0;
+  std::memcpy(&h, raw.data() + raw.size() - 8, 8);
+  if (h != plan_fnv1a(body)) return bad();
+  auto p = std::make_unique<zg_plan>();
+  size_t at = 0;
+  bool ok = get(body, at, &p->L) && get(body, at, &p->B) && get(body, at, &p->beam) && get(body, at, &p->fused) &&
+            get(body, at, &p->order) && get(body, at, &p->plan_ms);
+  for (float& x : p->fused_ms) ok = ok && get(body, at, &x);
+  ok = ok && p->L >= 1 && p->L <= ZG_MAX_STEPS && p->B >= 1 && p->beam >= 1 && p->beam <= ZG_MAX_BEAM &&
+       (p->order == ZG_ORDER_FILTER_FIRST || p->order == ZG_ORDER_SCORE_FIRST) &&
+       (p->fused == 0 || p->fused == 1 || p->fused == 2 || p->fused == 4 || p->fused == 8 || p->fused == 16);
+  if (ok) {
+    p->variant.resize(p->L);
+    p->step_ms.resize((size_t)p->L * 2);
+    for (auto& v : p->variant) ok = ok && get(body, at, &v) && (v == ZG_SELECTIVE || v == ZG_FULL || v == ZG_NAIVE);
+    for (auto& x : p->step_ms) ok = ok && get(body, at, &x);
+  }
+  if (!ok || at != body.size()) return bad();
+  *out = p.release();
+  return ZG_OK;
+}
+
 zg_status zg_plan_set_fusion(zg_plan* plan, int32_t cluster_ctas) {
   if (!plan) return fail(ZG_ERR_INVALID_ARG, "zg_plan_set_fusion: plan is NULL");
   if (cluster_ctas != 0 && cluster_ctas != 1 && cluster_ctas != 2 && cluster_ctas != 4 && cluster_ctas != 8 &&
@@ -623,6 +735,7 @@ zg_status zg_tune(const zg_index* idx, const zg_model* model, const float* warm_
                   int32_t reps, void* stream, zg_plan** out) {
   if (!out) return fail(ZG_ERR_INVALID_ARG, "zg_tune: out is NULL");
   *out = nullptr;
+  NvtxRange range("zg_tune");
   if (!idx) return fail(ZG_ERR_INVALID_ARG, "zg_tune: idx is NULL (the unconstrained decode has one variant)");
   if (!warm_u) return fail(ZG_ERR_INVALID_ARG, "zg_tune: warm_u is NULL");
   if (reps < 1) reps = 1;

@@ -23,6 +23,8 @@
 #include <new>
 #include <thread>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "zg_internal.h"
 
 namespace zg {
@@ -131,6 +133,17 @@ void fill_bucket(const Layout& lay, const uint64_t* keys, int b, int s, int fmt,
   }
 }
 
+// Host-side failure injection for tests (zg_debug_inject_build_failure):
+// the `after`-th next call at `point` reports a failure instead of running.
+std::atomic<int> g_inject_point{0}, g_inject_after{0};
+
+bool injected(int point) {
+  if (g_inject_point.load(std::memory_order_relaxed) != point) return false;
+  if (g_inject_after.fetch_sub(1) > 0) return false;
+  g_inject_point.store(0);  // fires once
+  return true;
+}
+
 struct Pinned {
   uint8_t* p = nullptr;
   size_t n = 0;
@@ -142,6 +155,7 @@ struct Pinned {
     if (p) cudaFreeHost(p);
     p = nullptr;
     n = 0;
+    if (injected(ZG_INJECT_PINNED_ALLOC)) return cudaErrorMemoryAllocation;
     cudaError_t e = cudaHostAlloc((void**)&p, bytes, cudaHostAllocDefault);
     if (e == cudaSuccess) n = bytes;
     return e;
@@ -248,6 +262,7 @@ zg_status build_impl(const int32_t* sids, int64_t n, int L, int V, const zg_buil
   double ms_sort = ms_since(t0);
 
   // ---- pass 1: count rows / entries per bucket and step ----------------------
+  nvtxMarkA("zg_index_build: pass 1 (count)");
   t0 = clk::now();
   lay.cnt.assign(nb, std::vector<uint32_t>(L + 1, 0));
   lay.maxf.assign(nb, std::vector<uint32_t>(L + 1, 0));
@@ -332,6 +347,7 @@ zg_status build_impl(const int32_t* sids, int64_t n, int L, int V, const zg_buil
   double ms_count = ms_since(t0);
 
   // ---- pass 2: fill, streamed through two pinned buffers ---------------------
+  nvtxMarkA("zg_index_build: pass 2 (fill + copy)");
   t0 = clk::now();
   const bool dev = (o.residency == ZG_RESIDENT_DEVICE);
   if (dev) {
@@ -388,7 +404,8 @@ zg_status build_impl(const int32_t* sids, int64_t n, int L, int V, const zg_buil
       cudaError_t e = buf[i].ensure(cap);
       if (e != cudaSuccess) {
         cleanup_events();
-        return cuda_fail(e, "zg_index_build: cudaHostAlloc of a staging buffer");
+        return e == cudaErrorMemoryAllocation ? fail(ZG_ERR_OUT_OF_MEMORY, "zg_index_build: cudaHostAlloc of a staging buffer")
+                                              : cuda_fail(e, "zg_index_build: cudaHostAlloc of a staging buffer");
       }
       e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
       if (e != cudaSuccess) {
@@ -412,7 +429,8 @@ zg_status build_impl(const int32_t* sids, int64_t n, int L, int V, const zg_buil
                        const uint8_t* src_pay, uint64_t n_pay) -> zg_status {
     if (!dev) return ZG_OK;
     cudaError_t e = cudaSuccess;
-    if (n_rp) e = cudaMemcpyAsync(idx->dev + dst_rp, src_rp, n_rp, cudaMemcpyHostToDevice, stream);
+    if (injected(ZG_INJECT_COPY)) e = cudaErrorUnknown;
+    if (e == cudaSuccess && n_rp) e = cudaMemcpyAsync(idx->dev + dst_rp, src_rp, n_rp, cudaMemcpyHostToDevice, stream);
     if (e == cudaSuccess && n_pay)
       e = cudaMemcpyAsync(idx->dev + dst_pay, src_pay, n_pay, cudaMemcpyHostToDevice, stream);
     if (e == cudaSuccess) e = cudaEventRecord(ev[cur], stream);
@@ -562,6 +580,11 @@ zg_status zg_index_build(const int32_t* sids, int64_t n, int32_t L, int32_t V, c
   } catch (const std::exception& e) {
     return fail(ZG_ERR_INVALID_ARG, std::string("zg_index_build: ") + e.what());
   }
+}
+
+void zg_debug_inject_build_failure(int32_t point, int32_t after) {
+  g_inject_after.store(after < 0 ? 0 : after);
+  g_inject_point.store(point);
 }
 
 zg_status zg_index_stats(const zg_index* idx, int32_t step, zg_step_stats* out) {

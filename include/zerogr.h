@@ -211,6 +211,15 @@ ZG_API zg_status zg_plan_describe(const zg_plan* plan, uint8_t* variant, float* 
  * Changes the workspace size: size the workspace after setting the order.
  * ZG_ERR_INVALID_ARG for another value. */
 ZG_API zg_status zg_plan_set_order(zg_plan* plan, int32_t order);
+/* Save / load a plan ([Speed]: the variant chosen per step on warm-up
+ * requests is kept until the next model update, so a serving process can
+ * reuse a tuned plan across restarts).  The file holds the steps, batch,
+ * beam, order, fusion, the per-step variants and the tuner's timings, and a
+ * 64-bit FNV-1a checksum.  zg_plan_load returns ZG_ERR_IO for a missing,
+ * short, corrupt or foreign file, or one whose fields are out of range; the
+ * new plan is owned by the caller (zg_plan_free). */
+ZG_API zg_status zg_plan_save(const zg_plan* plan, const char* path);
+ZG_API zg_status zg_plan_load(const char* path, zg_plan** out);
 ZG_API void zg_plan_free(zg_plan* plan);
 
 /* --------------------------------------------------------------- decode ---
@@ -332,6 +341,16 @@ ZG_API size_t zg_static_scratch_bytes(void);
  * launches issued after the call, process-wide.  A limit too small for the
  * work makes decodes fail with ZG_ERR_DEVICE_STATUS. */
 ZG_API void zg_debug_set_wait_limit(uint32_t polls);
+
+/* Test hook, no counterpart in the paper: makes the index builder's next
+ * pinned staging allocation (ZG_INJECT_PINNED_ALLOC) or host-to-device copy
+ * (ZG_INJECT_COPY) report a failure after `after` successful ones, once, so
+ * the error paths of zg_index_build (status, cleanup of the device image and
+ * staging buffers) can be exercised without a real failure.  point 0 disarms.
+ * Process-wide; only builds with ZG_RESIDENT_DEVICE stage or copy. */
+#define ZG_INJECT_PINNED_ALLOC 1
+#define ZG_INJECT_COPY 2
+ZG_API void zg_debug_inject_build_failure(int32_t point, int32_t after);
 
 /* Synchronises `stream`, then reports and clears the device status word that
  * kernels set instead of trapping (bit 0: row out of range, bit 1: token out

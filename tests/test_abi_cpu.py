@@ -288,3 +288,40 @@ def test_static_scratch_size_matches_header(zg):
     txt = open(os.path.join(ROOT, "include", "zerogr.h")).read()
     m = re.search(r"#define ZG_STATIC_SCRATCH_BYTES \((\d+)u << (\d+)\)", txt)
     assert m and zg._lib.ZG_STATIC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))
+
+
+def test_plan_save_load_roundtrip_and_damage(zg, tmp_path):
+    """[Speed]: the per-step choice is kept until the next model update; a
+    saved plan loads back identical, and short, corrupt or out-of-range files
+    are refused."""
+    sids = tiny_catalogue(3, 16, 300, 2)
+    idx = zg.zg_index_build(sids, 16, residency=zg.ZG_RESIDENT_HOST)
+    plan = zg.zg_plan_force(idx, 5, 8, [1, 0, 2])
+    zg.zg_plan_set_fusion(plan, 4)
+    zg.zg_plan_set_order(plan, zg.ZG_ORDER_SCORE_FIRST)
+    p = str(tmp_path / "p.zgplan")
+    zg.zg_plan_save(plan, p)
+    back = zg.zg_plan_load(p)
+    a, b = zg.zg_plan_describe(plan), zg.zg_plan_describe(back)
+    for x, y in zip(a, b):
+        assert np.array_equal(np.asarray(x), np.asarray(y))
+    raw = open(p, "rb").read()
+    for cut in range(0, len(raw)):                     # every truncation
+        open(p, "wb").write(raw[:cut])
+        with pytest.raises(zg.ZgError) as e:
+            zg.zg_plan_load(p)
+        assert e.value.status == 7
+    bad = bytearray(raw)
+    bad[20] ^= 0x40                                    # a flipped bit: checksum mismatch
+    open(p, "wb").write(bytes(bad))
+    with pytest.raises(zg.ZgError):
+        zg.zg_plan_load(p)
+    # a well-formed file with an invalid variant (checksum recomputed)
+    body = bytearray(raw[8:-8])
+    L = int.from_bytes(body[0:4], "little")
+    body[4 * 5 + 4 + 20] = 7                           # first variant byte
+    fixed = raw[:8] + bytes(body) + np.array([_fnv1a(bytes(body))], "<u8").tobytes()
+    open(p, "wb").write(fixed)
+    with pytest.raises(zg.ZgError):
+        zg.zg_plan_load(p)
+    assert L == 3

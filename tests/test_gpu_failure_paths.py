@@ -1,4 +1,10 @@
-"""The tensor-core full projection's failure path: every mbarrier wait in the
+"""Failure paths exercised without a GPU fault.
+
+Index build: a host-side injection makes the builder's pinned staging
+allocation or a host-to-device copy report a failure; the build must return
+the status, release what it holds, and the next build must work.
+
+Tensor-core full projection: every mbarrier wait in the
 kernel is bounded; when one gives up, the kernel records the timeout bit in
 the device status word, drains its own copies and tensor-core operations,
 frees its tensor memory and returns, leaving the context usable.
@@ -60,3 +66,22 @@ def test_tensor_core_wait_expiry_is_reported_and_recovers(zg, dtype):
         trie = oracle.Trie(sids, L, V)
         ref = oracle.decode(trie, model, u, beam, K)
         check_topk(s.cpu().numpy(), sc.cpu().numpy(), ref, trie, model, u, 2e-2, 1e-4)
+
+
+@pytest.mark.parametrize("point,after,code", [(1, 0, 2), (1, 1, 2), (2, 0, 3), (2, 3, 3)])
+def test_index_build_injected_failure_and_recovery(zg, point, after, code):
+    V = 64
+    sids = tiny_catalogue(3, V, 3000, 4)
+    stream = torch.cuda.current_stream().cuda_stream
+    zg.zg_debug_inject_build_failure(point, after)
+    try:
+        with pytest.raises(zg.ZgError) as e:
+            zg.zg_index_build(sids, V, stream=stream, pinned_chunk_bytes=1 << 12)
+        assert e.value.status == code
+    finally:
+        zg.zg_debug_inject_build_failure(0, 0)
+    torch.cuda.synchronize()
+    idx = zg.zg_index_build(sids, V, stream=stream, pinned_chunk_bytes=1 << 12)
+    tabs = oracle.serialize_index(sids, 3, V)
+    for s in (1, 2, 3):
+        assert zg.zg_index_export(idx, s) == tabs[s - 1].export_bytes()
