@@ -25,6 +25,8 @@ ZG_SELECTIVE, ZG_FULL, ZG_NAIVE = 0, 1, 2
 ZG_RESIDENT_DEVICE, ZG_RESIDENT_HOST = 0, 1
 ZG_FORMAT_AUTO, ZG_FORMAT_ALL_SPARSE, ZG_FORMAT_ALL_DENSE = 0, 1, 2
 ZG_ORDER_FILTER_FIRST, ZG_ORDER_SCORE_FIRST = 0, 1
+ZG_HIDDEN_SPLIT, ZG_HIDDEN_SINGLE = 0, 1
+ZG_SCORES_AUTO, ZG_SCORES_WRITTEN, ZG_SCORES_CHUNK_TOPS = 0, 1, 2
 
 
 class ZgError(RuntimeError):
@@ -86,6 +88,7 @@ def _load():
         "zg_plan_describe": [vp, vp, vp, vp, vp],
         "zg_plan_set_fusion": [vp, i32],
         "zg_plan_set_order": [vp, i32],
+        "zg_plan_set_full_projection": [vp, i32, i32],
         "zg_decode_workspace_size": [vp, vp, P(zg_model), i32, i32, i32, P(sz)],
         "zg_decode": [vp, vp, P(zg_model), vp, i32, i32, i32, vp, vp, vp, sz, vp],
         "zg_decode_host_workspace_size": [vp, vp, P(zg_model), i32, i32, i32, P(sz)],
@@ -334,6 +337,12 @@ def zg_plan_set_order(plan: Plan, order: int):
     """ZG_ORDER_FILTER_FIRST (default) or ZG_ORDER_SCORE_FIRST (every step full,
     log-softmax over the whole codebook, then the mask)."""
     _check(lib.zg_plan_set_order(plan, int(order)))
+
+
+def zg_plan_set_full_projection(plan: Plan, hidden_rounding: int = ZG_HIDDEN_SPLIT, scores: int = ZG_SCORES_AUTO):
+    """How full steps run: the hidden as two half operands or one rounding;
+    scores written out or handed to the select as chunk tops (auto by size)."""
+    _check(lib.zg_plan_set_full_projection(plan, int(hidden_rounding), int(scores)))
 
 
 def zg_plan_set_fusion(plan: Plan, cluster_ctas):

@@ -40,10 +40,22 @@ struct Dims {
   int S_full;            // padded token stride of full scores
   int nch_sel[ZG_MAX_STEPS];
   int S_sel[ZG_MAX_STEPS];
+  bool tops[ZG_MAX_STEPS];   // a full step hands chunk tops (no written scores) to the select
+  bool split_h;              // half weights: the hidden as hi + lo operands
+  bool need_mask;            // per-beam legal bitmaps (score-first, or chunk tops on sparse tables)
+  bool sparse[ZG_MAX_STEPS]; // the step's table is sparse (constrained)
 };
 
+// Chunk tops on a full step when its beams hold at least 16 chunks per kept
+// candidate (then the chunk-maximum cut is selective and re-scores are rare).
+bool auto_tops(const Dims& m, int s) {
+  const int64_t Wc = (s == 1) ? 1 : m.beam;
+  const int64_t keep = (s < m.L) ? m.beam : m.K;
+  return Wc * (m.S_full / kChunk) >= 16 * keep;
+}
+
 struct WsLayout {
-  size_t tok_hist, par_hist, row[2], cum[2], h[2], hhi, hlo, Z, part, part_all, mask, naive_cnt, naive_off,
+  size_t tok_hist, par_hist, row[2], cum[2], h[2], hhi, hlo, Z, part, ptop, part_all, mask, naive_cnt, naive_off,
       naive_list, naive_temp, trace, u_stage, o_sids, o_scores, total;
   size_t trace_bytes;
 };
@@ -71,7 +83,7 @@ WsLayout layout(const Dims& m, bool host_io) {
   size_t zf = 0, pf = 0;
   for (int s = 1; s <= m.L; ++s) {
     const size_t N = (size_t)m.B * (s == 1 ? 1 : m.beam);
-    size_t S = m.S_full;
+    size_t S = m.tops[s - 1] ? 0 : m.S_full;       // full scores are written only without chunk tops
     pf = std::max(pf, N * (m.S_full / kChunk));  // full-projection chunk partials
     if (m.constrained) {
       S = std::max<size_t>(S, m.S_sel[s - 1]);
@@ -81,10 +93,9 @@ WsLayout layout(const Dims& m, bool host_io) {
   }
   w.Z = take(zf * 4);
   w.part = take(pf * 8);
-  if (m.score_first) {  // codebook-wide partials and per-beam token bitmaps
-    w.part_all = take(BW * (m.S_full / kChunk) * 8);
-    w.mask = take(BW * (size_t)((m.V + 31) / 32) * 4);
-  }
+  w.ptop = take(pf * 8);
+  if (m.score_first) w.part_all = take(BW * (m.S_full / kChunk) * 8);  // codebook-wide partials
+  if (m.need_mask) w.mask = take(BW * (size_t)((m.V + 31) / 32) * 4);  // per-beam token bitmaps
   if (m.naive_rows) {  // fan-outs, offsets, compact list, temporary matrix
     w.naive_cnt = take((BW + 1) * 4);
     w.naive_off = take((BW + 1) * 4);
@@ -146,7 +157,12 @@ zg_status check_common(const zg_index* idx, const zg_model* model, int B, int be
     d.nch_sel[s - 1] = nch;
     d.S_sel[s - 1] = nch * kChunk;
     d.nnz[s - 1] = idx ? (int64_t)idx->steps[s - 1].nnz : 0;
+    d.sparse[s - 1] = idx && idx->steps[s - 1].fmt == ZG_FMT_SPARSE;
   }
+  d.split_h = true;
+  for (int s = 1; s <= m.L; ++s) d.tops[s - 1] = auto_tops(d, s);
+  d.need_mask = false;
+  for (int s = 1; s <= m.L; ++s) d.need_mask = d.need_mask || (d.tops[s - 1] && d.sparse[s - 1]);
   *out = d;
   return ZG_OK;
 }
@@ -156,6 +172,13 @@ zg_status check_common(const zg_index* idx, const zg_model* model, int B, int be
 // candidates are at most min(beams * max_fanout, nnz) of the step).
 zg_status apply_plan(Dims& m, const zg_index* idx, const zg_plan* plan) {
   m.score_first = idx && plan && plan->order == ZG_ORDER_SCORE_FIRST;
+  if (plan) {
+    m.split_h = plan->hidden != ZG_HIDDEN_SINGLE;
+    for (int s = 1; s <= m.L; ++s)
+      m.tops[s - 1] = plan->scores == ZG_SCORES_CHUNK_TOPS || (plan->scores == ZG_SCORES_AUTO && auto_tops(m, s));
+  }
+  m.need_mask = m.score_first;
+  for (int s = 1; s <= m.L; ++s) m.need_mask = m.need_mask || (m.tops[s - 1] && m.sparse[s - 1]);
   m.naive_rows = 0;
   for (int s = 1; s <= m.L; ++s) {
     m.naive[s - 1] = idx && plan && !m.score_first && plan->variant[s - 1] == ZG_NAIVE;
@@ -270,15 +293,16 @@ StepLaunch make_launch(const Run& r, int s, int variant) {
     a.nch = m.nch_sel[s - 1];
     a.S = m.S_sel[s - 1];
     a.part = reinterpret_cast<float2*>(r.ws + r.w.part);
-  } else if (m.score_first && r.idx) {
-    // project every token, normalise over the codebook, mask, select: token
-    // slots on every step; sparse-format steps expand their legal lists into
-    // per-beam bitmap rows first
+  } else if ((m.score_first || m.tops[s - 1]) && r.idx) {
+    // token slots with a legal bitmap: the score-first order (project every
+    // token, normalise over the codebook, mask, select) and full steps that
+    // hand chunk tops to the select; sparse-format steps expand their legal
+    // lists into per-beam bitmap rows first
     a.mode = kFullDense;
     a.S = m.S_full;
     a.nch = m.S_full / kChunk;
     a.part = reinterpret_cast<float2*>(r.ws + r.w.part);
-    a.part_all = reinterpret_cast<const float2*>(r.ws + r.w.part_all);
+    if (m.score_first) a.part_all = reinterpret_cast<const float2*>(r.ws + r.w.part_all);
     if (r.idx->steps[s - 1].fmt == ZG_FMT_SPARSE) {
       a.mask_by_beam = 1;
       a.tab.bitmap = U32(r.w.mask);
@@ -297,6 +321,18 @@ StepLaunch make_launch(const Run& r, int s, int variant) {
   }
   a.zq = (int64_t)a.Wc * a.S;      // contiguous beam rows (the full projection's layout)
   a.pq = (int64_t)a.Wc * a.nch;
+  if (full && m.tops[s - 1]) {
+    // no scores written: the select works from the chunk tops and re-scores
+    // from the projection's own operands
+    a.ptop = reinterpret_cast<const float2*>(r.ws + r.w.ptop);
+    a.Z = nullptr;
+    const float* H = (s >= 2) ? a.h_out : r.u;
+    a.hq = H;
+    if (m.w_dtype != ZG_F32) {
+      a.hq_hi = r.ws + r.w.hhi;
+      a.hq_lo = m.split_h ? r.ws + r.w.hlo : nullptr;
+    }
+  }
   return a;
 }
 
@@ -332,12 +368,14 @@ zg_status run_step(const Run& r, int s, int variant, cudaStream_t st, const Step
       H = a.h_out;
     }
     const int M = a.B * a.Wc;
+    void* hlo = r.m.split_h ? r.ws + r.w.hlo : nullptr;  // none: a single rounding of the hidden
     if (a.w_dtype != ZG_F32) {
-      e = launch_split_h(H, r.ws + r.w.hhi, r.ws + r.w.hlo, (size_t)M * a.d, a.w_dtype, st);
+      e = launch_split_h(H, r.ws + r.w.hhi, hlo, (size_t)M * a.d, a.w_dtype, st);
       if (e != cudaSuccess) return cuda_fail(e, "hidden split launch");
     }
     FullEpi epi{};
     epi.part = a.part;
+    epi.ptop = const_cast<float2*>(a.ptop);
     epi.part_all = const_cast<float2*>(a.part_all);
     if (a.mode == kFullDense) {
       epi.bitmap = a.tab.bitmap;
@@ -354,7 +392,7 @@ zg_status run_step(const Run& r, int s, int variant, cudaStream_t st, const Step
     }
     if (tm) cudaEventRecord(tm->ev[1], st);
     if (a.w_dtype != ZG_F32)
-      e = launch_full_tc(r.ws + r.w.hhi, r.ws + r.w.hlo, a.W, a.Z, M, a.V, a.d, a.S, a.w_dtype, epi, a.status, st);
+      e = launch_full_tc(r.ws + r.w.hhi, hlo, a.W, a.Z, M, a.V, a.d, a.S, a.w_dtype, epi, a.status, st);
     else
       e = launch_full_simt(a, H, epi, st);
     if (e != cudaSuccess) return cuda_fail(e, "full projection launch");
@@ -571,7 +609,7 @@ void zg_plan_free(zg_plan* plan) { delete plan; }
 }  // extern "C"
 
 namespace {
-const char kPlanMagic[8] = {'Z', 'G', 'P', 'L', 'A', 'N', 0, 1};
+const char kPlanMagic[8] = {'Z', 'G', 'P', 'L', 'A', 'N', 0, 2};
 
 uint64_t plan_fnv1a(const std::vector<uint8_t>& b) {
   uint64_t h = 1469598103934665603ull;
@@ -607,6 +645,8 @@ zg_status zg_plan_save(const zg_plan* plan, const char* path) {
   put(body, plan->beam);
   put(body, plan->fused);
   put(body, plan->order);
+  put(body, plan->hidden);
+  put(body, plan->scores);
   put(body, plan->plan_ms);
   for (float x : plan->fused_ms) put(body, x);
   for (uint8_t v : plan->variant) put(body, v);
@@ -640,10 +680,13 @@ zg_status zg_plan_load(const char* path, zg_plan** out) {
   auto p = std::make_unique<zg_plan>();
   size_t at = 0;
   bool ok = get(body, at, &p->L) && get(body, at, &p->B) && get(body, at, &p->beam) && get(body, at, &p->fused) &&
-            get(body, at, &p->order) && get(body, at, &p->plan_ms);
+            get(body, at, &p->order) && get(body, at, &p->hidden) && get(body, at, &p->scores) &&
+            get(body, at, &p->plan_ms);
   for (float& x : p->fused_ms) ok = ok && get(body, at, &x);
   ok = ok && p->L >= 1 && p->L <= ZG_MAX_STEPS && p->B >= 1 && p->beam >= 1 && p->beam <= ZG_MAX_BEAM &&
        (p->order == ZG_ORDER_FILTER_FIRST || p->order == ZG_ORDER_SCORE_FIRST) &&
+       (p->hidden == ZG_HIDDEN_SPLIT || p->hidden == ZG_HIDDEN_SINGLE) &&
+       (p->scores == ZG_SCORES_AUTO || p->scores == ZG_SCORES_WRITTEN || p->scores == ZG_SCORES_CHUNK_TOPS) &&
        (p->fused == 0 || p->fused == 1 || p->fused == 2 || p->fused == 4 || p->fused == 8 || p->fused == 16);
   if (ok) {
     p->variant.resize(p->L);
@@ -662,6 +705,17 @@ zg_status zg_plan_set_fusion(zg_plan* plan, int32_t cluster_ctas) {
       cluster_ctas != 16)
     return fail(ZG_ERR_INVALID_ARG, "zg_plan_set_fusion: cluster_ctas must be 0, 1, 2, 4, 8 or 16");
   plan->fused = cluster_ctas;
+  return ZG_OK;
+}
+
+zg_status zg_plan_set_full_projection(zg_plan* plan, int32_t hidden_rounding, int32_t scores) {
+  if (!plan) return fail(ZG_ERR_INVALID_ARG, "zg_plan_set_full_projection: plan is NULL");
+  if (hidden_rounding != ZG_HIDDEN_SPLIT && hidden_rounding != ZG_HIDDEN_SINGLE)
+    return fail(ZG_ERR_INVALID_ARG, "zg_plan_set_full_projection: hidden_rounding must be ZG_HIDDEN_SPLIT or ZG_HIDDEN_SINGLE");
+  if (scores != ZG_SCORES_AUTO && scores != ZG_SCORES_WRITTEN && scores != ZG_SCORES_CHUNK_TOPS)
+    return fail(ZG_ERR_INVALID_ARG, "zg_plan_set_full_projection: scores must be ZG_SCORES_AUTO, _WRITTEN or _CHUNK_TOPS");
+  plan->hidden = hidden_rounding;
+  plan->scores = scores;
   return ZG_OK;
 }
 
@@ -965,6 +1019,7 @@ zg_status zg_check_device_status(void* stream) {
   if (v & kStatusToken) msg += " token out of range;";
   if (v & kStatusTimeout) msg += " tensor-core wait expired;";
   if (v & kStatusTmem) msg += " tensor-memory allocation failed;";
+  if (v & kStatusSelect) msg += " select found fewer candidates than its cut;";
   return fail(ZG_ERR_DEVICE_STATUS, msg);
 }
 

@@ -297,30 +297,53 @@ __global__ void __launch_bounds__(256) k_full_simt(const float* __restrict__ H, 
     }
     __syncthreads();
   }
+  if (Z) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int m = m0 + ty * 4 + i;
-    if (m >= M) continue;
+    for (int i = 0; i < 4; ++i) {
+      const int m = m0 + ty * 4 + i;
+      if (m >= M) continue;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int n = n0 + tx * 4 + j;
-      if (n < V) Z[(size_t)m * ldz + n] = acc[i][j];
+      for (int j = 0; j < 4; ++j) {
+        const int n = n0 + tx * 4 + j;
+        if (n < V) Z[(size_t)m * ldz + n] = acc[i][j];
+      }
     }
   }
   if (epi.part) {
     // legal-only (max, sum exp) of each 32-token chunk: 8 threads (4 tokens
-    // each) share a chunk; lanes tx^1, tx^2, tx^4 hold its other tokens
+    // each) share a chunk; lanes tx^1, tx^2, tx^4 hold its other tokens.
+    // With ptop also the chunk's second-largest legal z and the offset of
+    // the lowest token holding its largest.
     const int chunk = (n0 >> 5) + (tx >> 3);
     const int sh = (tx & 7) * 4;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int m = m0 + ty * 4 + i;
       const uint32_t lm = (m < M) ? (epi_legal_mask(epi, m, chunk, V) >> sh) & 0xFu : 0u;
-      float mx = -INFINITY;
+      float mx = -INFINITY, m2 = -INFINITY;
+      int arg = 0;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) mx = ((lm >> j) & 1u) ? fmaxf(mx, acc[i][j]) : mx;
+      for (int j = 0; j < 4; ++j) {
+        const bool l = (lm >> j) & 1u;
+        if (l && acc[i][j] > mx) {
+          m2 = mx;
+          mx = acc[i][j];
+          arg = sh + j;
+        } else if (l && acc[i][j] > m2) {
+          m2 = acc[i][j];
+        }
+      }
 #pragma unroll
-      for (int o = 1; o < 8; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+      for (int o = 1; o < 8; o <<= 1) {  // merge (largest, lowest offset, second) pairs
+        const float omx = __shfl_xor_sync(0xFFFFFFFFu, mx, o);
+        const float om2 = __shfl_xor_sync(0xFFFFFFFFu, m2, o);
+        const int oarg = __shfl_xor_sync(0xFFFFFFFFu, arg, o);
+        const bool mine = (mx > omx) || (mx == omx && arg < oarg);
+        const float lose = mine ? omx : mx;
+        m2 = fmaxf(fmaxf(m2, om2), lose);
+        arg = mine ? arg : oarg;
+        mx = mine ? mx : omx;
+      }
       float sm = 0.f;
       if (mx != -INFINITY) {
 #pragma unroll
@@ -328,7 +351,11 @@ __global__ void __launch_bounds__(256) k_full_simt(const float* __restrict__ H, 
       }
 #pragma unroll
       for (int o = 1; o < 8; o <<= 1) sm += __shfl_xor_sync(0xFFFFFFFFu, sm, o);
-      if ((tx & 7) == 0 && m < M && chunk * 32 < V) epi.part[(size_t)m * (ldz >> 5) + chunk] = make_float2(mx, sm);
+      if ((tx & 7) == 0 && m < M && chunk * 32 < V) {
+        const size_t pi = (size_t)m * (ldz >> 5) + chunk;
+        epi.part[pi] = make_float2(mx, sm);
+        if (epi.ptop) epi.ptop[pi] = make_float2(m2, __int_as_float(arg));
+      }
     }
   }
   if (epi.part_all) {
@@ -374,6 +401,15 @@ __global__ void __launch_bounds__(kSelThreads) k_select(const __grid_constant__ 
   beam_lse<kSelThreads>(a, q, bt, (!staged && !a.part && a.Wc * rt <= kSelCap / 2) ? keys : nullptr, rt, tw);
   __syncthreads();
   const int ni = bt.istart[a.Wc];
+  if (a.ptop) {  // the scores were never written: chunk-top select
+    int n = cta_select_tops<kSelThreads>(a, q, bt, sw);
+    if (n < 0) {
+      if (threadIdx.x == 0) flag(a.status, kStatusSelect);  // unreachable: the cut's own maxima are listed
+      n = 0;
+    }
+    write_survivors<kSelThreads>(a, q, bt, sw, n);
+    return;
+  }
   int n = (a.part && 2 * ni <= kSelCap)
               ? cta_select_chunks<kSelThreads, false>(a, q, bt, sw, nullptr, nullptr, keys, keys + ni, 1) : -1;
   if (n < 0) {

@@ -36,11 +36,24 @@ namespace zg {
 namespace {
 
 constexpr int kBM = 128, kBN = 256, kBK = 64;  // tile; kBK bf16 = 128 bytes = one swizzle row
-constexpr int kStages = 3;
 constexpr int kTileA = kBM * kBK * 2;          // 16 KiB
 constexpr int kTileB = kBN * kBK * 2;          // 32 KiB
-constexpr int kStageBytes = 2 * kTileA + kTileB;
 constexpr int kTmemCols = 256;
+constexpr int kStagingBytes = 8 * 4096;        // one 4 KiB store block per epilogue warp
+
+// Shared-memory layout of one variant: SPLIT = the hidden as two half
+// operands (two MMAs per K-step), else one (a single rounding of the hidden);
+// ZSTORE = the scores are written out through staging blocks by TMA stores,
+// else only the epilogue's per-chunk summaries leave the SM.
+template <bool SPLIT, bool ZSTORE>
+struct TcCfg {
+  static constexpr int kA = SPLIT ? 2 : 1;                    // A operands a stage
+  static constexpr int kStageBytes = kA * kTileA + kTileB;    // 64 or 48 KiB
+  static constexpr int kStaging = ZSTORE ? kStagingBytes : 0;
+  static constexpr int kStages = (227 * 1024 - 1024 - kStaging) / kStageBytes;  // 3 or 4
+  static constexpr size_t kSmem = (size_t)kStages * kStageBytes + kStaging + 1024;
+  static_assert(kStages >= 3, "a ring of three stages at least");
+};
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer, MMA issuer, epilogue warps
 constexpr uint32_t kSpinLimit = 1u << 26;  // default polls of a wait (seconds at most)
@@ -136,14 +149,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+template <bool SPLIT, bool ZSTORE>
 __global__ void __launch_bounds__(kThreads, 1)
     k_full_tc(const __grid_constant__ CUtensorMap map_hi, const __grid_constant__ CUtensorMap map_lo,
               const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_z, int M, int V,
               int d, int ldz, uint32_t ab_type, const FullEpi epi, uint32_t* status, uint32_t spin) {
+  using Cfg = TcCfg<SPLIT, ZSTORE>;
+  constexpr int kStages = Cfg::kStages;
+  constexpr int kStageBytes = Cfg::kStageBytes;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // stage buffers must sit on 1024-byte boundaries (swizzle atoms)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* staging = smem + kStages * kStageBytes;  // one 4 KiB block per epilogue warp
+  uint8_t* staging = smem + kStages * kStageBytes;  // one 4 KiB block per epilogue warp (ZSTORE)
   __shared__ uint64_t full_bar[kStages], empty_bar[kStages], tfull_bar[2], tempty_bar[2], drain_bar;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
@@ -190,11 +207,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         uint8_t* sa_hi = smem + st * kStageBytes;
-        uint8_t* sa_lo = sa_hi + kTileA;
-        uint8_t* sb = sa_lo + kTileA;
+        uint8_t* sb = sa_hi + Cfg::kA * kTileA;
         mbar_expect_tx(&full_bar[st], kStageBytes);
         tma_load_2d(sa_hi, &map_hi, &full_bar[st], kb * kBK, m0);
-        tma_load_2d(sa_lo, &map_lo, &full_bar[st], kb * kBK, m0);
+        if constexpr (SPLIT) tma_load_2d(sa_hi + kTileA, &map_lo, &full_bar[st], kb * kBK, m0);
         tma_load_2d(sb, &map_w, &full_bar[st], kb * kBK, n0);
       }
     }
@@ -226,13 +242,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint8_t* sa_hi = smem + st * kStageBytes;
-        const uint8_t* sa_lo = sa_hi + kTileA;
-        const uint8_t* sb = sa_lo + kTileA;
+        const uint8_t* sb = sa_hi + Cfg::kA * kTileA;
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk) {
           const uint64_t bd = smem_desc(sb + kk * 32);
           mma_f16(acc, smem_desc(sa_hi + kk * 32), bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-          mma_f16(acc, smem_desc(sa_lo + kk * 32), bd, idesc, 1u);
+          if constexpr (SPLIT) mma_f16(acc, smem_desc(sa_hi + kTileA + kk * 32), bd, idesc, 1u);
         }
         mma_commit(&empty_bar[st]);  // stage free once these MMAs have read it
       }
@@ -297,17 +312,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t vm = rem >= 32 ? 0xFFFFFFFFu : ((1u << rem) - 1u);
         if (row < M && epi.part) {
           // legal-only (max, sum exp) of this 32-token chunk (the fast
-          // exponential: ~1e-6 relative, far inside the score tolerance)
+          // exponential: ~1e-6 relative, far inside the score tolerance);
+          // with ptop also the second-largest legal z and the lowest token
+          // offset holding the largest
           const uint32_t lm = dead ? 0u : (lmw[ci] & vm);
-          float mx = -INFINITY;
+          float mx = -INFINITY, m2 = -INFINITY;
+          int arg = 0;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) mx = ((lm >> j) & 1u) ? fmaxf(mx, v[j]) : mx;
+          for (int j = 0; j < 32; ++j) {
+            const bool l = (lm >> j) & 1u;
+            const float x = v[j];
+            if (l && x > mx) {
+              m2 = mx;
+              mx = x;
+              arg = j;
+            } else if (l && x > m2) {
+              m2 = x;
+            }
+          }
           float sm = 0.f;
           if (mx != -INFINITY) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) sm += ((lm >> j) & 1u) ? __expf(v[j] - mx) : 0.f;
           }
-          epi.part[(size_t)row * (ldz >> 5) + chunk] = make_float2(mx, sm);
+          const size_t pi = (size_t)row * (ldz >> 5) + chunk;
+          epi.part[pi] = make_float2(mx, sm);
+          if (epi.ptop) epi.ptop[pi] = make_float2(m2, __int_as_float(arg));
         }
         if (row < M && epi.part_all) {
           // (max, sum exp) over every token of the chunk (score-first normaliser)
@@ -319,30 +349,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 32; ++j) sm += ((vm >> j) & 1u) ? __expf(v[j] - mx) : 0.f;
           epi.part_all[(size_t)row * (ldz >> 5) + chunk] = make_float2(mx, sm);
         }
-        // stage the 32 x 32 block (row = lane; 16-byte piece j of a row at
-        // j ^ (row & 7): the 128-byte swizzle of the store map), then store
-        if (issued > 0) {
-          if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-          __syncwarp();
-        }
+        if constexpr (ZSTORE) {
+          // stage the 32 x 32 block (row = lane; 16-byte piece j of a row at
+          // j ^ (row & 7): the 128-byte swizzle of the store map), then store
+          if (issued > 0) {
+            if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+            __syncwarp();
+          }
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          *reinterpret_cast<float4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
-              make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_2d(&map_z, buf, n0 + c0, m0 + quarter * 32);
-          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<float4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&map_z, buf, n0 + c0, m0 + quarter * 32);
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+          }
+          ++issued;
         }
-        ++issued;
       }
       // this warp's part of accumulator b is read: let the MMA issuer reuse it
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       __syncwarp();
       if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&tempty_bar[b])) : "memory");
     }
-    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+    if constexpr (ZSTORE) {
+      if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+    }
     __syncwarp();
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -382,7 +416,7 @@ __global__ void __launch_bounds__(256) k_split_h(const float* __restrict__ H, HT
     const float x = H[i];
     const HT h = to_half<HT>(x);
     hi[i] = h;
-    lo[i] = to_half<HT>(x - from_half<HT>(h));
+    if (lo) lo[i] = to_half<HT>(x - from_half<HT>(h));  // no lo: a single rounding of the hidden
   }
 }
 
@@ -420,8 +454,6 @@ std::atomic<uint32_t> g_wait_limit{kSpinLimit};
 
 }  // namespace
 
-size_t full_tc_smem_bytes() { return (size_t)kStages * kStageBytes + kEpiWarps * 4096 + 1024; }
-
 cudaError_t launch_split_h(const float* H, void* hi, void* lo, size_t n, int w_dtype, cudaStream_t st) {
   const int blocks = (int)std::min<size_t>((n + 255) / 256, 4096);
   if (w_dtype == ZG_BF16)
@@ -431,6 +463,8 @@ cudaError_t launch_split_h(const float* H, void* hi, void* lo, size_t n, int w_d
     k_split_h<__half><<<blocks, 256, 0, st>>>(H, static_cast<__half*>(hi), static_cast<__half*>(lo), n);
   return cudaGetLastError();
 }
+
+namespace {
 
 // Store map of the scores: fp32 [rows][ldz], 32 x 32 boxes, 128B swizzle.
 bool make_store_map(CUtensorMap* m, float* Z, int rows, int ldz) {
@@ -445,26 +479,45 @@ bool make_store_map(CUtensorMap* m, float* Z, int rows, int ldz) {
   return r == CUDA_SUCCESS;
 }
 
-cudaError_t launch_full_tc(const void* hi, const void* lo, const void* W, float* Z, int M, int V, int d, int ldz,
-                           int w_dtype, const FullEpi& epi, uint32_t* status, cudaStream_t st) {
-  const bool bf16 = (w_dtype == ZG_BF16);
-  CUtensorMap mh, ml, mw, mz;
-  if (ldz % 32 != 0 || !make_map(&mh, hi, M, d, kBM, bf16) || !make_map(&ml, lo, M, d, kBM, bf16) ||
-      !make_map(&mw, W, V, d, kBN, bf16) || !make_store_map(&mz, Z, M, ldz))
-    return cudaErrorInvalidValue;
-  static bool attr_done = false;
-  const size_t smem = full_tc_smem_bytes();
+template <bool SPLIT, bool ZSTORE>
+cudaError_t launch_tc_t(const CUtensorMap& mh, const CUtensorMap& ml, const CUtensorMap& mw, const CUtensorMap& mz,
+                        int M, int V, int d, int ldz, bool bf16, const FullEpi& epi, uint32_t* status,
+                        cudaStream_t st) {
+  auto kern = k_full_tc<SPLIT, ZSTORE>;
+  constexpr size_t smem = TcCfg<SPLIT, ZSTORE>::kSmem;
+  static bool attr_done = false;  // per instantiation
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(k_full_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
   // persistent: one CTA per SM (shared memory admits one), tiles strided over the CTAs
   const int ntiles = ((V + kBN - 1) / kBN) * ((M + kBM - 1) / kBM);
   const int grid = std::max(1, std::min(ntiles, sm_count()));
-  k_full_tc<<<grid, kThreads, smem, st>>>(mh, ml, mw, mz, M, V, d, ldz, bf16 ? 1u : 0u, epi, status,
-                                          g_wait_limit.load(std::memory_order_relaxed));
+  kern<<<grid, kThreads, smem, st>>>(mh, ml, mw, mz, M, V, d, ldz, bf16 ? 1u : 0u, epi, status,
+                                     g_wait_limit.load(std::memory_order_relaxed));
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_full_tc(const void* hi, const void* lo, const void* W, float* Z, int M, int V, int d, int ldz,
+                           int w_dtype, const FullEpi& epi, uint32_t* status, cudaStream_t st) {
+  const bool bf16 = (w_dtype == ZG_BF16);
+  const bool split = (lo != nullptr);   // the hidden as hi + lo halves, else one rounding (hi)
+  const bool zstore = (Z != nullptr);   // scores written out, else only the chunk summaries
+  CUtensorMap mh, ml, mw, mz;
+  if (ldz % 32 != 0 || !make_map(&mh, hi, M, d, kBM, bf16) || (split && !make_map(&ml, lo, M, d, kBM, bf16)) ||
+      !make_map(&mw, W, V, d, kBN, bf16) || (zstore && !make_store_map(&mz, Z, M, ldz)))
+    return cudaErrorInvalidValue;
+  if (!zstore && !(epi.part && epi.ptop)) return cudaErrorInvalidValue;  // nothing would leave the kernel
+  if (!split) ml = mh;
+  if (!zstore) mz = mh;  // unused
+  if (split)
+    return zstore ? launch_tc_t<true, true>(mh, ml, mw, mz, M, V, d, ldz, bf16, epi, status, st)
+                  : launch_tc_t<true, false>(mh, ml, mw, mz, M, V, d, ldz, bf16, epi, status, st);
+  return zstore ? launch_tc_t<false, true>(mh, ml, mw, mz, M, V, d, ldz, bf16, epi, status, st)
+                : launch_tc_t<false, false>(mh, ml, mw, mz, M, V, d, ldz, bf16, epi, status, st);
 }
 
 void set_wait_limit(uint32_t polls) { g_wait_limit.store(polls ? polls : kSpinLimit, std::memory_order_relaxed); }

@@ -1367,6 +1367,249 @@ __device__ int cta_select_chunks(const StepLaunch& a, int q, BeamTab& bt, SW& sw
   return keep_n;
 }
 
+// ---------------------------------------------------------------------------
+// Chunk-top select: full steps whose scores were never written.  The full
+// projection's epilogue left, per 32-token chunk of every beam row, the
+// legal-only partial (max, sum exp) and the chunk's second-largest legal z
+// with the offset of the lowest token holding the largest (a.ptop).
+//
+// Within one chunk all candidates share the beam's cumulative score and
+// log-sum-exp, so their order is the order of z.  Let tc be the keep-th
+// largest chunk-maximum key: at least keep candidates (those maxima) reach
+// tc, so every winner does.  A chunk whose second-largest is below the cut
+// holds at most one candidate above it, its maximum; only chunks whose second
+// also clears the cut are re-scored token by token, from the same operands
+// the projection used.  Re-scored values may differ from the projection's by
+// rounding, so the cut is lowered by a margin (kTopMargin on the score): every
+// candidate left out is then below the keep-th largest listed.
+// Candidates at or above the lowered cut are listed as (key << 32 | ~flat)
+// and placed; when the list overflows, 2,048-bin histograms over the same
+// implicit candidate set narrow the cut (at most three rounds, to one key
+// value), and ties at that key go to the lowest flat slots by an ordered walk.
+// Exact for any data; deterministic (a re-score is recomputed identically).
+// ---------------------------------------------------------------------------
+constexpr float kTopMargin = 1e-4f;
+
+// Sequential dot W_s[t] . h_b with the full projection's operands.  For fp32
+// weights the order of accumulation is the SIMT projection's (one fused
+// multiply-add per element, ascending), so the value is bit-identical to it.
+template <typename WT>
+__device__ __forceinline__ float rescore_token(const StepLaunch& a, size_t b, int t) {
+  const WT* w = static_cast<const WT*>(a.W) + (size_t)t * a.d;
+  float z = 0.f;
+  if constexpr (sizeof(WT) == 4) {
+    const float4* h4 = reinterpret_cast<const float4*>(a.hq + b * a.d);
+    const float4* w4 = reinterpret_cast<const float4*>(w);
+    for (int e = 0; e < a.d / 4; ++e) {
+      const float4 h = h4[e], x = w4[e];
+      z = fmaf(h.x, x.x, z);
+      z = fmaf(h.y, x.y, z);
+      z = fmaf(h.z, x.z, z);
+      z = fmaf(h.w, x.w, z);
+    }
+  } else {
+    const uint4* hh = reinterpret_cast<const uint4*>(static_cast<const WT*>(a.hq_hi) + b * a.d);
+    const uint4* hl = a.hq_lo ? reinterpret_cast<const uint4*>(static_cast<const WT*>(a.hq_lo) + b * a.d) : nullptr;
+    const uint4* w8 = reinterpret_cast<const uint4*>(w);
+    for (int e = 0; e < a.d / 8; ++e) {
+      float wf[8], hf[8], lf[8];
+      Vec<WT>::cvt(w8[e], wf);
+      Vec<WT>::cvt(hh[e], hf);
+      if (hl) Vec<WT>::cvt(hl[e], lf);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        z = fmaf(hf[i], wf[i], z);
+        if (hl) z = fmaf(lf[i], wf[i], z);
+      }
+    }
+  }
+  return z;
+}
+
+__device__ __forceinline__ float rescore(const StepLaunch& a, size_t b, int t) {
+  switch (a.w_dtype) {
+    case ZG_F32:
+      return rescore_token<float>(a, b, t);
+    case ZG_BF16:
+      return rescore_token<__nv_bfloat16>(a, b, t);
+    default:
+      return rescore_token<__half>(a, b, t);
+  }
+}
+
+// Key of score s lowered by the re-score margin (0 stays 0).
+__device__ __forceinline__ uint32_t key_lowered(uint32_t k) {
+  if (!k) return 0u;
+  const float s = ord2f(k);
+  const uint32_t lk = f2ord(s - kTopMargin * (1.f + fabsf(s)));
+  return lk ? lk : 1u;
+}
+
+// Candidates of chunk item i (beam k, chunk c) at or above tmin, one a lane:
+// lane j's (key, flat) for token 32c + j (key 0: none).  Warp-wide.
+__device__ __forceinline__ uint32_t chunk_top_cands(const StepLaunch& a, const BeamTab& bt, int q, int k, int c,
+                                                    uint32_t tmin, int lane, int* flat) {
+  const size_t pi = (size_t)q * a.pq + (size_t)k * a.nch + c;
+  const float2 p = a.part[pi];
+  const float2 t2 = a.ptop[pi];
+  *flat = bt.start[k] + c * kChunk + lane;
+  if (!(p.y > 0.f)) return 0u;
+  const float cum = bt.cum[k], lse = bt.lse[k];
+  const uint32_t k1 = f2ord(cum + (p.x - lse));
+  if (k1 < tmin) return 0u;
+  const uint32_t k2 = (t2.x != -INFINITY) ? f2ord(cum + (t2.x - lse)) : 0u;
+  if (k2 < tmin) return (lane == __float_as_int(t2.y)) ? k1 : 0u;  // only the maximum can clear the cut
+  // re-score the chunk: every legal token at or above the cut
+  const int t = c * kChunk + lane;
+  bool legal = t < a.V;
+  if (legal && a.mode != kUncon) legal = (legal_bits(a, bt, q, k)[c] >> lane) & 1u;
+  if (!legal) return 0u;
+  const float z = rescore(a, (size_t)q * a.Wc + k, t);
+  const uint32_t kz = f2ord(cum + (z - lse));
+  return kz >= tmin ? kz : 0u;
+}
+
+template <int NT, typename SW>
+__device__ int cta_select_tops(const StepLaunch& a, int q, BeamTab& bt, SW& sw) {
+  constexpr int NW = NT / 32;
+  constexpr int LCAP = NW * 256 / 2;
+  static_assert(NW * 256 >= kBins, "histogram space");
+  uint32_t* hist = &sw.whist[0][0];
+  unsigned long long* list = reinterpret_cast<unsigned long long*>(hist);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int keep_n = min(a.keep, bt.nlegal);
+  if (keep_n == 0) return 0;
+  const int nitems = bt.istart[a.Wc];
+  for (int i = tid; i < kBins; i += NT) hist[i] = 0u;
+  __syncthreads();  // publishes the lse and the chunk-maximum key range of beam_lse_sel
+  // 1. cut tc on the chunk maxima (their keys counted over [kfloor, kceil])
+  uint32_t tmin = 1u;
+  if (bt.nne >= keep_n && bt.kfloor <= bt.kceil) {
+    const uint32_t lo = bt.kfloor, hi = bt.kceil;
+    const int sh = bin_shift(lo, hi);
+    for (int i = tid; i < nitems; i += NT) {
+      const int k = upper_find(bt.istart, a.Wc, i);
+      const float2 p = a.part[(size_t)q * a.pq + (size_t)k * a.nch + (i - bt.istart[k])];
+      if (p.y > 0.f) {
+        const uint32_t ck = f2ord(bt.cum[k] + (p.x - bt.lse[k]));
+        if (ck >= lo) atomicAdd(&hist[bin_of(ck, lo, sh)], 1u);
+      }
+    }
+    __syncthreads();
+    if (hist_cut<NT>(hist, sw, (uint32_t)keep_n) >= (uint32_t)keep_n) tmin = key_lowered(lo + (sw.prefix << sh));
+    __syncthreads();
+  }
+  // every pass visits the chunks whose maximum reaches tmin: each lane tests
+  // one chunk, the warp then takes the passing ones in turn
+  auto for_chunks = [&](auto&& body) {
+    for (int i0 = 0; i0 < nitems; i0 += NT) {
+      const int ic = i0 + lane * NW + warp;
+      int kl = 0;
+      bool pass = false;
+      if (ic < nitems) {
+        kl = upper_find(bt.istart, a.Wc, ic);
+        const float2 p = a.part[(size_t)q * a.pq + (size_t)kl * a.nch + (ic - bt.istart[kl])];
+        pass = (p.y > 0.f) && f2ord(bt.cum[kl] + (p.x - bt.lse[kl])) >= tmin;
+      }
+      unsigned bal = __ballot_sync(kFull, pass);
+      while (bal) {
+        const int src = __ffs(bal) - 1;
+        bal &= bal - 1u;
+        const int k = __shfl_sync(kFull, kl, src);
+        const int c = i0 + src * NW + warp - bt.istart[k];
+        int flat;
+        const uint32_t key = chunk_top_cands(a, bt, q, k, c, tmin, lane, &flat);
+        body(key, flat);
+      }
+    }
+  };
+  // 2. list every candidate at or above tmin
+  if (tid == 0) sw.nwin = 0;
+  __syncthreads();
+  for_chunks([&](uint32_t key, int flat) { warp_append(list, LCAP, sw.nwin, key != 0u, key, flat, lane); });
+  __syncthreads();
+  int nl = sw.nwin;
+  if (nl < keep_n) return -1;  // cannot happen (the keep chunk maxima are listed); caller flags it
+  if (nl <= LCAP) {
+    place_winners<NT>(list, nl, keep_n, sw);
+    return keep_n;
+  }
+  // 3. overflow: narrow [lo, hi] by histograms of the same candidates until
+  //    the keys at or above the cut fit the list, or the cut is one key value
+  uint32_t lo = tmin, hi = 0xFFFFFFFFu;
+  int above = 0;  // candidates with a key > hi (all winners)
+  for (int round = 0; round < 4; ++round) {
+    const int sh = bin_shift(lo, hi);
+    for (int i = tid; i < kBins; i += NT) hist[i] = 0u;
+    __syncthreads();
+    for_chunks([&](uint32_t key, int flat) {
+      if (key >= lo && key <= hi) atomicAdd(&hist[bin_of(key, lo, sh)], 1u);
+    });
+    __syncthreads();
+    hist_cut<NT>(hist, sw, (uint32_t)(keep_n - above));  // total >= keep_n - above by construction
+    const uint32_t b = sw.prefix;
+    const uint32_t nlo = lo + (b << sh);
+    const unsigned long long top = (unsigned long long)nlo + ((1ull << sh) - 1ull);
+    const uint32_t nhi = (b == (uint32_t)(kBins - 1)) ? hi : (uint32_t)(top < hi ? top : hi);
+    const int gt = sw.cnt_gt, eq = sw.cnt_eq;
+    __syncthreads();
+    if (above + gt + eq <= LCAP) {  // list everything at or above the cut bin
+      if (tid == 0) sw.nwin = 0;
+      __syncthreads();
+      for_chunks([&](uint32_t key, int flat) { warp_append(list, LCAP, sw.nwin, key >= nlo, key, flat, lane); });
+      __syncthreads();
+      place_winners<NT>(list, sw.nwin, keep_n, sw);
+      return keep_n;
+    }
+    above += gt;
+    lo = nlo;
+    hi = nhi;
+    if (lo == hi) break;  // one key value: ties
+  }
+  // 4. ties at key value T = lo: every key > T wins; the remaining winners are
+  //    the lowest flat slots with key == T, found by one warp walking the
+  //    chunks in order
+  const uint32_t T = lo;
+  if (tid == 0) sw.nwin = 0;
+  __syncthreads();
+  for_chunks([&](uint32_t key, int flat) { warp_append(list, LCAP, sw.nwin, key > T, key, flat, lane); });
+  __syncthreads();
+  if (warp == 0) {
+    int need = keep_n - sw.nwin;  // the same in every lane
+    for (int i0 = 0; i0 < nitems && need > 0; i0 += 32) {
+      const int ic = i0 + lane;
+      int kl = 0;
+      bool pass = false;
+      if (ic < nitems) {
+        kl = upper_find(bt.istart, a.Wc, ic);
+        const float2 p = a.part[(size_t)q * a.pq + (size_t)kl * a.nch + (ic - bt.istart[kl])];
+        pass = (p.y > 0.f) && f2ord(bt.cum[kl] + (p.x - bt.lse[kl])) >= tmin;
+      }
+      unsigned bal = __ballot_sync(kFull, pass);
+      while (bal && need > 0) {
+        const int src = __ffs(bal) - 1;  // ascending chunk order = ascending flat order
+        bal &= bal - 1u;
+        const int k = __shfl_sync(kFull, kl, src);
+        int flat;
+        const uint32_t key = chunk_top_cands(a, bt, q, k, i0 + src - bt.istart[k], tmin, lane, &flat);
+        const unsigned tie = __ballot_sync(kFull, key == T && key != 0u);
+        const int before = __popc(tie & ((1u << lane) - 1u));
+        if (key == T && key != 0u && before < need) {
+          const int pos = sw.nwin + before;
+          if (pos < LCAP) list[pos] = ((unsigned long long)key << 32) | (0xFFFFFFFFu - (uint32_t)flat);
+        }
+        const int took = min(__popc(tie), need);
+        need -= took;
+        if (lane == 0) sw.nwin += took;
+        __syncwarp();
+      }
+    }
+  }
+  __syncthreads();
+  place_winners<NT>(list, min(sw.nwin, LCAP), keep_n, sw);
+  return keep_n;
+}
+
 // Write the survivors (sorted winners) of request q, one thread a survivor:
 // the next beams (parent, token, next-step row, score) or, at the last step,
 // the output SIDs by following parent indices back; rows beyond n are dead

@@ -20,6 +20,7 @@ constexpr uint32_t kStatusRow = 1u;
 constexpr uint32_t kStatusToken = 2u;
 constexpr uint32_t kStatusTimeout = 4u;
 constexpr uint32_t kStatusTmem = 8u;
+constexpr uint32_t kStatusSelect = 16u;  // a select found fewer candidates than its own cut guarantees
 
 // Host-side metadata of one step table.
 struct StepMeta {
@@ -78,6 +79,14 @@ struct StepLaunch {
                            // order (log-softmax over the codebook), else NULL
   int32_t mask_by_beam;    // tab.bitmap holds one row per beam (b = q*Wc + k), not per
                            // index row: a sparse step's legal lists expanded (score-first)
+  // chunk-top select (full steps whose scores were not written): ptop[q*pq +
+  // k*nch + c] = (second-largest legal z, offset of the lowest token holding the
+  // largest) of each chunk, and the operands the projection used, to re-score a
+  // chunk: hq (fp32 hidden, fp32 weights) or hq_hi (+ hq_lo when split) [B*Wc][d]
+  const float2* ptop;
+  const float* hq;
+  const void* hq_hi;
+  const void* hq_lo;
   // outputs
   uint32_t* row_out;       // [B*beam] (s < L)
   float* cum_out;          // [B*beam]
@@ -93,6 +102,9 @@ struct StepLaunch {
 // tokens of the chunk, the same partials the selective kernels produce.
 struct FullEpi {
   float2* part;            // [M][ldz/32], or null (no partials)
+  float2* ptop;            // [M][ldz/32] (second-largest legal z, offset 0..31 of the lowest token holding the
+                           // largest, as int bits) of every chunk, or null; with it the scores need not be
+                           // written (chunk-top select)
   float2* part_all;        // [M][ldz/32] (max, sum exp) over every token < V, or null
   const uint32_t* bitmap;  // dense step's bitmap rows; null: every token < V is legal
   const uint32_t* rows;    // [M] index row of each beam (kDeadRow: dead); null: row 0
@@ -188,6 +200,8 @@ struct zg_plan {
   int32_t L = 0, B = 0, beam = 0;
   int32_t fused = 8;            // CTAs per cluster of the fused kernel; 0 = no fusion
   int32_t order = 0;            // zg_order
+  int32_t hidden = 0;           // zg_hidden_rounding of the tensor-core full projection
+  int32_t scores = 0;           // zg_full_scores: how full steps hand their scores to the select
   float fused_ms[5] = {-1, -1, -1, -1, -1};  // tuned decode times with 1, 2, 4, 8, 16 CTAs a cluster
   float plan_ms = -1.f;                      // tuned decode time of the kept plan
   std::vector<uint8_t> variant;  // [L]

@@ -68,6 +68,8 @@ typedef enum { ZG_SELECTIVE = 0, ZG_FULL = 1, ZG_NAIVE = 2 } zg_variant;
 typedef enum { ZG_RESIDENT_DEVICE = 0, ZG_RESIDENT_HOST = 1 } zg_residency;
 typedef enum { ZG_FORMAT_AUTO = 0, ZG_FORMAT_ALL_SPARSE = 1, ZG_FORMAT_ALL_DENSE = 2 } zg_format_mode;
 typedef enum { ZG_ORDER_FILTER_FIRST = 0, ZG_ORDER_SCORE_FIRST = 1 } zg_order;
+typedef enum { ZG_HIDDEN_SPLIT = 0, ZG_HIDDEN_SINGLE = 1 } zg_hidden_rounding;
+typedef enum { ZG_SCORES_AUTO = 0, ZG_SCORES_WRITTEN = 1, ZG_SCORES_CHUNK_TOPS = 2 } zg_full_scores;
 
 typedef struct zg_index zg_index; /* opaque: step tables + host header */
 typedef struct zg_plan zg_plan;   /* opaque: per-step variant choice   */
@@ -211,6 +213,31 @@ ZG_API zg_status zg_plan_describe(const zg_plan* plan, uint8_t* variant, float* 
  * Changes the workspace size: size the workspace after setting the order.
  * ZG_ERR_INVALID_ARG for another value. */
 ZG_API zg_status zg_plan_set_order(zg_plan* plan, int32_t order);
+/* How ZG_FULL steps run ([Speed]: a dense step scores every token in one
+ * large product, then picks the legal ones).
+ *   hidden_rounding (bf16/fp16 weights; the tensor cores take both operands
+ *   in the weights' type):
+ *     ZG_HIDDEN_SPLIT (default): the fp32 hidden vector enters as two half
+ *       operands (hi + lo, two products into one fp32 accumulator), so full
+ *       and selective scores agree to ~1e-6;
+ *     ZG_HIDDEN_SINGLE: one rounding of the hidden vector (half the tensor
+ *       work; scores off by ~1e-3 for bf16, ~1e-4 for fp16, inside the 2e-2
+ *       tolerance of half weights).
+ *   scores:
+ *     ZG_SCORES_WRITTEN: every score goes to the workspace, the select reads
+ *       them back;
+ *     ZG_SCORES_CHUNK_TOPS: no score is written: per 32-token chunk of a beam
+ *       the projection keeps the legal (max, sum exp), the second-largest
+ *       legal score and the position of the largest; the select cuts on the
+ *       chunk maxima and re-scores the rare chunk whose second-largest also
+ *       clears the cut (exact; same results as written scores);
+ *     ZG_SCORES_AUTO (default): chunk tops on steps whose beams hold at least
+ *       16 chunks per kept candidate (beams * ceil(V/32) >= 16 * keep), else
+ *       written.
+ * Results agree with the other settings within the rounding stated above.
+ * Changes the workspace size: size the workspace after setting it.
+ * ZG_ERR_INVALID_ARG for other values. */
+ZG_API zg_status zg_plan_set_full_projection(zg_plan* plan, int32_t hidden_rounding, int32_t scores);
 /* Save / load a plan ([Speed]: the variant chosen per step on warm-up
  * requests is kept until the next model update, so a serving process can
  * reuse a tuned plan across restarts).  The file holds the steps, batch,
@@ -355,7 +382,8 @@ ZG_API void zg_debug_inject_build_failure(int32_t point, int32_t after);
 /* Synchronises `stream`, then reports and clears the device status word that
  * kernels set instead of trapping (bit 0: row out of range, bit 1: token out
  * of range, bit 2: a bounded wait in the tensor-core kernel expired, bit 3:
- * tensor-memory allocation failed).  Non-zero -> ZG_ERR_DEVICE_STATUS. */
+ * tensor-memory allocation failed, bit 4: a select found fewer candidates
+ * than its own cut guarantees).  Non-zero -> ZG_ERR_DEVICE_STATUS. */
 ZG_API zg_status zg_check_device_status(void* stream);
 
 ZG_API const char* zg_last_error(void);

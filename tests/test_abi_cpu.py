@@ -299,6 +299,7 @@ def test_plan_save_load_roundtrip_and_damage(zg, tmp_path):
     plan = zg.zg_plan_force(idx, 5, 8, [1, 0, 2])
     zg.zg_plan_set_fusion(plan, 4)
     zg.zg_plan_set_order(plan, zg.ZG_ORDER_SCORE_FIRST)
+    zg.zg_plan_set_full_projection(plan, zg.ZG_HIDDEN_SINGLE, zg.ZG_SCORES_CHUNK_TOPS)
     p = str(tmp_path / "p.zgplan")
     zg.zg_plan_save(plan, p)
     back = zg.zg_plan_load(p)
@@ -319,7 +320,7 @@ def test_plan_save_load_roundtrip_and_damage(zg, tmp_path):
     # a well-formed file with an invalid variant (checksum recomputed)
     body = bytearray(raw[8:-8])
     L = int.from_bytes(body[0:4], "little")
-    body[4 * 5 + 4 + 20] = 7                           # first variant byte
+    body[4 * 7 + 4 + 20] = 7                           # first variant byte
     fixed = raw[:8] + bytes(body) + np.array([_fnv1a(bytes(body))], "<u8").tobytes()
     open(p, "wb").write(fixed)
     with pytest.raises(zg.ZgError):
