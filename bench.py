@@ -356,6 +356,8 @@ def run_gpu(args, cfg):
         zg.zg_plan_set_fusion(plan, args.cluster)
     else:
         plan = zg.zg_tune(idx, dm.struct, torch.from_numpy(warm_u).to(dev), B, beam, K, 20, stream)
+    zg.zg_plan_set_full_projection(plan, {"split": 0, "single": 1}[args.hidden],
+                                   {"auto": 0, "written": 1, "tops": 2}[args.scores])
     variants, step_ms, cluster_ctas, fused_ms = zg.zg_plan_describe(plan)
     dec = Decoder(idx, plan, dm, B, beam, K, dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -531,6 +533,7 @@ def run_gpu(args, cfg):
             "data": "synthetic",
             "config": {"workload": workload_desc(cfg), "global_batch": B * world, "beam": beam, "topk": K,
                        "plan": ["full" if v else "selective" for v in variants],
+                       "full_projection": {"hidden": args.hidden, "scores": args.scores},
                        "tune_ms": [[round(float(x), 4) for x in r] for r in step_ms],
                        "cluster_ctas": int(cluster_ctas),
                        "tune_fused_ms": [round(float(x), 4) for x in fused_ms],
@@ -732,6 +735,10 @@ def main(argv=None):
                     help="tune, capture and replay only (a short command for profilers)")
     ap.add_argument("--plan", default="", help="fixed per-step variants instead of tuning, e.g. sss or fss")
     ap.add_argument("--cluster", type=int, default=8, help="fused cluster size with --plan (0: no fusion)")
+    ap.add_argument("--hidden", choices=["split", "single"], default="split",
+                    help="tensor-core full steps: the hidden as hi + lo halves, or one rounding")
+    ap.add_argument("--scores", choices=["auto", "written", "tops"], default="auto",
+                    help="full steps: scores written out, or chunk tops handed to the select")
     ap.add_argument("--index-rebuild", action="store_true",
                     help="rebuild throughput of the workload's index while a decode is served (one JSON line)")
     args = ap.parse_args(argv)

@@ -46,13 +46,13 @@ struct Dims {
   bool sparse[ZG_MAX_STEPS]; // the step's table is sparse (constrained)
 };
 
-// Chunk tops on a full step when its beams hold at least 16 chunks per kept
-// candidate (then the chunk-maximum cut is selective and re-scores are rare).
-bool auto_tops(const Dims& m, int s) {
-  const int64_t Wc = (s == 1) ? 1 : m.beam;
-  const int64_t keep = (s < m.L) ? m.beam : m.K;
-  return Wc * (m.S_full / kChunk) >= 16 * keep;
-}
+// The automatic choice of how a full step hands its scores to the select:
+// written.  Chunk tops save the score stores (~9 us of a 69 us tensor-core
+// step at the dense-early catalogue's step 2) but their select, which
+// re-scores chunks from the weights, measured slower on every configuration
+// (dense early, the unconstrained decodes of the large catalogue), so they
+// are used only when a plan asks for them.
+bool auto_tops(const Dims&, int) { return false; }
 
 struct WsLayout {
   size_t tok_hist, par_hist, row[2], cum[2], h[2], hhi, hlo, Z, part, ptop, part_all, mask, naive_cnt, naive_off,

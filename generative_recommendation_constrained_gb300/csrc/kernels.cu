@@ -179,16 +179,26 @@ __global__ void __launch_bounds__(kClusterThreads, 2) k_decode_cluster(const __g
       int n;
       if (in_smem) {
         beam_lse_sel<NT>(a, q, bt, psm);
-        // chunk beams and keys replace the spent partials in place
-        n = cta_select_chunks<NT, true>(a, q, bt, sw, psm, reinterpret_cast<const float*>(zsm),
-                                  reinterpret_cast<uint32_t*>(psm) + 1, reinterpret_cast<uint32_t*>(psm), 2);
+        // the chunk-maximum cut filters only when the chunks outnumber the
+        // survivors well; otherwise one flat histogram pass over the staged
+        // scores is faster.  Chunk beams and keys replace the spent partials
+        // in place.
+        n = -1;
+        if (4 * min(a.keep, bt.nlegal) < nitems)
+          n = cta_select_chunks<NT, true>(a, q, bt, sw, psm, reinterpret_cast<const float*>(zsm),
+                                          reinterpret_cast<uint32_t*>(psm) + 1, reinterpret_cast<uint32_t*>(psm), 2);
         if (n < 0) n = cta_select_bins<NT>(a, q, bt, sw, zsm, kZStaged);
         write_survivors<NT>(a, q, bt, sw, n, msm);
       } else {
         beam_lse<NT>(a, q, bt);
         __syncthreads();
         const int ni = bt.istart[a.Wc];
-        n = (a.part && 2 * ni <= A.cap) ? cta_select_chunks<NT, false>(a, q, bt, sw, nullptr, nullptr, zsm, zsm + ni, 1) : -1;
+        // spare: the rest of the slot stage plus the (unused) partial and mask
+        // stages, contiguous after it
+        n = (a.part && 2 * ni <= A.cap)
+                ? cta_select_chunks<NT, false>(a, q, bt, sw, nullptr, nullptr, zsm, zsm + ni, 1, zsm + 2 * ni,
+                                               A.cap - 2 * ni + 3 * A.pcap)
+                : -1;
         if (n < 0) {
           if (bt.total <= A.cap) {
             stage_keys_global<NT>(a, q, bt, zsm);
@@ -402,7 +412,7 @@ __global__ void __launch_bounds__(kSelThreads) k_select(const __grid_constant__ 
   __syncthreads();
   const int ni = bt.istart[a.Wc];
   if (a.ptop) {  // the scores were never written: chunk-top select
-    int n = cta_select_tops<kSelThreads>(a, q, bt, sw);
+    int n = cta_select_tops<kSelThreads>(a, q, bt, sw, keys, kSelCap);
     if (n < 0) {
       if (threadIdx.x == 0) flag(a.status, kStatusSelect);  // unreachable: the cut's own maxima are listed
       n = 0;
@@ -411,7 +421,9 @@ __global__ void __launch_bounds__(kSelThreads) k_select(const __grid_constant__ 
     return;
   }
   int n = (a.part && 2 * ni <= kSelCap)
-              ? cta_select_chunks<kSelThreads, false>(a, q, bt, sw, nullptr, nullptr, keys, keys + ni, 1) : -1;
+              ? cta_select_chunks<kSelThreads, false>(a, q, bt, sw, nullptr, nullptr, keys, keys + ni, 1, keys + 2 * ni,
+                                                      kSelCap - 2 * ni)
+              : -1;
   if (n < 0) {
     if (staged) {
       stage_keys_global<kSelThreads>(a, q, bt, keys);

@@ -1207,6 +1207,90 @@ __device__ int cta_select_bins(const StepLaunch& a, int q, BeamTab& bt, SW& sw, 
   return keep_n;
 }
 
+// Staged second cut of the chunk-filtered select (scores in the global slot
+// buffer): the chunks whose maximum key reaches tc are compacted into cid[],
+// their candidates' keys (0 below tc or beyond the beam's slots) copied into
+// kst[] by a flat pass, the keys cut for keep by 2,048 bins over [tc, kceil],
+// and the keys at or above the cut listed and placed.  spare holds cid (at
+// most spare_cap / 33 chunks) then kst.  Returns -1, having written nothing
+// the caller needs, when the chunks or the final list do not fit.
+template <int NT, typename SW>
+__device__ int stage_passing_chunks(const StepLaunch& a, int q, BeamTab& bt, SW& sw, const uint32_t* ckb,
+                                    const uint32_t* kb, int st, uint32_t tc, uint32_t* spare, int spare_cap) {
+  constexpr int NW = NT / 32;
+  constexpr int LCAP = NW * 256 / 2;
+  uint32_t* hist = &sw.whist[0][0];
+  unsigned long long* list = reinterpret_cast<unsigned long long*>(hist);
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int keep_n = min(a.keep, bt.nlegal);
+  const int maxc = spare ? spare_cap / 33 : 0;
+  if (maxc == 0) return -1;
+  const int nitems = bt.istart[a.Wc];
+  int* cid = reinterpret_cast<int*>(spare);
+  uint32_t* kst = spare + maxc;
+  if (tid == 0) sw.nwin = 0;
+  __syncthreads();
+  for (int i0 = 0; i0 < nitems; i0 += NT) {
+    const int i = i0 + tid;
+    const bool f = (i < nitems) && ckb[(size_t)i * st] >= tc;
+    const unsigned bal = __ballot_sync(kFull, f);
+    int pos = 0;
+    if (lane == 0 && bal) pos = atomicAdd(&sw.nwin, __popc(bal));
+    pos = __shfl_sync(kFull, pos, 0) + __popc(bal & ((1u << lane) - 1u));
+    if (f && pos < maxc) cid[pos] = i;
+  }
+  __syncthreads();
+  const int npass = sw.nwin;
+  if (npass > maxc) return -1;
+  const int ne = npass * kChunk;
+  for (int e0 = tid; e0 < ne; e0 += 4 * NT) {
+    uint32_t key[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int e = e0 + u * NT;
+      key[u] = 0u;
+      if (e < ne) {
+        const int item = cid[e >> 5];
+        const int k = (int)kb[(size_t)item * st];
+        const int j = (item - bt.istart[k]) * kChunk + (e & 31);
+        if (j < bt.cnt[k]) key[u] = cand_key_kj(a, bt, q, k, j);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (e0 + u * NT < ne) kst[e0 + u * NT] = key[u] >= tc ? key[u] : 0u;
+  }
+  for (int i = tid; i < kBins; i += NT) hist[i] = 0u;
+  __syncthreads();
+  const uint32_t hi = bt.kceil;
+  const int sh = bin_shift(tc, hi);
+  for (int e = tid; e < ne; e += NT) {
+    const uint32_t key = kst[e];
+    if (key) atomicAdd(&hist[bin_of(key, tc, sh)], 1u);
+  }
+  __syncthreads();
+  if (hist_cut<NT>(hist, sw, (uint32_t)keep_n) < (uint32_t)keep_n) return -1;
+  if (sw.cnt_gt + sw.cnt_eq > LCAP) return -1;
+  const uint32_t t2 = tc + (sw.prefix << sh);
+  __syncthreads();  // every thread has read the cut before the list overwrites the histogram
+  if (tid == 0) sw.nwin = 0;
+  __syncthreads();
+  for (int e0 = 0; e0 < ne; e0 += NT) {
+    const int e = e0 + tid;
+    const uint32_t key = (e < ne) ? kst[e] : 0u;
+    int flat = 0;
+    if (key >= t2 && key) {
+      const int item = cid[e >> 5];
+      const int k = (int)kb[(size_t)item * st];
+      flat = bt.start[k] + (item - bt.istart[k]) * kChunk + (e & 31);
+    }
+    warp_append(list, LCAP, sw.nwin, key && key >= t2, key, flat, lane);
+  }
+  __syncthreads();
+  place_winners<NT>(list, sw.nwin, keep_n, sw);
+  return keep_n;
+}
+
 // ---------------------------------------------------------------------------
 // Chunk-filtered select for steps with chunk partials (from shared memory
 // `ps` by chunk item, or the global partial buffer when ps is null), with the
@@ -1228,7 +1312,7 @@ __device__ int cta_select_bins(const StepLaunch& a, int q, BeamTab& bt, SW& sw, 
 // ---------------------------------------------------------------------------
 template <int NT, bool kSmemZ, typename SW>
 __device__ int cta_select_chunks(const StepLaunch& a, int q, BeamTab& bt, SW& sw, const float2* ps, const float* zs,
-                                 uint32_t* ckb, uint32_t* kb, int st) {
+                                 uint32_t* ckb, uint32_t* kb, int st, uint32_t* spare = nullptr, int spare_cap = 0) {
   constexpr int NW = NT / 32;
   constexpr int LCAP = NW * 256 / 2;
   constexpr int U = 4;  // chunks a warp has in flight
@@ -1276,6 +1360,15 @@ __device__ int cta_select_chunks(const StepLaunch& a, int q, BeamTab& bt, SW& sw
   const int sh2 = bin_shift(tc, hi);
   // a small keep lists every candidate >= tc at once (pass 1) and cuts again
   // only when that list overflows; a large keep cuts again first (pass 2)
+  if constexpr (!kSmemZ) {
+    // scores in the global slot buffer: copy the candidates of the chunks
+    // whose maximum reaches tc into shared memory in one flat pass (many
+    // loads in flight), then cut, list and place from there
+    const int n = stage_passing_chunks<NT>(a, q, bt, sw, ckb, kb, st, tc, spare, spare_cap);
+    if (n >= 0) return n;
+    if (tid == 0) sw.nwin = 0;  // the passes below list from an empty list
+    __syncthreads();
+  }
   const int first = (keep_n * 16 <= LCAP) ? 1 : 2;
   if (first == 2) {
     for (int i = tid; i < kBins; i += NT) hist[i] = 0u;
@@ -1395,32 +1488,59 @@ constexpr float kTopMargin = 1e-4f;
 // multiply-add per element, ascending), so the value is bit-identical to it.
 template <typename WT>
 __device__ __forceinline__ float rescore_token(const StepLaunch& a, size_t b, int t) {
+  // loads are issued eight 16-byte vectors at a time (d is a multiple of 8,
+  // so d/4 fp32 or d/8 half vectors), then consumed in order
+  constexpr int U = 8;
   const WT* w = static_cast<const WT*>(a.W) + (size_t)t * a.d;
   float z = 0.f;
   if constexpr (sizeof(WT) == 4) {
     const float4* h4 = reinterpret_cast<const float4*>(a.hq + b * a.d);
     const float4* w4 = reinterpret_cast<const float4*>(w);
-    for (int e = 0; e < a.d / 4; ++e) {
-      const float4 h = h4[e], x = w4[e];
-      z = fmaf(h.x, x.x, z);
-      z = fmaf(h.y, x.y, z);
-      z = fmaf(h.z, x.z, z);
-      z = fmaf(h.w, x.w, z);
+    const int n = a.d / 4;
+    for (int e0 = 0; e0 < n; e0 += U) {
+      float4 hv[U], wv[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (e0 + u < n) {
+          hv[u] = h4[e0 + u];
+          wv[u] = w4[e0 + u];
+        }
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (e0 + u < n) {
+          z = fmaf(hv[u].x, wv[u].x, z);
+          z = fmaf(hv[u].y, wv[u].y, z);
+          z = fmaf(hv[u].z, wv[u].z, z);
+          z = fmaf(hv[u].w, wv[u].w, z);
+        }
     }
   } else {
     const uint4* hh = reinterpret_cast<const uint4*>(static_cast<const WT*>(a.hq_hi) + b * a.d);
     const uint4* hl = a.hq_lo ? reinterpret_cast<const uint4*>(static_cast<const WT*>(a.hq_lo) + b * a.d) : nullptr;
     const uint4* w8 = reinterpret_cast<const uint4*>(w);
-    for (int e = 0; e < a.d / 8; ++e) {
-      float wf[8], hf[8], lf[8];
-      Vec<WT>::cvt(w8[e], wf);
-      Vec<WT>::cvt(hh[e], hf);
-      if (hl) Vec<WT>::cvt(hl[e], lf);
+    const int n = a.d / 8;
+    for (int e0 = 0; e0 < n; e0 += U) {
+      uint4 wv[U], hv[U], lv[U];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        z = fmaf(hf[i], wf[i], z);
-        if (hl) z = fmaf(lf[i], wf[i], z);
-      }
+      for (int u = 0; u < U; ++u)
+        if (e0 + u < n) {
+          wv[u] = w8[e0 + u];
+          hv[u] = hh[e0 + u];
+          lv[u] = hl ? hl[e0 + u] : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (e0 + u < n) {
+          float wf[8], hf[8], lf[8];
+          Vec<WT>::cvt(wv[u], wf);
+          Vec<WT>::cvt(hv[u], hf);
+          Vec<WT>::cvt(lv[u], lf);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            z = fmaf(hf[i], wf[i], z);
+            if (hl) z = fmaf(lf[i], wf[i], z);
+          }
+        }
     }
   }
   return z;
@@ -1445,32 +1565,65 @@ __device__ __forceinline__ uint32_t key_lowered(uint32_t k) {
   return lk ? lk : 1u;
 }
 
-// Candidates of chunk item i (beam k, chunk c) at or above tmin, one a lane:
-// lane j's (key, flat) for token 32c + j (key 0: none).  Warp-wide.
-__device__ __forceinline__ uint32_t chunk_top_cands(const StepLaunch& a, const BeamTab& bt, int q, int k, int c,
-                                                    uint32_t tmin, int lane, int* flat) {
-  const size_t pi = (size_t)q * a.pq + (size_t)k * a.nch + c;
+// What the select needs of chunk item i: the keys of its maximum (ck) and of
+// its second-largest (k2), 0 when absent, its beam k and the offset t1 of its
+// maximum.  Read from the global partials, or from a shared-memory stage of
+// three words an item ([ck], [k2], [k << 8 | t1]) filled by one flat pass.
+struct ChunkTop {
+  uint32_t ck, k2;
+  int k, t1;
+};
+
+__device__ __forceinline__ ChunkTop chunk_top_global(const StepLaunch& a, const BeamTab& bt, int q, int i) {
+  ChunkTop t;
+  t.k = upper_find(bt.istart, a.Wc, i);
+  const size_t pi = (size_t)q * a.pq + (size_t)t.k * a.nch + (i - bt.istart[t.k]);
   const float2 p = a.part[pi];
   const float2 t2 = a.ptop[pi];
+  const float cum = bt.cum[t.k], lse = bt.lse[t.k];
+  t.ck = (p.y > 0.f) ? f2ord(cum + (p.x - lse)) : 0u;
+  t.k2 = (p.y > 0.f && t2.x != -INFINITY) ? f2ord(cum + (t2.x - lse)) : 0u;
+  t.t1 = __float_as_int(t2.y);
+  return t;
+}
+
+struct TopStage {
+  const uint32_t* st;  // null: read the global partials
+  int n;
+  __device__ __forceinline__ ChunkTop get(const StepLaunch& a, const BeamTab& bt, int q, int i) const {
+    if (!st) return chunk_top_global(a, bt, q, i);
+    ChunkTop t;
+    t.ck = st[i];
+    t.k2 = st[n + i];
+    const uint32_t w = st[2 * n + i];
+    t.k = (int)(w >> 8);
+    t.t1 = (int)(w & 255u);
+    return t;
+  }
+};
+
+// Candidates of chunk item i (beam t.k, chunk c) at or above tmin, one a
+// lane: lane j's (key, flat) for token 32c + j (key 0: none).  Warp-wide.
+__device__ __forceinline__ uint32_t chunk_top_cands(const StepLaunch& a, const BeamTab& bt, int q, const ChunkTop& t,
+                                                    int c, uint32_t tmin, int lane, int* flat) {
+  const int k = t.k;
   *flat = bt.start[k] + c * kChunk + lane;
-  if (!(p.y > 0.f)) return 0u;
-  const float cum = bt.cum[k], lse = bt.lse[k];
-  const uint32_t k1 = f2ord(cum + (p.x - lse));
-  if (k1 < tmin) return 0u;
-  const uint32_t k2 = (t2.x != -INFINITY) ? f2ord(cum + (t2.x - lse)) : 0u;
-  if (k2 < tmin) return (lane == __float_as_int(t2.y)) ? k1 : 0u;  // only the maximum can clear the cut
+  if (t.ck < tmin) return 0u;
+  if (t.k2 < tmin) return (lane == t.t1) ? t.ck : 0u;  // only the maximum can clear the cut
   // re-score the chunk: every legal token at or above the cut
-  const int t = c * kChunk + lane;
-  bool legal = t < a.V;
+  const int tok = c * kChunk + lane;
+  bool legal = tok < a.V;
   if (legal && a.mode != kUncon) legal = (legal_bits(a, bt, q, k)[c] >> lane) & 1u;
   if (!legal) return 0u;
-  const float z = rescore(a, (size_t)q * a.Wc + k, t);
-  const uint32_t kz = f2ord(cum + (z - lse));
+  const float z = rescore(a, (size_t)q * a.Wc + k, tok);
+  const uint32_t kz = f2ord(bt.cum[k] + (z - bt.lse[k]));
   return kz >= tmin ? kz : 0u;
 }
 
+// stage: shared memory of stage_cap words for the per-chunk stage (used when
+// three words an item fit), else null.
 template <int NT, typename SW>
-__device__ int cta_select_tops(const StepLaunch& a, int q, BeamTab& bt, SW& sw) {
+__device__ int cta_select_tops(const StepLaunch& a, int q, BeamTab& bt, SW& sw, uint32_t* stage, int stage_cap) {
   constexpr int NW = NT / 32;
   constexpr int LCAP = NW * 256 / 2;
   static_assert(NW * 256 >= kBins, "histogram space");
@@ -1482,48 +1635,138 @@ __device__ int cta_select_tops(const StepLaunch& a, int q, BeamTab& bt, SW& sw) 
   const int nitems = bt.istart[a.Wc];
   for (int i = tid; i < kBins; i += NT) hist[i] = 0u;
   __syncthreads();  // publishes the lse and the chunk-maximum key range of beam_lse_sel
-  // 1. cut tc on the chunk maxima (their keys counted over [kfloor, kceil])
-  uint32_t tmin = 1u;
-  if (bt.nne >= keep_n && bt.kfloor <= bt.kceil) {
-    const uint32_t lo = bt.kfloor, hi = bt.kceil;
-    const int sh = bin_shift(lo, hi);
-    for (int i = tid; i < nitems; i += NT) {
-      const int k = upper_find(bt.istart, a.Wc, i);
-      const float2 p = a.part[(size_t)q * a.pq + (size_t)k * a.nch + (i - bt.istart[k])];
-      if (p.y > 0.f) {
-        const uint32_t ck = f2ord(bt.cum[k] + (p.x - bt.lse[k]));
-        if (ck >= lo) atomicAdd(&hist[bin_of(ck, lo, sh)], 1u);
+  // 1. one flat pass over the chunks: stage their tops (when they fit) and
+  //    count the maxima's keys over [kfloor, kceil]; cut tc = the keep-th
+  //    largest chunk maximum
+  TopStage ts{(stage && 3 * nitems <= stage_cap) ? stage : nullptr, nitems};
+  const bool cut = bt.nne >= keep_n && bt.kfloor <= bt.kceil;
+  const uint32_t lo = bt.kfloor, hi = bt.kceil;
+  const int sh = cut ? bin_shift(lo, hi) : 0;
+  for (int i0 = tid; i0 < nitems; i0 += 4 * NT) {
+    ChunkTop t[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (i0 + u * NT < nitems) t[u] = chunk_top_global(a, bt, q, i0 + u * NT);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * NT;
+      if (i >= nitems) continue;
+      if (ts.st) {
+        stage[i] = t[u].ck;
+        stage[nitems + i] = t[u].k2;
+        stage[2 * nitems + i] = ((uint32_t)t[u].k << 8) | (uint32_t)t[u].t1;
       }
+      if (cut && t[u].ck >= lo) atomicAdd(&hist[bin_of(t[u].ck, lo, sh)], 1u);
     }
-    __syncthreads();
+  }
+  __syncthreads();
+  uint32_t tmin = 1u;
+  if (cut) {
     if (hist_cut<NT>(hist, sw, (uint32_t)keep_n) >= (uint32_t)keep_n) tmin = key_lowered(lo + (sw.prefix << sh));
     __syncthreads();
   }
-  // every pass visits the chunks whose maximum reaches tmin: each lane tests
-  // one chunk, the warp then takes the passing ones in turn
+  // 2. the chunks whose maximum reaches tmin are compacted, then each warp
+  //    produces their candidates once (re-scoring where needed) into a
+  //    shared-memory list, which is cut and placed without touching the
+  //    scores again.  The multi-pass route below is the fallback when the
+  //    list space does not hold them.
+  if (stage) {
+    const int used = ts.st ? 3 * nitems : 0;
+    const int room = stage_cap - used;
+    if (tid == 0) sw.nwin = 0;
+    __syncthreads();
+    int* cid = reinterpret_cast<int*>(stage + used);
+    const int maxc = room / 4;  // chunk ids, then candidates (two words each)
+    for (int i0 = 0; i0 < nitems; i0 += NT) {
+      const int i = i0 + tid;
+      bool f = false;
+      if (i < nitems) f = (ts.st ? ts.st[i] : chunk_top_global(a, bt, q, i).ck) >= tmin;
+      const unsigned bal = __ballot_sync(kFull, f);
+      int pos = 0;
+      if (lane == 0 && bal) pos = atomicAdd(&sw.nwin, __popc(bal));
+      pos = __shfl_sync(kFull, pos, 0) + __popc(bal & ((1u << lane) - 1u));
+      if (f && pos < maxc) cid[pos] = i;
+    }
+    __syncthreads();
+    const int npass = sw.nwin;
+    if (npass <= maxc) {
+      // candidates after the chunk ids, 8-byte aligned
+      const int cofs = (used + npass + 1) & ~1;
+      unsigned long long* cand = reinterpret_cast<unsigned long long*>(stage + cofs);
+      const int ccap = (stage_cap - cofs) / 2;
+      __syncthreads();
+      if (tid == 0) sw.nwin = 0;
+      __syncthreads();
+      for (int w = warp; w < npass; w += NW) {
+        const int i = cid[w];
+        const ChunkTop t = ts.get(a, bt, q, i);
+        int flat;
+        const uint32_t key = chunk_top_cands(a, bt, q, t, i - bt.istart[t.k], tmin, lane, &flat);
+        warp_append(cand, ccap, sw.nwin, key != 0u, key, flat, lane);
+      }
+      __syncthreads();
+      const int nc = sw.nwin;
+      if (nc <= ccap && nc >= keep_n) {
+        // cut the list's keys for keep over [tmin, max] by 2,048 bins; keys
+        // at or above the cut go to the list space and are placed
+        for (int i = tid; i < kBins; i += NT) hist[i] = 0u;
+        if (tid == 0) sw.prefmask = 0u;
+        __syncthreads();
+        for (int e = tid; e < nc; e += NT) atomicMax(&sw.prefmask, (uint32_t)(cand[e] >> 32));
+        __syncthreads();
+        const uint32_t kmax = sw.prefmask;
+        const int csh = bin_shift(tmin, kmax);
+        for (int e = tid; e < nc; e += NT) atomicAdd(&hist[bin_of((uint32_t)(cand[e] >> 32), tmin, csh)], 1u);
+        __syncthreads();
+        hist_cut<NT>(hist, sw, (uint32_t)keep_n);
+        const uint32_t cutk = tmin + (sw.prefix << csh);
+        const int nlist = sw.cnt_gt + sw.cnt_eq;
+        __syncthreads();
+        if (nlist <= LCAP) {
+          if (tid == 0) sw.nwin = 0;
+          __syncthreads();
+          for (int e0 = 0; e0 < nc; e0 += NT) {
+            const int e = e0 + tid;
+            const unsigned long long x = (e < nc) ? cand[e] : 0ull;
+            const bool f = (e < nc) && (uint32_t)(x >> 32) >= cutk;
+            const unsigned bal = __ballot_sync(kFull, f);
+            int pos = 0;
+            if (lane == 0 && bal) pos = atomicAdd(&sw.nwin, __popc(bal));
+            pos = __shfl_sync(kFull, pos, 0) + __popc(bal & ((1u << lane) - 1u));
+            if (f && pos < LCAP) list[pos] = x;
+          }
+          __syncthreads();
+          place_winners<NT>(list, sw.nwin, keep_n, sw);
+          return keep_n;
+        }
+      }
+    }
+    __syncthreads();
+  }
+  // fallback: every pass visits the chunks whose maximum reaches tmin: each
+  // lane tests one chunk, the warp then takes the passing ones in turn
   auto for_chunks = [&](auto&& body) {
     for (int i0 = 0; i0 < nitems; i0 += NT) {
       const int ic = i0 + lane * NW + warp;
-      int kl = 0;
-      bool pass = false;
-      if (ic < nitems) {
-        kl = upper_find(bt.istart, a.Wc, ic);
-        const float2 p = a.part[(size_t)q * a.pq + (size_t)kl * a.nch + (ic - bt.istart[kl])];
-        pass = (p.y > 0.f) && f2ord(bt.cum[kl] + (p.x - bt.lse[kl])) >= tmin;
-      }
-      unsigned bal = __ballot_sync(kFull, pass);
+      ChunkTop t{0u, 0u, 0, 0};
+      if (ic < nitems) t = ts.get(a, bt, q, ic);
+      unsigned bal = __ballot_sync(kFull, ic < nitems && t.ck >= tmin);
       while (bal) {
         const int src = __ffs(bal) - 1;
         bal &= bal - 1u;
-        const int k = __shfl_sync(kFull, kl, src);
-        const int c = i0 + src * NW + warp - bt.istart[k];
+        ChunkTop tt;
+        tt.ck = __shfl_sync(kFull, t.ck, src);
+        tt.k2 = __shfl_sync(kFull, t.k2, src);
+        tt.k = __shfl_sync(kFull, t.k, src);
+        tt.t1 = __shfl_sync(kFull, t.t1, src);
+        const int c = i0 + src * NW + warp - bt.istart[tt.k];
         int flat;
-        const uint32_t key = chunk_top_cands(a, bt, q, k, c, tmin, lane, &flat);
+        const uint32_t key = chunk_top_cands(a, bt, q, tt, c, tmin, lane, &flat);
         body(key, flat);
       }
     }
   };
-  // 2. list every candidate at or above tmin
+  // fallback 1: list every candidate at or above tmin
   if (tid == 0) sw.nwin = 0;
   __syncthreads();
   for_chunks([&](uint32_t key, int flat) { warp_append(list, LCAP, sw.nwin, key != 0u, key, flat, lane); });
@@ -1536,21 +1779,21 @@ __device__ int cta_select_tops(const StepLaunch& a, int q, BeamTab& bt, SW& sw) 
   }
   // 3. overflow: narrow [lo, hi] by histograms of the same candidates until
   //    the keys at or above the cut fit the list, or the cut is one key value
-  uint32_t lo = tmin, hi = 0xFFFFFFFFu;
-  int above = 0;  // candidates with a key > hi (all winners)
+  uint32_t rlo = tmin, rhi = 0xFFFFFFFFu;
+  int above = 0;  // candidates with a key > rhi (all winners)
   for (int round = 0; round < 4; ++round) {
-    const int sh = bin_shift(lo, hi);
+    const int rsh = bin_shift(rlo, rhi);
     for (int i = tid; i < kBins; i += NT) hist[i] = 0u;
     __syncthreads();
     for_chunks([&](uint32_t key, int flat) {
-      if (key >= lo && key <= hi) atomicAdd(&hist[bin_of(key, lo, sh)], 1u);
+      if (key >= rlo && key <= rhi) atomicAdd(&hist[bin_of(key, rlo, rsh)], 1u);
     });
     __syncthreads();
     hist_cut<NT>(hist, sw, (uint32_t)(keep_n - above));  // total >= keep_n - above by construction
     const uint32_t b = sw.prefix;
-    const uint32_t nlo = lo + (b << sh);
-    const unsigned long long top = (unsigned long long)nlo + ((1ull << sh) - 1ull);
-    const uint32_t nhi = (b == (uint32_t)(kBins - 1)) ? hi : (uint32_t)(top < hi ? top : hi);
+    const uint32_t nlo = rlo + (b << rsh);
+    const unsigned long long top = (unsigned long long)nlo + ((1ull << rsh) - 1ull);
+    const uint32_t nhi = (b == (uint32_t)(kBins - 1)) ? rhi : (uint32_t)(top < rhi ? top : rhi);
     const int gt = sw.cnt_gt, eq = sw.cnt_eq;
     __syncthreads();
     if (above + gt + eq <= LCAP) {  // list everything at or above the cut bin
@@ -1562,14 +1805,14 @@ __device__ int cta_select_tops(const StepLaunch& a, int q, BeamTab& bt, SW& sw) 
       return keep_n;
     }
     above += gt;
-    lo = nlo;
-    hi = nhi;
-    if (lo == hi) break;  // one key value: ties
+    rlo = nlo;
+    rhi = nhi;
+    if (rlo == rhi) break;  // one key value: ties
   }
-  // 4. ties at key value T = lo: every key > T wins; the remaining winners are
-  //    the lowest flat slots with key == T, found by one warp walking the
+  // 4. ties at key value T = rlo: every key > T wins; the remaining winners
+  //    are the lowest flat slots with key == T, found by one warp walking the
   //    chunks in order
-  const uint32_t T = lo;
+  const uint32_t T = rlo;
   if (tid == 0) sw.nwin = 0;
   __syncthreads();
   for_chunks([&](uint32_t key, int flat) { warp_append(list, LCAP, sw.nwin, key > T, key, flat, lane); });
@@ -1578,20 +1821,19 @@ __device__ int cta_select_tops(const StepLaunch& a, int q, BeamTab& bt, SW& sw) 
     int need = keep_n - sw.nwin;  // the same in every lane
     for (int i0 = 0; i0 < nitems && need > 0; i0 += 32) {
       const int ic = i0 + lane;
-      int kl = 0;
-      bool pass = false;
-      if (ic < nitems) {
-        kl = upper_find(bt.istart, a.Wc, ic);
-        const float2 p = a.part[(size_t)q * a.pq + (size_t)kl * a.nch + (ic - bt.istart[kl])];
-        pass = (p.y > 0.f) && f2ord(bt.cum[kl] + (p.x - bt.lse[kl])) >= tmin;
-      }
-      unsigned bal = __ballot_sync(kFull, pass);
+      ChunkTop t{0u, 0u, 0, 0};
+      if (ic < nitems) t = ts.get(a, bt, q, ic);
+      unsigned bal = __ballot_sync(kFull, ic < nitems && t.ck >= tmin);
       while (bal && need > 0) {
         const int src = __ffs(bal) - 1;  // ascending chunk order = ascending flat order
         bal &= bal - 1u;
-        const int k = __shfl_sync(kFull, kl, src);
+        ChunkTop tt;
+        tt.ck = __shfl_sync(kFull, t.ck, src);
+        tt.k2 = __shfl_sync(kFull, t.k2, src);
+        tt.k = __shfl_sync(kFull, t.k, src);
+        tt.t1 = __shfl_sync(kFull, t.t1, src);
         int flat;
-        const uint32_t key = chunk_top_cands(a, bt, q, k, i0 + src - bt.istart[k], tmin, lane, &flat);
+        const uint32_t key = chunk_top_cands(a, bt, q, tt, i0 + src - bt.istart[tt.k], tmin, lane, &flat);
         const unsigned tie = __ballot_sync(kFull, key == T && key != 0u);
         const int before = __popc(tie & ((1u << lane) - 1u));
         if (key == T && key != 0u && before < need) {

@@ -231,9 +231,8 @@ ZG_API zg_status zg_plan_set_order(zg_plan* plan, int32_t order);
  *       legal score and the position of the largest; the select cuts on the
  *       chunk maxima and re-scores the rare chunk whose second-largest also
  *       clears the cut (exact; same results as written scores);
- *     ZG_SCORES_AUTO (default): chunk tops on steps whose beams hold at least
- *       16 chunks per kept candidate (beams * ceil(V/32) >= 16 * keep), else
- *       written.
+ *     ZG_SCORES_AUTO (default): written (chunk tops measured slower: their
+ *       re-scores cost more than the stores they save).
  * Results agree with the other settings within the rounding stated above.
  * Changes the workspace size: size the workspace after setting it.
  * ZG_ERR_INVALID_ARG for other values. */
@@ -264,7 +263,8 @@ ZG_API zg_status zg_decode_workspace_size(const zg_index* idx, const zg_plan* pl
  * lower parent-beam rank, then lower slot (ascending token).  One root beam
  * per request.
  *   idx:  device-resident index, or NULL for the unconstrained decode of
- *         [Results] (every token legal, plan ignored, SIDs need not exist).
+ *         [Results] (every token legal, every step full, SIDs need not
+ *         exist; of the plan only its full-projection settings apply).
  *   plan: per-step variants; NULL = ZG_SELECTIVE at every step.
  *   u:    device float32 [B][d] request vectors.
  *   out_sids:   device int32 [B][K][L]; out_scores: device float32 [B][K],
