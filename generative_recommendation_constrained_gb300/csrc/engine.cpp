@@ -462,10 +462,14 @@ void fused_launches(const Run& r, int s0, StepLaunch* steps) {
 }
 
 // Tables the fused kernel prefetches into L2 at launch, in priority order,
-// up to a budget of half the L2: the output heads W_s of the fused steps,
-// their index tables, then the token tables C_{s-1} their gather-add reads.
+// up to a budget of about 60 % of the L2: the output heads W_s of the fused
+// steps (every legal row is read by some beam), the token tables C_{s-1}
+// their gather-add reads (every beam reads one row), then the index tables of
+// at most 8 MiB (a large table is touched only at the live beams' rows, so
+// fetching all of it would evict useful lines).
 int prefetch_set(const Run& r, int s0, PrefetchRegion* pf) {
-  constexpr uint64_t kBudget = 64ull << 20;
+  constexpr uint64_t kBudget = 80ull << 20;
+  constexpr uint64_t kSmallTable = 8ull << 20;
   uint64_t used = 0;
   int n = 0;
   auto add = [&](const void* p, uint64_t bytes) {
@@ -477,11 +481,12 @@ int prefetch_set(const Run& r, int s0, PrefetchRegion* pf) {
   };
   const uint64_t wrow = (uint64_t)r.m.d * (r.m.w_dtype == ZG_F32 ? 4 : 2);
   for (int s = s0; s <= r.m.L; ++s) add(r.model->W[s - 1], wrow * r.m.V);
+  for (int s = std::max(s0, 2); s <= r.m.L; ++s) add(r.model->C[s - 2], (uint64_t)r.m.d * 4 * r.m.V);
   for (int s = s0; s <= r.m.L; ++s) {
     const StepMeta& sm = r.idx->steps[s - 1];
-    add(r.idx->dev + sm.off_rowptr, sm.off_payload + sm.bytes_payload - sm.off_rowptr);
+    const uint64_t bytes = sm.off_payload + sm.bytes_payload - sm.off_rowptr;
+    if (bytes <= kSmallTable) add(r.idx->dev + sm.off_rowptr, bytes);
   }
-  for (int s = std::max(s0, 2); s <= r.m.L; ++s) add(r.model->C[s - 2], (uint64_t)r.m.d * 4 * r.m.V);
   return n;
 }
 

@@ -154,15 +154,16 @@ __global__ void __launch_bounds__(kClusterThreads, 2) k_decode_cluster(const __g
     const StepLaunch& a = A.st[s - 1];
     build_beam_table<NT>(a, q, bt);
     const int nitems = bt.istart[a.Wc];
-    const bool in_smem = bt.total <= A.cap && nitems <= A.pcap;
+    const bool p_smem = nitems <= A.pcap;              // chunk partials in rank 0's shared memory
+    const bool in_smem = p_smem && bt.total <= A.cap;  // and the slot scores too
     SlotSink sink{};
-    if (in_smem) {
-      sink.z = cl.map_shared_rank(reinterpret_cast<float*>(zsm), 0);
+    if (p_smem) {
+      sink.z = in_smem ? cl.map_shared_rank(reinterpret_cast<float*>(zsm), 0) : nullptr;
       sink.part = cl.map_shared_rank(psm, 0);
       sink.mask = cl.map_shared_rank(msm, 0);
     }
     for (int it = r * NW + warp; it < nitems; it += G * NW) {
-      const int k = upper_find(bt.istart, a.Wc, it);
+      const int k = item_beam(bt, a.Wc, it);
       const int c = it - bt.istart[k];
       BeamState bs;
       bs.row = bt.row[k];
@@ -172,7 +173,7 @@ __global__ void __launch_bounds__(kClusterThreads, 2) k_decode_cluster(const __g
       sink.flat0 = bt.start[k] + c * kChunk;
       sink.item = it;
       sink.cnt = bt.cnt[k];
-      score_chunk<WT, VPL>(a, q, k, bs, bt.rp[k], (uint32_t)bt.nleg[k], c, lane, in_smem ? &sink : nullptr);
+      score_chunk<WT, VPL>(a, q, k, bs, bt.rp[k], (uint32_t)bt.nleg[k], c, lane, p_smem ? &sink : nullptr);
     }
     cl.sync();  // slots and partials of the whole request are now visible to rank 0
     if (r == 0) {
@@ -190,14 +191,19 @@ __global__ void __launch_bounds__(kClusterThreads, 2) k_decode_cluster(const __g
         if (n < 0) n = cta_select_bins<NT>(a, q, bt, sw, zsm, kZStaged);
         write_survivors<NT>(a, q, bt, sw, n, msm);
       } else {
-        beam_lse<NT>(a, q, bt);
+        // scores in the global slot buffer; the partials in shared memory too
+        // when they fit (their log-sum-exp then reads no global memory)
+        if (p_smem)
+          beam_lse_sel<NT>(a, q, bt, psm);
+        else
+          beam_lse<NT>(a, q, bt);
         __syncthreads();
         const int ni = bt.istart[a.Wc];
-        // spare: the rest of the slot stage plus the (unused) partial and mask
-        // stages, contiguous after it
+        // spare: the rest of the slot stage plus the partial and mask stages,
+        // contiguous after it (the partials are read before the spare is used)
         n = (a.part && 2 * ni <= A.cap)
-                ? cta_select_chunks<NT, false>(a, q, bt, sw, nullptr, nullptr, zsm, zsm + ni, 1, zsm + 2 * ni,
-                                               A.cap - 2 * ni + 3 * A.pcap)
+                ? cta_select_chunks<NT, false>(a, q, bt, sw, p_smem ? psm : nullptr, nullptr, zsm, zsm + ni, 1,
+                                               zsm + 2 * ni, A.cap - 2 * ni + 3 * A.pcap)
                 : -1;
         if (n < 0) {
           if (bt.total <= A.cap) {

@@ -151,8 +151,9 @@ __device__ __forceinline__ BeamState load_beam(const StepLaunch& a, int q, int k
 // Destination of a chunk's scores inside the cluster: the rank-0 CTA's shared
 // memory (reached through distributed shared memory), or none (global Z).
 struct SlotSink {
-  float* z;        // z of flat candidate start[k] + j
-  float2* part;    // chunk partials, by item istart[k] + c
+  float* z;        // z of flat candidate start[k] + j, or null: the global slot buffer
+  float2* part;    // chunk partials, by item istart[k] + c (also written to the global partials
+                   // when z is null, for the selects that read them there)
   uint32_t* mask;  // chunk legal masks, by item
   int flat0;       // flat index of the chunk's first slot
   int item;        // item index of the chunk
@@ -168,6 +169,8 @@ __device__ __forceinline__ void score_chunk(const StepLaunch& a, int q, int k, c
   const int nvec = d / E;
   const int b = q * a.Wc + k;
   const int j0 = c * kChunk;
+  // the chunk's legal tokens (index column entries or bitmap word) and the
+  // hidden vector below are loaded together, then checked
   uint32_t vmask;
   int t_lane = 0;
   if (a.mode == kSelDense) {
@@ -179,11 +182,6 @@ __device__ __forceinline__ void score_chunk(const StepLaunch& a, int q, int k, c
     vmask = (nvalid >= 32) ? kFull : ((1u << nvalid) - 1u);
     if (lane < nvalid) t_lane = a.tab.col[rp0 + j0 + lane];
   }
-  if (((vmask >> lane) & 1u) && t_lane >= a.V) {
-    flag(a.status, kStatusToken);
-    vmask &= ~(1u << lane);
-  }
-  vmask = __ballot_sync(kFull, (vmask >> lane) & 1u);  // each lane vouches for its own slot
 
   float h[VPL][E];
   {
@@ -221,6 +219,12 @@ __device__ __forceinline__ void score_chunk(const StepLaunch& a, int q, int k, c
       }
     }
   }
+
+  if (((vmask >> lane) & 1u) && t_lane >= a.V) {
+    flag(a.status, kStatusToken);
+    vmask &= ~(1u << lane);
+  }
+  vmask = __ballot_sync(kFull, (vmask >> lane) & 1u);  // each lane vouches for its own slot
 
   float acc[32];
 #pragma unroll
@@ -273,15 +277,18 @@ __device__ __forceinline__ void score_chunk(const StepLaunch& a, int q, int k, c
   const float e = valid ? expf(z - m) : 0.f;
   float ssum = warp_sum(e);
   ssum = __shfl_sync(kFull, ssum, 0);
-  if (sink) {
+  const float2 pc = make_float2(m, vmask ? ssum : 0.f);
+  if (sink && sink->z) {
     if (j0 + lane < sink->cnt) sink->z[sink->flat0 + lane] = z;
-    if (lane == 0) {
-      sink->part[sink->item] = make_float2(m, vmask ? ssum : 0.f);
-      sink->mask[sink->item] = vmask;
-    }
   } else {
     a.Z[(size_t)q * a.zq + (size_t)k * a.S + j0 + lane] = z;
-    if (lane == 0) a.part[(size_t)q * a.pq + (size_t)k * a.nch + c] = make_float2(m, vmask ? ssum : 0.f);
+  }
+  if (lane == 0) {
+    if (sink) {
+      sink->part[sink->item] = pc;
+      sink->mask[sink->item] = vmask;
+    }
+    if (!sink || !sink->z) a.part[(size_t)q * a.pq + (size_t)k * a.nch + c] = pc;
   }
 }
 
@@ -305,7 +312,13 @@ struct BeamTab {
   // chunk-maximum key and the number of chunks holding a legal candidate
   uint32_t kceil, kfloor;
   int nne;
+  // beam of every 32-slot chunk item, when the step has at most kItemMap
+  // items (else items look their beam up in istart)
+  static constexpr int kItemMap = 2048;
+  int imap_ok;
+  uint16_t ibeam[kItemMap];
 };
+
 
 template <int NW>
 struct SelWorkT {
@@ -334,6 +347,11 @@ __device__ __forceinline__ int upper_find(const int* arr, int n, int c) {
       hi = mid - 1;
   }
   return lo;
+}
+
+// Beam of chunk item i (items are numbered beam by beam: istart).
+__device__ __forceinline__ int item_beam(const BeamTab& bt, int Wc, int i) {
+  return bt.imap_ok ? (int)bt.ibeam[i] : upper_find(bt.istart, Wc, i);
 }
 
 // Fill the beam table of request q entering step s (threads k < Wc), then
@@ -407,9 +425,16 @@ __device__ void build_beam_table(const StepLaunch& a, int q, BeamTab& bt) {
       bt.kceil = 0u;
       bt.kfloor = 0xFFFFFFFFu;
       bt.nne = 0;
+      bt.imap_ok = (ii <= BeamTab::kItemMap) ? 1 : 0;
     }
   }
   __syncthreads();
+  // chunk item -> beam, once per step, for every pass that walks items
+  if (bt.imap_ok) {
+    const int nitems = bt.istart[a.Wc];
+    for (int i = tid; i < nitems; i += NT) bt.ibeam[i] = (uint16_t)upper_find(bt.istart, a.Wc, i);
+    __syncthreads();
+  }
 }
 
 // Log-sum-exp of every live beam from its chunk partials (m_c, s_c): lse =
@@ -500,12 +525,18 @@ __device__ void beam_lse_sel(const StepLaunch& a, int q, BeamTab& bt, const floa
     for (int h = 0; h < 2; ++h) {
       float m = p0[h].x, mn = (p0[h].y > 0.f) ? p0[h].x : INFINITY;
       int ne = (p0[h].y > 0.f) ? 1 : 0;  // a chunk with a legal candidate has sum >= 1
-      for (int c = sl + 8; c < n[h]; c += 8) {
-        const float2 p = pp[h][c];
-        m = fmaxf(m, p.x);
-        if (p.y > 0.f) {
-          mn = fminf(mn, p.x);
-          ++ne;
+      // a beam with many chunks: four partials a lane in flight at a time
+      for (int c0 = sl + 8; c0 < n[h]; c0 += 32) {
+        float2 pv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) pv[u] = (c0 + 8 * u < n[h]) ? pp[h][c0 + 8 * u] : make_float2(-INFINITY, 0.f);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          m = fmaxf(m, pv[u].x);
+          if (pv[u].y > 0.f) {
+            mn = fminf(mn, pv[u].x);
+            ++ne;
+          }
         }
       }
       float ma = a0[h].x;  // maximum of the normalised set
@@ -520,21 +551,41 @@ __device__ void beam_lse_sel(const StepLaunch& a, int q, BeamTab& bt, const floa
       }
       if (!all_v) ma = m;
       float sum = (a0[h].y > 0.f) ? a0[h].y * expf(a0[h].x - ma) : 0.f;
-      for (int c = sl + 8; c < n[h]; c += 8) {
-        const float2 p = pa[h][c];
-        if (p.y > 0.f) sum += p.y * expf(p.x - ma);
+      for (int c0 = sl + 8; c0 < n[h]; c0 += 32) {
+        float2 pv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) pv[u] = (c0 + 8 * u < n[h]) ? pa[h][c0 + 8 * u] : make_float2(-INFINITY, 0.f);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (pv[u].y > 0.f) sum += pv[u].y * expf(pv[u].x - ma);
       }
 #pragma unroll
       for (int o = 4; o; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
       const int k = kb[h];
-      if (n[h] > 0 && sl == 0) {
+      // keys of the beam's best and of its weakest chunk maximum, as the
+      // select computes them; folded over the warp's four beams first, so one
+      // lane a warp updates the shared range
+      uint32_t kc = 0u, kf = 0xFFFFFFFFu;
+      int nn = 0;
+      if (n[h] > 0) {
         const float lse = ma + logf(sum);
-        bt.lse[k] = lse;
-        if (ne > 0) {  // keys of the beam's best and of its weakest chunk maximum, as the select computes them
-          atomicMax(&bt.kceil, f2ord(bt.cum[k] + (m - lse)));
-          atomicMin(&bt.kfloor, f2ord(bt.cum[k] + (mn - lse)));
-          atomicAdd(&bt.nne, ne);
+        if (sl == 0) bt.lse[k] = lse;
+        if (ne > 0) {
+          kc = f2ord(bt.cum[k] + (m - lse));
+          kf = f2ord(bt.cum[k] + (mn - lse));
+          nn = ne;
         }
+      }
+#pragma unroll
+      for (int o = 8; o < 32; o <<= 1) {
+        kc = max(kc, __shfl_xor_sync(kFull, kc, o));
+        kf = min(kf, __shfl_xor_sync(kFull, kf, o));
+        nn += __shfl_xor_sync(kFull, nn, o);
+      }
+      if (lane == 0 && nn > 0) {
+        atomicMax(&bt.kceil, kc);
+        atomicMin(&bt.kfloor, kf);
+        atomicAdd(&bt.nne, nn);
       }
     }
   }
@@ -786,7 +837,7 @@ __device__ int cta_select_filtered(const StepLaunch& a, int q, BeamTab& bt, SW& 
       k = i / rt;
       j0 = (i - k * rt) * tw;
     } else {  // one 32-slot chunk a representative, numbered by the chunk prefix
-      k = upper_find(bt.istart, a.Wc, i);
+      k = item_beam(bt, a.Wc, i);
       j0 = (i - bt.istart[k]) * kChunk;
     }
     const int j1 = min(j0 + tw, bt.cnt[k]);
@@ -850,7 +901,7 @@ template <int NT>
 __device__ int chunk_rep_keys(const StepLaunch& a, int q, const BeamTab& bt, uint32_t* rep) {
   const int n = bt.istart[a.Wc];
   for (int i = threadIdx.x; i < n; i += NT) {
-    const int k = upper_find(bt.istart, a.Wc, i);
+    const int k = item_beam(bt, a.Wc, i);
     const float m = a.part[(size_t)q * a.pq + (size_t)k * a.nch + (i - bt.istart[k])].x;
     rep[i] = (m != -INFINITY) ? f2ord(bt.cum[k] + (m - bt.lse[k])) : 0u;
   }
@@ -1177,13 +1228,18 @@ __device__ int cta_select_bins(const StepLaunch& a, int q, BeamTab& bt, SW& sw, 
   if (bt.nne < keep_n || lo > hi) return cta_select<NT>(a, q, bt, sw, keys, src);
   const int sh = bin_shift(lo, hi);
   if (src == kZStaged) {
-    int c = tid, k = (c < total) ? upper_find(bt.start, a.Wc, c) : 0;
-    for (; c < total; c += NT) {
-      while (bt.start[k + 1] <= c) ++k;
-      const float z = __uint_as_float(keys[c]);
-      const uint32_t key = (z == -INFINITY) ? 0u : f2ord(bt.cum[k] + (z - bt.lse[k]));
-      keys[c] = key;
-      if (key >= lo) atomicAdd(&hist[bin_of(key, lo, sh)], 1u);
+    // one warp a 32-slot chunk (the beam looked up once for 32 candidates)
+    const int nitems = bt.istart[a.Wc];
+    for (int i = warp; i < nitems; i += NW) {
+      const int k = item_beam(bt, a.Wc, i);
+      const int j = (i - bt.istart[k]) * kChunk + lane;
+      if (j < bt.cnt[k]) {
+        const int c = bt.start[k] + j;
+        const float z = __uint_as_float(keys[c]);
+        const uint32_t key = (z == -INFINITY) ? 0u : f2ord(bt.cum[k] + (z - bt.lse[k]));
+        keys[c] = key;
+        if (key >= lo) atomicAdd(&hist[bin_of(key, lo, sh)], 1u);
+      }
     }
   } else {
     for (int c = tid; c < total; c += NT) {
@@ -1243,10 +1299,11 @@ __device__ int stage_passing_chunks(const StepLaunch& a, int q, BeamTab& bt, SW&
   const int npass = sw.nwin;
   if (npass > maxc) return -1;
   const int ne = npass * kChunk;
-  for (int e0 = tid; e0 < ne; e0 += 4 * NT) {
-    uint32_t key[4];
+  constexpr int UL = 16;  // global loads a thread keeps in flight
+  for (int e0 = tid; e0 < ne; e0 += UL * NT) {
+    uint32_t key[UL];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < UL; ++u) {
       const int e = e0 + u * NT;
       key[u] = 0u;
       if (e < ne) {
@@ -1257,7 +1314,7 @@ __device__ int stage_passing_chunks(const StepLaunch& a, int q, BeamTab& bt, SW&
       }
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
+    for (int u = 0; u < UL; ++u)
       if (e0 + u * NT < ne) kst[e0 + u * NT] = key[u] >= tc ? key[u] : 0u;
   }
   for (int i = tid; i < kBins; i += NT) hist[i] = 0u;
@@ -1338,7 +1395,7 @@ __device__ int cta_select_chunks(const StepLaunch& a, int q, BeamTab& bt, SW& sw
       p[u] = make_float2(-INFINITY, 0.f);
       kk[u] = 0;
       if (i < nitems) {
-        kk[u] = upper_find(bt.istart, a.Wc, i);
+        kk[u] = item_beam(bt, a.Wc, i);
         p[u] = ps ? ps[i] : a.part[(size_t)q * a.pq + (size_t)kk[u] * a.nch + (i - bt.istart[kk[u]])];
       }
     }
@@ -1576,7 +1633,7 @@ struct ChunkTop {
 
 __device__ __forceinline__ ChunkTop chunk_top_global(const StepLaunch& a, const BeamTab& bt, int q, int i) {
   ChunkTop t;
-  t.k = upper_find(bt.istart, a.Wc, i);
+  t.k = item_beam(bt, a.Wc, i);
   const size_t pi = (size_t)q * a.pq + (size_t)t.k * a.nch + (i - bt.istart[t.k]);
   const float2 p = a.part[pi];
   const float2 t2 = a.ptop[pi];
