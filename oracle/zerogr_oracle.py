@@ -283,6 +283,68 @@ ORDERS = ("filter_first", "score_first")
 
 
 # ---------------------------------------------------------------------------
+# light causal decoder producing each step's hidden vector ("Separating
+# Thinking from Spelling", AI Papers Daily digest: a backbone emits a fixed-size
+# next-item concept once; a light 2-layer, 256-wide causal decoder conditioned
+# on the concept and the generated prefix runs the trie-constrained beam
+# search).  Readings (the digest gives only the above): inputs are the M
+# concept vectors then the embeddings of the chosen tokens, each plus a
+# position embedding; pre-norm layers x += attention(norm(x)), x += MLP(norm(x));
+# RMS normalisation without gain, causal multi-head attention scaled by
+# 1/sqrt(head width), ReLU MLP; the hidden vector is the normalised output of
+# the last position.
+# ---------------------------------------------------------------------------
+
+RMS_EPS = 1e-6
+
+
+def rms_norm(X: np.ndarray) -> np.ndarray:
+    """Each row divided by the root of its mean square (plus RMS_EPS)."""
+    X = np.asarray(X, dtype=np.float64)
+    return X / np.sqrt(np.mean(X * X, axis=-1, keepdims=True) + RMS_EPS)
+
+
+def causal_attention(Q: np.ndarray, K: np.ndarray, V: np.ndarray, heads: int) -> np.ndarray:
+    """Per head h (a contiguous block of d/heads columns): row i attends to
+    rows j <= i with weights softmax_j(q_i . k_j / sqrt(d/heads))."""
+    n, d = Q.shape
+    dh = d // heads
+    out = np.zeros((n, d))
+    mask = np.tril(np.ones((n, n), dtype=bool))
+    for h in range(heads):
+        c = slice(h * dh, (h + 1) * dh)
+        S = Q[:, c] @ K[:, c].T / math.sqrt(dh)
+        S = np.where(mask, S, -np.inf)
+        P = np.exp(S - S.max(axis=1, keepdims=True))
+        P /= P.sum(axis=1, keepdims=True)
+        out[:, c] = P @ V[:, c]
+    return out
+
+
+def deco_forward(w, concepts_q: np.ndarray, prefix) -> np.ndarray:
+    """Output rows of every position of the sequence [concepts, tokens of the
+    prefix] after all layers (before the final normalisation)."""
+    rows = [np.asarray(concepts_q[m], np.float64) + w.P[m] for m in range(w.M)]
+    rows += [np.asarray(w.E[j][int(t)], np.float64) + w.P[w.M + j] for j, t in enumerate(prefix)]
+    X = np.array(rows)
+    for l in range(w.layers):
+        A = rms_norm(X)
+        Q = A @ np.asarray(w.Wq[l], np.float64).T
+        K = A @ np.asarray(w.Wk[l], np.float64).T
+        Vv = A @ np.asarray(w.Wv[l], np.float64).T
+        X = X + causal_attention(Q, K, Vv, w.heads) @ np.asarray(w.Wo[l], np.float64).T
+        H = np.maximum(rms_norm(X) @ np.asarray(w.W1[l], np.float64).T, 0.0)
+        X = X + H @ np.asarray(w.W2[l], np.float64).T
+    return X
+
+
+def deco_hidden(w, concepts_q: np.ndarray, prefix) -> np.ndarray:
+    """Hidden vector of a beam with the given prefix: the normalised output of
+    the sequence's last position."""
+    return rms_norm(deco_forward(w, concepts_q, prefix)[-1])
+
+
+# ---------------------------------------------------------------------------
 # beam search  [Pipeline]
 # ---------------------------------------------------------------------------
 
@@ -316,7 +378,7 @@ def candidate_order(vals: np.ndarray, flat: np.ndarray) -> np.ndarray:
 
 
 def decode(trie: Trie | None, model, u: np.ndarray, beam: int, K: int,
-           requests=None, order: str = "filter_first") -> DecodeResult:
+           requests=None, order: str = "filter_first", deco=None) -> DecodeResult:
     """Filtering-first constrained beam search, one request at a time.
 
     Per request: one root beam (empty prefix, cumulative score 0, hidden u).
@@ -333,6 +395,9 @@ def decode(trie: Trie | None, model, u: np.ndarray, beam: int, K: int,
     order="score_first" replaces lp_t by the conventional order's
     score_first_log_probs (every token scored, normaliser over the codebook,
     then the mask); everything else is unchanged.
+    deco: a light decoder's weights; then u holds each request's concept
+    vectors [B, M, d] and a beam's hidden vector is deco_hidden of its prefix
+    (the token tables C are not used).
     """
     if order not in ORDERS:
         raise ValueError(order)
@@ -341,7 +406,7 @@ def decode(trie: Trie | None, model, u: np.ndarray, beam: int, K: int,
     B = u.shape[0]
     req = range(B) if requests is None else list(requests)
     Wd = _weights_f64(model)
-    Cd = [np.asarray(c, dtype=np.float64) for c in model.C]
+    Cd = [np.asarray(c, dtype=np.float64) for c in model.C] if deco is None else None
     out_sids = np.full((B, K, L), -1, dtype=np.int64)
     out_scores = np.full((B, K), -np.inf)
     gaps = np.full((B, L), np.inf)
@@ -349,7 +414,8 @@ def decode(trie: Trie | None, model, u: np.ndarray, beam: int, K: int,
     next_score = np.full(B, -np.inf)
     all_tok = np.arange(V)
     for q in req:
-        beams = [((), 0.0, u[q].astype(np.float64))]
+        h0 = deco_hidden(deco, u[q], ()) if deco is not None else u[q].astype(np.float64)
+        beams = [((), 0.0, h0)]
         for s in range(1, L + 1):
             keep = beam if s < L else K
             legal = [trie.children(p) if trie is not None else all_tok for p, _, _ in beams]
@@ -379,7 +445,12 @@ def decode(trie: Trie | None, model, u: np.ndarray, beam: int, K: int,
             for i in chosen:
                 p, cum, h = beams[ranks[i]]
                 t = int(toks[i])
-                h2 = advance_hidden(h, Cd, s, t) if s < L else None
+                if s == L:
+                    h2 = None
+                elif deco is not None:
+                    h2 = deco_hidden(deco, u[q], p + (t,))
+                else:
+                    h2 = advance_hidden(h, Cd, s, t)
                 new.append((p + (t,), float(vals[i]), h2))
             beams = new
         for i, (p, cum, _) in enumerate(beams):
@@ -389,7 +460,7 @@ def decode(trie: Trie | None, model, u: np.ndarray, beam: int, K: int,
 
 
 def path_score(trie: Trie | None, model, u_q: np.ndarray, sid, order: str = "filter_first",
-               Wd=None) -> float:
+               Wd=None, deco=None) -> float:
     """Filter-first score of one item along its own path: the sum over steps
     of its token's log-probability among the legal tokens after its prefix
     (score-first: among all V tokens).  The hidden vector is recomputed from
@@ -401,9 +472,12 @@ def path_score(trie: Trie | None, model, u_q: np.ndarray, sid, order: str = "fil
     total = 0.0
     for s in range(1, L + 1):
         prefix = tuple(int(t) for t in sid[:s - 1])
-        h = np.asarray(u_q, dtype=np.float64).copy()
-        for j, t in enumerate(prefix):
-            h = h + np.asarray(model.C[j][t], dtype=np.float64)
+        if deco is not None:
+            h = deco_hidden(deco, u_q, prefix)
+        else:
+            h = np.asarray(u_q, dtype=np.float64).copy()
+            for j, t in enumerate(prefix):
+                h = h + np.asarray(model.C[j][t], dtype=np.float64)
         T = trie.children(prefix) if trie is not None else np.arange(V)
         t = int(sid[s - 1])
         pos = np.searchsorted(T, t)
@@ -418,7 +492,7 @@ def path_score(trie: Trie | None, model, u_q: np.ndarray, sid, order: str = "fil
     return total
 
 
-def brute_force(trie: Trie, model, u_q: np.ndarray, order: str = "filter_first"):
+def brute_force(trie: Trie, model, u_q: np.ndarray, order: str = "filter_first", deco=None):
     """Exhaustive enumeration for tiny catalogues: every item with its
     filter-first score, computed as the log of the product of per-step
     probabilities softmax(z over legal tokens)[token] (score-first:
@@ -431,9 +505,12 @@ def brute_force(trie: Trie, model, u_q: np.ndarray, order: str = "filter_first")
 
     def walk(prefix, prob):
         s = len(prefix) + 1
-        h = np.asarray(u_q, dtype=np.float64) + sum(
-            (np.asarray(model.C[j][t], dtype=np.float64) for j, t in enumerate(prefix)),
-            np.zeros(model.d))
+        if deco is not None:
+            h = deco_hidden(deco, u_q, prefix)
+        else:
+            h = np.asarray(u_q, dtype=np.float64) + sum(
+                (np.asarray(model.C[j][t], dtype=np.float64) for j, t in enumerate(prefix)),
+                np.zeros(model.d))
         T = trie.children(prefix)
         if order == "score_first":
             z = Wd[s - 1] @ h

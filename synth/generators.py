@@ -28,6 +28,8 @@ _PURPOSE = {
     "W": 5,
     "zipf": 6,
     "level": 7,
+    "deco": 8,
+    "concept": 9,
 }
 
 
@@ -375,3 +377,57 @@ def make_model(L: int, V: int, d: int, w_dtype: str = "f32", seed: int = 0,
 def make_requests(B: int, d: int, seed: int = 0) -> np.ndarray:
     """Request vectors u ~ N(0, 1/d) (variance), float32 [B, d]."""
     return (rng_for(seed, "u").standard_normal((B, d)) / math.sqrt(d)).astype(np.float32)
+
+
+# ---------------------------------------------------------------------------
+# light decoder (the model producing each step's hidden vector from a fixed
+# set of concept vectors and the prefix of chosen tokens)
+# ---------------------------------------------------------------------------
+
+@dataclass
+class DecoWeights:
+    """Random weights of a causal decoder of `layers` layers, width d, `heads`
+    attention heads and MLP width `ffn`, for an L-step SID decode with M
+    concept vectors.  Every matrix is float32 [out][in] (row-major).
+      E[s]: [V, d] embedding of the token chosen at step s+1 (s = 0..L-2)
+      P:    [M + L - 1, d] position embeddings
+      Wq, Wk, Wv, Wo: per layer [d, d];  W1: per layer [ffn, d];  W2: per layer [d, ffn]"""
+    M: int
+    d: int
+    heads: int
+    ffn: int
+    layers: int
+    E: list
+    P: np.ndarray
+    Wq: list
+    Wk: list
+    Wv: list
+    Wo: list
+    W1: list
+    W2: list
+
+
+def make_deco(L: int, V: int, d: int = 256, M: int = 2, heads: int = 4, ffn: int = 1024, layers: int = 2,
+              seed: int = 0, zero_residual: bool = False) -> DecoWeights:
+    """Embeddings ~ N(0, 1/d); projections ~ N(0, 1/fan_in) (variance), so
+    activations stay of order one.  zero_residual: attention-output and
+    MLP-output weights all zero (every layer leaves its input unchanged)."""
+    def draw(i, shape, fan_in):
+        return (rng_for(seed, "deco", i).standard_normal(shape) / math.sqrt(fan_in)).astype(np.float32)
+    E = [draw(s, (V, d), d) for s in range(L - 1)]
+    P = draw(10, (M + L - 1, d), d)
+    Wq, Wk, Wv, Wo, W1, W2 = [], [], [], [], [], []
+    for l in range(layers):
+        b = 100 + 10 * l
+        Wq.append(draw(b, (d, d), d))
+        Wk.append(draw(b + 1, (d, d), d))
+        Wv.append(draw(b + 2, (d, d), d))
+        Wo.append(np.zeros((d, d), np.float32) if zero_residual else draw(b + 3, (d, d), d))
+        W1.append(draw(b + 4, (ffn, d), d))
+        W2.append(np.zeros((d, ffn), np.float32) if zero_residual else draw(b + 5, (d, ffn), ffn))
+    return DecoWeights(M, d, heads, ffn, layers, E, P, Wq, Wk, Wv, Wo, W1, W2)
+
+
+def make_concepts(B: int, M: int, d: int, seed: int = 0) -> np.ndarray:
+    """Concept vectors of each request ~ N(0, 1/d) (variance), float32 [B, M, d]."""
+    return (rng_for(seed, "concept").standard_normal((B, M, d)) / math.sqrt(d)).astype(np.float32)

@@ -21,7 +21,8 @@ def golden_catalogue(fx):
     return L, V, sids
 
 
-def check_topk(gpu_sids, gpu_scores, ref, trie, model, u, tol, window, requests=None, order="filter_first"):
+def check_topk(gpu_sids, gpu_scores, ref, trie, model, u, tol, window, requests=None, order="filter_first",
+               deco=None):
     """Compare a decode's top-K output with the oracle's.
 
     Both sides compute the same beam search; floating-point rounding differs
@@ -35,6 +36,8 @@ def check_topk(gpu_sids, gpu_scores, ref, trie, model, u, tol, window, requests=
         the same number of outputs is returned, the sorted score lists agree
         within ``tol`` and every oracle item whose score clears the first
         dropped candidate by more than ``window`` is returned.
+    deco: the light decoder's weights when it produces the hidden vectors (u
+    then holds the concept vectors).
     Returns the number of requests that had only the first two checks; the
     largest |score - exact path score| seen is left in LAST_MAX_ERR."""
     global LAST_MAX_ERR
@@ -61,7 +64,7 @@ def check_topk(gpu_sids, gpu_scores, ref, trie, model, u, tol, window, requests=
             seen.add(sid)
             if trie is not None:
                 assert trie.contains(sid), f"request {q}: SID {sid} not in catalogue"
-            exact = _path(trie, model, u[q], sid, order, Wd)
+            exact = _path(trie, model, u[q], sid, order, Wd, deco)
             max_err = max(max_err, abs(exact - sc[i]))
             LAST_MAX_ERR = max_err
             assert abs(exact - sc[i]) <= tol, \
@@ -83,9 +86,9 @@ def check_topk(gpu_sids, gpu_scores, ref, trie, model, u, tol, window, requests=
     return ambiguous
 
 
-def _path(trie, model, u_q, sid, order="filter_first", Wd=None):
+def _path(trie, model, u_q, sid, order="filter_first", Wd=None, deco=None):
     from oracle import path_score
-    return path_score(trie, model, u_q, sid, order, Wd)
+    return path_score(trie, model, u_q, sid, order, Wd, deco)
 
 
 def isclose_inf(a, b, tol):

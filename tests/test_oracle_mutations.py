@@ -212,3 +212,57 @@ def test_mistake_trie_children_wrong_digit(monkeypatch):
         return np.unique((self.keys[lo:hi] // div) % self.V)
     monkeypatch.setattr(Z.Trie, "children", wrong_children)
     assert not _trie_pin_holds()
+
+
+# ---------------------------------------------------------------- light decoder
+
+def test_decoder_pins_hold_on_the_real_oracle():
+    import test_oracle_deco as P
+    assert P.rms_matches_torch() and P.attention_matches_torch() and P.zero_residual_closed_form()
+    assert P.uniform_attention_is_running_mean() and P.causal()
+
+
+def test_mistake_attention_without_causal_mask(monkeypatch):
+    import test_oracle_deco as P
+
+    def full(Q, K, V, heads):
+        n, d = Q.shape
+        dh = d // heads
+        out = np.zeros((n, d))
+        for h in range(heads):
+            c = slice(h * dh, (h + 1) * dh)
+            S = Q[:, c] @ K[:, c].T / np.sqrt(dh)
+            Pm = np.exp(S - S.max(axis=1, keepdims=True))
+            out[:, c] = (Pm / Pm.sum(axis=1, keepdims=True)) @ V[:, c]
+        return out
+    monkeypatch.setattr(Z, "causal_attention", full)
+    assert not P.causal()
+    assert not P.attention_matches_torch()
+
+
+def test_mistake_attention_unscaled(monkeypatch):
+    import test_oracle_deco as P
+    real = Z.causal_attention
+    monkeypatch.setattr(Z, "causal_attention", lambda Q, K, V, heads: real(Q * np.sqrt(Q.shape[1] // heads), K, V, heads))
+    assert not P.attention_matches_torch()
+
+
+def test_mistake_position_embedding_off_by_one(monkeypatch):
+    import test_oracle_deco as P
+    real = Z.deco_forward
+
+    def shifted(w, concepts_q, prefix):
+        import copy
+        w2 = copy.copy(w)
+        w2.P = np.roll(w.P, 1, axis=0)
+        return real(w2, concepts_q, prefix)
+    monkeypatch.setattr(Z, "deco_forward", shifted)
+    assert not P.zero_residual_closed_form()
+
+
+def test_mistake_norm_by_sum_of_squares(monkeypatch):
+    import test_oracle_deco as P
+    monkeypatch.setattr(Z, "rms_norm", lambda X: np.asarray(X, np.float64) / np.sqrt(
+        np.sum(np.asarray(X, np.float64) ** 2, axis=-1, keepdims=True) + Z.RMS_EPS))
+    assert not P.rms_matches_torch()
+    assert not P.zero_residual_closed_form()
