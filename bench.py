@@ -719,6 +719,68 @@ def run_index_rebuild(args, cfg):
     print(json.dumps(line), flush=True)
 
 
+def run_light_decoder(args, cfg):
+    """The decode with a light causal decoder producing the hidden vectors
+    (2 layers, width d, 4 heads, MLP 4d, 2 concept vectors a request; random
+    weights): graph-replayed decode time, and from a traced decode the
+    decoder's share of the step kernels' time, next to the same workload's
+    decode with the synthetic gather-add model."""
+    import torch
+    import generative_recommendation_constrained_gb300 as zg
+    from generative_recommendation_constrained_gb300.device import Decoder, DeviceModel
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream().cuda_stream
+    sids = synth.make_catalogue(cfg, 0)
+    model = synth.make_model(cfg.L, cfg.V, cfg.d, cfg.w_dtype, 0)
+    deco = synth.make_deco(cfg.L, cfg.V, cfg.d, M=2, heads=4, ffn=4 * cfg.d, layers=2, seed=0)
+    B, beam, K = cfg.batch, cfg.beam, cfg.topk
+    c = torch.from_numpy(synth.make_concepts(B, 2, cfg.d, request_seed(0))).to(dev)
+    u = torch.from_numpy(synth.make_requests(B, cfg.d, request_seed(0))).to(dev)
+    idx = zg.zg_index_build(sids, cfg.V, stream=stream)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    out = {}
+    for name, dm, x in (("light_decoder", DeviceModel(model, dev, deco=deco), c),
+                        ("gather_add", DeviceModel(model, dev), u)):
+        plan = zg.zg_tune(idx, dm.struct, x, B, beam, K, 5, stream)
+        dec = Decoder(idx, plan, dm, B, beam, K, dev)
+        dec(x)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                dec(x, side.cuda_stream)
+        torch.cuda.current_stream().wait_stream(side)
+        times = []
+        for i in range(args.warmup + args.steps):
+            flush.fill_(1.0)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            if i >= args.warmup:
+                times.append(a.elapsed_time(b))
+        flush.fill_(1.0)
+        tr = dec.trace(x)
+        model_ms = sum(st["ms_model"] for st in tr["steps"])
+        step_ms = sum(st["ms_model"] + st["ms_gather"] + st["ms_project"] + st["ms_select"] for st in tr["steps"])
+        out[name] = {"ms_per_batch": statistics.fmean(times), "requests_per_s": B / (statistics.fmean(times) / 1e3),
+                     "plan": "".join("f" if v else "s" for v in zg.zg_plan_describe(plan)[0]),
+                     "traced_model_ms": model_ms, "traced_step_kernels_ms": step_ms}
+    ld = out["light_decoder"]
+    ld["model_share_of_step_kernels"] = ld["traced_model_ms"] / ld["traced_step_kernels_ms"]
+    line = {"metric": "constrained decode with a light causal decoder producing the hidden vectors",
+            "unit": "ms/batch", "value": ld["ms_per_batch"], "higher_is_better": False, "n_gpus": 1,
+            "data": "synthetic", "config": {"workload": workload_desc(cfg),
+                                            "decoder": "2 layers, width d, 4 heads, MLP 4d, 2 concept vectors, "
+                                                       "fp32 random weights"},
+            **out}
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -739,6 +801,8 @@ def main(argv=None):
                     help="tensor-core full steps: the hidden as hi + lo halves, or one rounding")
     ap.add_argument("--scores", choices=["auto", "written", "tops"], default="auto",
                     help="full steps: scores written out, or chunk tops handed to the select")
+    ap.add_argument("--light-decoder", action="store_true",
+                    help="decode with a light causal decoder producing the hidden vectors (one JSON line)")
     ap.add_argument("--index-rebuild", action="store_true",
                     help="rebuild throughput of the workload's index while a decode is served (one JSON line)")
     args = ap.parse_args(argv)
@@ -751,6 +815,8 @@ def main(argv=None):
         run_reference(args, cfg)
     elif args.index_rebuild:
         run_index_rebuild(args, cfg)
+    elif args.light_decoder:
+        run_light_decoder(args, cfg)
     else:
         run_gpu(args, cfg)
 

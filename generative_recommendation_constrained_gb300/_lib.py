@@ -35,9 +35,19 @@ class ZgError(RuntimeError):
         self.status = status
 
 
+ZG_MAX_DECO_LAYERS = 4
+
+
+class zg_deco(C.Structure):
+    _fields_ = [("M", C.c_int32), ("heads", C.c_int32), ("ffn", C.c_int32), ("layers", C.c_int32),
+                ("E", C.c_void_p * ZG_MAX_STEPS), ("P", C.c_void_p)] + \
+               [(n, C.c_void_p * ZG_MAX_DECO_LAYERS) for n in ("Wq", "Wk", "Wv", "Wo", "W1", "W2")]
+
+
 class zg_model(C.Structure):
     _fields_ = [("L", C.c_int32), ("V", C.c_int32), ("d", C.c_int32), ("w_dtype", C.c_int32),
-                ("C", C.c_void_p * ZG_MAX_STEPS), ("W", C.c_void_p * ZG_MAX_STEPS)]
+                ("C", C.c_void_p * ZG_MAX_STEPS), ("W", C.c_void_p * ZG_MAX_STEPS),
+                ("deco", C.POINTER(zg_deco))]
 
 
 class zg_build_opts(C.Structure):
@@ -62,7 +72,7 @@ class zg_step_trace(C.Structure):
     _fields_ = [("variant", C.c_int32), ("live_beams", C.c_int32), ("legal_slots", C.c_int64),
                 ("chunks", C.c_int64), ("unique_tokens", C.c_int64), ("index_bytes", C.c_int64),
                 ("ms_gather", C.c_float), ("ms_project", C.c_float), ("ms_select", C.c_float),
-                ("reserved", C.c_float)]
+                ("ms_model", C.c_float)]
 
 
 class zg_trace(C.Structure):
@@ -222,14 +232,31 @@ def zg_index_load(path: str, residency: int = ZG_RESIDENT_DEVICE, stream: int = 
     return Index(h.value)
 
 
-def make_model(L: int, V: int, d: int, w_dtype: int, C_ptrs, W_ptrs) -> zg_model:
+def make_model(L: int, V: int, d: int, w_dtype: int, C_ptrs, W_ptrs, deco: zg_deco | None = None) -> zg_model:
     m = zg_model()
     m.L, m.V, m.d, m.w_dtype = L, V, d, w_dtype
     for s, p in enumerate(C_ptrs):
         m.C[s] = _ptr(p)
     for s, p in enumerate(W_ptrs):
         m.W[s] = _ptr(p)
+    if deco is not None:
+        m.deco = C.pointer(deco)
+        m._deco_ref = deco          # keeps the struct alive with the model
     return m
+
+
+def make_deco(M: int, heads: int, ffn: int, E_ptrs, P_ptr, Wq, Wk, Wv, Wo, W1, W2) -> zg_deco:
+    """zg_deco from device pointers (per layer lists for the matrices)."""
+    t = zg_deco()
+    t.M, t.heads, t.ffn, t.layers = M, heads, ffn, len(Wq)
+    for s, p in enumerate(E_ptrs):
+        t.E[s] = _ptr(p)
+    t.P = _ptr(P_ptr)
+    for name, ptrs in (("Wq", Wq), ("Wk", Wk), ("Wv", Wv), ("Wo", Wo), ("W1", W1), ("W2", W2)):
+        arr = getattr(t, name)
+        for l, p in enumerate(ptrs):
+            arr[l] = _ptr(p)
+    return t
 
 
 def zg_plan_force(idx: Index, B: int, beam: int, variant) -> Plan:

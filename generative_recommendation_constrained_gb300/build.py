@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libzerogr.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["index_build.cpp", "engine.cpp", "kernels.cu", "kernels_tc.cu", "naive.cu", "decode_static.cu"]
+SOURCES = ["index_build.cpp", "engine.cpp", "kernels.cu", "kernels_tc.cu", "naive.cu", "decode_static.cu", "deco.cu"]
 
 
 def _nvcc() -> str:

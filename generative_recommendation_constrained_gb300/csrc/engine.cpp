@@ -44,6 +44,8 @@ struct Dims {
   bool split_h;              // half weights: the hidden as hi + lo operands
   bool need_mask;            // per-beam legal bitmaps (score-first, or chunk tops on sparse tables)
   bool sparse[ZG_MAX_STEPS]; // the step's table is sparse (constrained)
+  const zg_deco* deco;       // light decoder producing the hidden vectors, or null
+  int dM, dffn, dlayers;     // its concept vectors, MLP width, layers
 };
 
 // The automatic choice of how a full step hands its scores to the select:
@@ -55,6 +57,7 @@ struct Dims {
 bool auto_tops(const Dims&, int) { return false; }
 
 struct WsLayout {
+  size_t dX, dA, dQ, dO, dF, dKc, dVc, dKs, dVs, dH;  // light decoder
   size_t tok_hist, par_hist, row[2], cum[2], h[2], hhi, hlo, Z, part, ptop, part_all, mask, naive_cnt, naive_off,
       naive_list, naive_temp, trace, u_stage, o_sids, o_scores, total;
   size_t trace_bytes;
@@ -102,10 +105,23 @@ WsLayout layout(const Dims& m, bool host_io) {
     w.naive_list = take(m.naive_rows * 16);
     w.naive_temp = take(m.naive_rows * (size_t)m.d * esize(m.w_dtype));
   }
+  if (m.deco) {  // work rows, keys and values by position, hidden vectors
+    const size_t rows = std::max((size_t)m.B * m.dM, BW);
+    w.dX = take(rows * m.d * 4);
+    w.dA = take(rows * m.d * 4);
+    w.dQ = take(rows * m.d * 4);
+    w.dO = take(rows * m.d * 4);
+    w.dF = take(rows * (size_t)m.dffn * 4);
+    w.dKc = take((size_t)m.dlayers * m.B * m.dM * m.d * 4);
+    w.dVc = take((size_t)m.dlayers * m.B * m.dM * m.d * 4);
+    w.dKs = take((size_t)m.dlayers * (m.L + 1) * BW * m.d * 4);
+    w.dVs = take((size_t)m.dlayers * (m.L + 1) * BW * m.d * 4);
+    w.dH = take(BW * m.d * 4);
+  }
   w.trace_bytes = 32 + (size_t)((m.V + 31) / 32) * 4;  // 4 counters + token mask
   w.trace = take(w.trace_bytes);
   if (host_io) {
-    w.u_stage = take((size_t)m.B * m.d * 4);
+    w.u_stage = take((size_t)m.B * (m.deco ? m.dM : 1) * m.d * 4);
     w.o_sids = take((size_t)m.B * m.K * m.L * 4);
     w.o_scores = take((size_t)m.B * m.K * 4);
   }
@@ -125,7 +141,7 @@ zg_status check_common(const zg_index* idx, const zg_model* model, int B, int be
   for (int s = 0; s < m.L; ++s) {
     if (!m.W[s]) return fail(ZG_ERR_INVALID_ARG, "model.W[s] is NULL");
     if (reinterpret_cast<uintptr_t>(m.W[s]) % 16) return fail(ZG_ERR_INVALID_ARG, "model.W[s] not 16-byte aligned");
-    if (s < m.L - 1) {
+    if (s < m.L - 1 && !m.deco) {
       if (!m.C[s]) return fail(ZG_ERR_INVALID_ARG, "model.C[s] is NULL");
       if (reinterpret_cast<uintptr_t>(m.C[s]) % 16) return fail(ZG_ERR_INVALID_ARG, "model.C[s] not 16-byte aligned");
     }
@@ -138,7 +154,28 @@ zg_status check_common(const zg_index* idx, const zg_model* model, int B, int be
       return fail(ZG_ERR_INVALID_ARG, "index is host-resident; build or load it with ZG_RESIDENT_DEVICE");
     if (idx->L != m.L || idx->V != m.V) return fail(ZG_ERR_INVALID_ARG, "index and model disagree on L or V");
   }
+  if (m.deco) {
+    const zg_deco& w = *m.deco;
+    if (w.M < 1 || w.M > 8) return fail(ZG_ERR_INVALID_ARG, "deco.M must be in [1, 8]");
+    if (w.layers < 1 || w.layers > ZG_MAX_DECO_LAYERS) return fail(ZG_ERR_INVALID_ARG, "deco.layers must be in [1, 4]");
+    if (w.heads < 1 || m.d % w.heads != 0 || m.d / w.heads > 256)
+      return fail(ZG_ERR_INVALID_ARG, "deco.heads must divide d with d / heads <= 256");
+    if (w.ffn < 4 || w.ffn % 4 != 0) return fail(ZG_ERR_INVALID_ARG, "deco.ffn must be a positive multiple of 4");
+    auto bad = [](const float* p) { return !p || reinterpret_cast<uintptr_t>(p) % 16; };
+    if (bad(w.P)) return fail(ZG_ERR_INVALID_ARG, "deco.P is NULL or not 16-byte aligned");
+    for (int s = 0; s < m.L - 1; ++s)
+      if (bad(w.E[s])) return fail(ZG_ERR_INVALID_ARG, "deco.E[s] is NULL or not 16-byte aligned");
+    for (int l = 0; l < w.layers; ++l)
+      if (bad(w.Wq[l]) || bad(w.Wk[l]) || bad(w.Wv[l]) || bad(w.Wo[l]) || bad(w.W1[l]) || bad(w.W2[l]))
+        return fail(ZG_ERR_INVALID_ARG, "deco weight matrix is NULL or not 16-byte aligned");
+  }
   Dims d{};
+  d.deco = m.deco;
+  if (m.deco) {
+    d.dM = m.deco->M;
+    d.dffn = m.deco->ffn;
+    d.dlayers = m.deco->layers;
+  }
   d.L = m.L;
   d.V = m.V;
   d.d = m.d;
@@ -259,13 +296,18 @@ StepLaunch make_launch(const Run& r, int s, int variant) {
     a.h_prev = (s == 2) ? r.u : F32(r.w.h[pi]);
     a.C_prev = r.model->C[s - 2];
   }
+  if (m.deco) {  // hidden vectors from the light decoder, computed before the step
+    a.hpre = F32(r.w.dH);
+    a.h_prev = nullptr;
+    a.C_prev = nullptr;
+  }
   a.u = r.u;
   a.W = r.model->W[s - 1];
   const bool full = (variant == ZG_FULL) || !r.idx || m.score_first;
   const bool naive = !full && variant == ZG_NAIVE;
   // hidden of this step's beams: the next step's parents (s < L) and the
   // full projection's (or naive scores') input; at step 1 it is u itself
-  a.h_out = (s >= 2 && (s < m.L || full || naive)) ? F32(r.w.h[s & 1]) : nullptr;
+  a.h_out = (!m.deco && s >= 2 && (s < m.L || full || naive)) ? F32(r.w.h[s & 1]) : nullptr;
   a.Z = F32(r.w.Z);
   a.row_out = r.idx ? U32(r.w.row[s & 1]) : nullptr;
   a.cum_out = F32(r.w.cum[s & 1]);
@@ -326,7 +368,7 @@ StepLaunch make_launch(const Run& r, int s, int variant) {
     // from the projection's own operands
     a.ptop = reinterpret_cast<const float2*>(r.ws + r.w.ptop);
     a.Z = nullptr;
-    const float* H = (s >= 2) ? a.h_out : r.u;
+    const float* H = a.hpre ? a.hpre : ((s >= 2) ? a.h_out : r.u);
     a.hq = H;
     if (m.w_dtype != ZG_F32) {
       a.hq_hi = r.ws + r.w.hhi;
@@ -341,8 +383,8 @@ zg_status run_step(const Run& r, int s, int variant, cudaStream_t st, const Step
   cudaError_t e;
   if (tm) cudaEventRecord(tm->ev[0], st);
   if (variant == ZG_NAIVE && r.m.naive[s - 1]) {
-    const float* H = r.u;
-    if (s >= 2) {
+    const float* H = a.hpre ? a.hpre : r.u;
+    if (s >= 2 && !a.hpre) {
       e = launch_gather_add(a, a.h_out, st);
       if (e != cudaSuccess) return cuda_fail(e, "gather-add launch");
       H = a.h_out;
@@ -361,8 +403,8 @@ zg_status run_step(const Run& r, int s, int variant, cudaStream_t st, const Step
     e = launch_selective(a, st);
     if (e != cudaSuccess) return cuda_fail(e, "selective projection launch");
   } else {
-    const float* H = r.u;
-    if (s >= 2) {
+    const float* H = a.hpre ? a.hpre : r.u;
+    if (s >= 2 && !a.hpre) {
       e = launch_gather_add(a, a.h_out, st);
       if (e != cudaSuccess) return cuda_fail(e, "gather-add launch");
       H = a.h_out;
@@ -428,6 +470,41 @@ zg_status prepare(const zg_index* idx, const zg_plan* plan, const zg_model* mode
   return get_status_ptr(&r->status);
 }
 
+// The light decoder's step s: hidden vectors of the beams entering step s.
+zg_status run_deco_step(const Run& r, int s, cudaStream_t st) {
+  const Dims& m = r.m;
+  const size_t BW = (size_t)m.B * m.beam;
+  auto F32 = [&](size_t off) { return reinterpret_cast<float*>(r.ws + off); };
+  DecoStep a{};
+  a.s = s;
+  a.L = m.L;
+  a.B = m.B;
+  a.Wc = (s == 1) ? 1 : m.beam;
+  a.beam = m.beam;
+  a.M = m.dM;
+  a.d = m.d;
+  a.heads = m.deco->heads;
+  a.concepts = r.u;
+  if (s >= 2) {
+    a.tok_in = reinterpret_cast<const int32_t*>(r.ws + r.w.tok_hist) + (size_t)(s - 2) * BW;
+    a.cum_in = F32(r.w.cum[(s - 1) & 1]);
+  }
+  a.par_hist = reinterpret_cast<const int32_t*>(r.ws + r.w.par_hist);
+  a.X = F32(r.w.dX);
+  a.A = F32(r.w.dA);
+  a.Q = F32(r.w.dQ);
+  a.O = F32(r.w.dO);
+  a.F = F32(r.w.dF);
+  a.Kc = F32(r.w.dKc);
+  a.Vc = F32(r.w.dVc);
+  a.Ks = F32(r.w.dKs);
+  a.Vs = F32(r.w.dVs);
+  a.H = F32(r.w.dH);
+  cudaError_t e = launch_deco_step(*m.deco, a, st);
+  if (e != cudaSuccess) return cuda_fail(e, "light decoder launch");
+  return ZG_OK;
+}
+
 constexpr int kClusterCTAs = 8;  // default CTAs of the fused kernel's cluster (one cluster per request)
 
 int variant_of(const Run& r, const zg_plan* plan, int s) {
@@ -437,7 +514,7 @@ int variant_of(const Run& r, const zg_plan* plan, int s) {
 // First step of the trailing run of selective steps that zg_decode fuses
 // (L+1: none).
 int fused_from(const Run& r, const zg_plan* plan) {
-  if (!r.idx || r.m.score_first || (plan && !plan->fused)) return r.m.L + 1;
+  if (!r.idx || r.m.score_first || r.m.deco || (plan && !plan->fused)) return r.m.L + 1;
   int s0 = r.m.L + 1;
   while (s0 > 1 && variant_of(r, plan, s0 - 1) == ZG_SELECTIVE) --s0;
   return s0;
@@ -513,6 +590,10 @@ zg_status decode_steps(const Run& r, const zg_plan* plan, cudaStream_t st, cudaE
   for (int s = 1; s < s0; ++s) {
     const int v = variant_of(r, plan, s);
     NvtxRange step(step_range_name(s, v));
+    if (r.m.deco) {
+      zg_status e = run_deco_step(r, s, st);
+      if (e != ZG_OK) return e;
+    }
     zg_status e = run_step(r, s, v, st);
     if (e != ZG_OK) return e;
   }
@@ -776,7 +857,8 @@ zg_status zg_decode_host(const zg_index* idx, const zg_plan* plan, const zg_mode
   float* u_dev = reinterpret_cast<float*>(r.ws + r.w.u_stage);
   int32_t* sids_dev = reinterpret_cast<int32_t*>(r.ws + r.w.o_sids);
   float* sc_dev = reinterpret_cast<float*>(r.ws + r.w.o_scores);
-  cudaError_t e = cudaMemcpyAsync(u_dev, u_host, (size_t)B * r.m.d * 4, cudaMemcpyHostToDevice, s);
+  cudaError_t e = cudaMemcpyAsync(u_dev, u_host, (size_t)B * (r.m.deco ? r.m.dM : 1) * r.m.d * 4,
+                                  cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return cuda_fail(e, "zg_decode_host: copy of u");
   r.u = u_dev;
   r.out_sids = sids_dev;
@@ -838,6 +920,7 @@ zg_status zg_tune(const zg_index* idx, const zg_model* model, const float* warm_
   for (int step = 1; step <= m.L && st == ZG_OK; ++step) {
     float best = INFINITY;
     int best_v = ZG_SELECTIVE;
+    if (m.deco && (st = run_deco_step(r, step, s)) != ZG_OK) break;  // the entering beams' hidden vectors
     for (int v = ZG_SELECTIVE; v <= ZG_FULL && st == ZG_OK; ++v) {
       for (int i = 0; i < 2 && st == ZG_OK; ++i) st = run_step(r, step, v, s);
       if (st != ZG_OK) break;
@@ -934,7 +1017,7 @@ zg_status zg_decode_trace(const zg_index* idx, const zg_plan* plan, const zg_mod
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   std::memset(trace, 0, sizeof(*trace));
   trace->L = r.m.L;
-  constexpr int kEv = 4 * ZG_MAX_STEPS + 4;
+  constexpr int kEv = 6 * ZG_MAX_STEPS + 4;  // 4 a step, 2 a step for the light decoder, 4 for the whole
   cudaEvent_t ev[kEv] = {};
   int made = 0;
   cudaError_t e = cudaSuccess;
@@ -971,6 +1054,12 @@ zg_status zg_decode_trace(const zg_index* idx, const zg_plan* plan, const zg_mod
     const int v = variant_of(r, plan, step);
     StepTimer tm;
     for (int j = 0; j < 4; ++j) tm.ev[j] = ev[4 * (step - 1) + j];
+    cudaEvent_t* mev = &ev[4 * ZG_MAX_STEPS + 2 * (step - 1)];
+    if (r.m.deco) {
+      cudaEventRecord(mev[0], s);
+      if ((st = run_deco_step(r, step, s)) != ZG_OK) break;
+      cudaEventRecord(mev[1], s);
+    }
     st = run_step(r, step, v, s, &tm);
     if (st != ZG_OK) break;
     // untimed: what this step worked on (its entering state is still intact)
@@ -1001,6 +1090,7 @@ zg_status zg_decode_trace(const zg_index* idx, const zg_plan* plan, const zg_mod
     t.ms_gather = (v == ZG_NAIVE || (v == ZG_FULL && (step >= 2 || r.m.w_dtype != ZG_F32))) ? g : 0.f;
     t.ms_project = pj;
     t.ms_select = q;
+    if (r.m.deco) cudaEventElapsedTime(&t.ms_model, mev[0], mev[1]);
   }
   cleanup();
   return st;

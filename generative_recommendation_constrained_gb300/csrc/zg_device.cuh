@@ -187,7 +187,9 @@ __device__ __forceinline__ void score_chunk(const StepLaunch& a, int q, int k, c
   {
     const float* hp;
     const float* cr = nullptr;
-    if (a.s == 1) {
+    if (a.hpre) {  // the light decoder's hidden vector
+      hp = a.hpre + (size_t)b * d;
+    } else if (a.s == 1) {
       hp = a.u + (size_t)q * d;
     } else {
       hp = a.h_prev + ((size_t)q * a.Wp + bs.par) * d;

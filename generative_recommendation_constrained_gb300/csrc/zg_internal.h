@@ -1,6 +1,7 @@
 // Internal declarations of the zerogr library (host engine <-> kernels).
 #pragma once
 
+#include <algorithm>
 #include <cstddef>
 #include <cstdint>
 #include <string>
@@ -68,6 +69,7 @@ struct StepLaunch {
   const int32_t* par_in;   // parent index (within the request) of each beam
   const int32_t* tok_in;   // token chosen at step s-1
   const float* u;          // [B][d]
+  const float* hpre;       // [B*Wc][d] hidden vectors given by the light decoder (then no gather-add), or null
   const float* h_prev;     // [B*Wp][d] hidden of the previous step's beams (s >= 3)
   const float* C_prev;     // C_{s-1} [V][d] (s >= 2)
   const void* W;           // W_s [V][d]
@@ -160,6 +162,21 @@ constexpr int kMaxPrefetch = 24;
 cudaError_t launch_decode_cluster(const StepLaunch* steps, int s0, int L, int G, const PrefetchRegion* pf, int npf,
                                   cudaStream_t st);
 cudaError_t status_word(uint32_t** dev_ptr);   // per-device status word address
+// One step of the light decoder (deco.cu): the new positions' rows through
+// every layer, keys and values stored, hidden vectors of the beams entering
+// step s into H.
+struct DecoStep {
+  int32_t s, L, B, Wc, beam, M, d, heads;
+  const float* concepts;   // [B][M][d] (the decode's input)
+  const int32_t* tok_in;   // [B*beam] token chosen at step s-1 (s >= 2)
+  const float* cum_in;     // [B*beam] entering scores (-inf: dead beam), s >= 2
+  const int32_t* par_hist; // [L-1][B*beam] parent index history
+  float *X, *A, *Q, *O, *F;                 // [rows][d] (F: [rows][ffn]) work rows
+  float *Kc, *Vc;                           // [layers][B*M][d] concept keys / values
+  float *Ks, *Vs;                           // [layers][L+1][B*beam][d] token keys / values by step
+  float* H;                                 // [B*Wc][d] output hidden vectors
+};
+cudaError_t launch_deco_step(const zg_deco& w, const DecoStep& a, cudaStream_t st);
 // tensor-core full projection (kernels_tc.cu): H = hi + lo in W's half type
 cudaError_t launch_split_h(const float* H, void* hi, void* lo, size_t n, int w_dtype, cudaStream_t st);
 cudaError_t launch_full_tc(const void* hi, const void* lo, const void* W, float* Z, int M, int V, int d, int ldz,

@@ -19,16 +19,31 @@ def _to_device_weights(w: np.ndarray, w_dtype: str, device) -> torch.Tensor:
     raise ValueError(w_dtype)
 
 
+def _f32(x, device):
+    return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(device)
+
+
 class DeviceModel:
-    """Uploads a synthetic model (C_s float32, W_s in its storage dtype) and
+    """Uploads a synthetic model (C_s float32, W_s in its storage dtype) and,
+    optionally, a light decoder's weights (deco: the hidden vectors then come
+    from the decoder and the decode's input is the concept vectors), and
     builds the zg_model struct pointing at the device copies."""
 
-    def __init__(self, model, device="cuda"):
+    def __init__(self, model, device="cuda", deco=None):
         self.L, self.V, self.d, self.w_dtype = model.L, model.V, model.d, model.w_dtype
-        self.C = [torch.from_numpy(np.ascontiguousarray(c, np.float32)).to(device) for c in model.C]
+        self.C = [_f32(c, device) for c in model.C]
         self.W = [_to_device_weights(w, model.w_dtype, device) for w in model.W]
+        dstruct = None
+        if deco is not None:
+            self.deco = {"E": [_f32(e, device) for e in deco.E], "P": _f32(deco.P, device)}
+            for n in ("Wq", "Wk", "Wv", "Wo", "W1", "W2"):
+                self.deco[n] = [_f32(w, device) for w in getattr(deco, n)]
+            t = self.deco
+            dstruct = Z.make_deco(deco.M, deco.heads, deco.ffn, [e.data_ptr() for e in t["E"]],
+                                  t["P"].data_ptr(), *[[w.data_ptr() for w in t[n]]
+                                                       for n in ("Wq", "Wk", "Wv", "Wo", "W1", "W2")])
         self.struct = Z.make_model(self.L, self.V, self.d, Z.DTYPES[self.w_dtype],
-                                   [c.data_ptr() for c in self.C], [w.data_ptr() for w in self.W])
+                                   [c.data_ptr() for c in self.C], [w.data_ptr() for w in self.W], dstruct)
 
 
 class Decoder:

@@ -74,17 +74,54 @@ typedef enum { ZG_SCORES_AUTO = 0, ZG_SCORES_WRITTEN = 1, ZG_SCORES_CHUNK_TOPS =
 typedef struct zg_index zg_index; /* opaque: step tables + host header */
 typedef struct zg_plan zg_plan;   /* opaque: per-step variant choice   */
 
-/* The synthetic model the decoder scores with ([Pipeline] stage 1 is the
- * model's hidden vector; here h = u + sum_{j<s} C_j[t_j]).
+#define ZG_MAX_DECO_LAYERS 4
+
+/* A light causal decoder producing each step's hidden vector ("Separating
+ * Thinking from Spelling", AI Papers Daily digest: the backbone emits a fixed
+ * next-item concept once; a light 2-layer, 256-wide causal decoder
+ * conditioned on the concept and the generated prefix runs the
+ * trie-constrained beam search).  The hidden vector of a beam with prefix
+ * t_1..t_{s-1} at step s is the output of the last position of the sequence
+ * [c_1 .. c_M, E_1[t_1] .. E_{s-1}[t_{s-1}]], each row plus its position
+ * embedding, after `layers` pre-norm layers
+ *   x += attn(norm(x)) Wo^T,  attn = causal multi-head attention of
+ *        (norm(x) Wq^T, norm(x) Wk^T, norm(x) Wv^T), scores / sqrt(d/heads);
+ *   x += relu(norm(x) W1^T) W2^T;
+ * and a final norm; norm(x) = x / sqrt(mean(x^2) + 1e-6) per row.
+ * All device float32, row-major [out][in], 16-byte aligned, caller-owned:
+ *   E[s]: [V][d], s = 0..L-2;  P: [M + L - 1][d];
+ *   Wq, Wk, Wv, Wo[l]: [d][d];  W1[l]: [ffn][d];  W2[l]: [d][ffn].
+ * Limits: 1 <= M <= 8, 1 <= layers <= ZG_MAX_DECO_LAYERS, heads divides d
+ * with d / heads <= 256, ffn a multiple of 4. */
+typedef struct {
+  int32_t M, heads, ffn, layers;
+  const float* E[ZG_MAX_STEPS];
+  const float* P;
+  const float* Wq[ZG_MAX_DECO_LAYERS];
+  const float* Wk[ZG_MAX_DECO_LAYERS];
+  const float* Wv[ZG_MAX_DECO_LAYERS];
+  const float* Wo[ZG_MAX_DECO_LAYERS];
+  const float* W1[ZG_MAX_DECO_LAYERS];
+  const float* W2[ZG_MAX_DECO_LAYERS];
+} zg_deco;
+
+/* The model the decoder scores with ([Pipeline] stage 1 is the model's
+ * hidden vector).  Without a light decoder (deco NULL) it is the synthetic
+ * model h = u + sum_{j<s} C_j[t_j]:
  *   C[s]: device float32 [V][d], row-major, s = 0..L-2 (the table added after
  *         choosing the token of step s+1); C[L-1] is unused and may be NULL.
  *   W[s]: device w_dtype [V][d], row-major, s = 0..L-1 (output head of step
  *         s+1); rows must be 16-byte aligned (d % 8 == 0 ensures it).
+ *   deco: NULL, or a light decoder (zg_deco) producing the hidden vectors;
+ *         then C is unused and the decode's input u holds each request's M
+ *         concept vectors, device float32 [B][M][d], and zg_decode runs the
+ *         decoder before every step's projection (steps are not fused).
  * The struct and its pointer arrays are caller-owned. */
 typedef struct {
   int32_t L, V, d, w_dtype;
   const float* C[ZG_MAX_STEPS];
   const void* W[ZG_MAX_STEPS];
+  const zg_deco* deco;
 } zg_model;
 
 /* Index build options.  Zero-initialised = defaults. */
@@ -303,7 +340,7 @@ typedef struct {
   float ms_gather;        /* gather-add kernel (full steps at s >= 2), else 0       */
   float ms_project;       /* selective or full projection kernel                   */
   float ms_select;        /* masked log-softmax + cumulative add + top-K kernel     */
-  float reserved;
+  float ms_model;         /* the light decoder's kernels of this step (0 without)   */
 } zg_step_trace;
 
 typedef struct {
