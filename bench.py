@@ -291,6 +291,7 @@ def run_reference(args, cfg):
     model = synth.make_model(cfg.L, cfg.V, cfg.d, cfg.w_dtype, 0)
     u = synth.make_requests(cfg.batch, cfg.d, request_seed(0))
     t_trie = oracle_setup(cfg, sids, model, u)
+    _oracle_batch([0])  # warms the trie's first-step lookups once; the forked workers inherit them
     cores = os.cpu_count() or 1
     per_step = max(1, min(cfg.batch, args.ref_requests or cores))
     times = []
