@@ -58,6 +58,7 @@ bool auto_tops(const Dims&, int) { return false; }
 
 struct WsLayout {
   size_t dX, dA, dQ, dO, dF, dKc, dVc, dKs, dVs, dH;  // light decoder
+  size_t bscan;
   size_t tok_hist, par_hist, row[2], cum[2], h[2], hhi, hlo, Z, part, ptop, part_all, mask, naive_cnt, naive_off,
       naive_list, naive_temp, trace, u_stage, o_sids, o_scores, total;
   size_t trace_bytes;
@@ -118,6 +119,7 @@ WsLayout layout(const Dims& m, bool host_io) {
     w.dVs = take((size_t)m.dlayers * (m.L + 1) * BW * m.d * 4);
     w.dH = take(BW * m.d * 4);
   }
+  w.bscan = take((3 * BW + 1) * 4);  // stand-alone selective steps: chunk offsets, first entries, fan-outs
   w.trace_bytes = 32 + (size_t)((m.V + 31) / 32) * 4;  // 4 counters + token mask
   w.trace = take(w.trace_bytes);
   if (host_io) {
@@ -331,6 +333,7 @@ StepLaunch make_launch(const Run& r, int s, int variant) {
     a.part = nullptr;
   } else if (!full) {
     const StepMeta& sm = r.idx->steps[s - 1];
+    a.bscan = I32(r.w.bscan);
     a.mode = sm.fmt == ZG_FMT_SPARSE ? kSelSparse : kSelDense;
     a.nch = m.nch_sel[s - 1];
     a.S = m.S_sel[s - 1];

@@ -62,30 +62,111 @@ __device__ int select_large(const StepLaunch& a, int q, BeamTab& bt, SW& sw, uin
 }
 
 // ---------------------------------------------------------------------------
-// Stand-alone selective step: one warp per (beam, chunk) item, grid-stride,
-// chunk-major so the first warps get the non-empty chunks.
+// Stand-alone selective step over every request at once: the non-empty
+// (beam, 32-slot chunk) items of the whole batch are numbered by a per-step
+// scan of the beams' chunk counts, and every warp of the grid scores one
+// contiguous range of them, so the work is balanced across requests (a beam
+// with thousands of legal tokens is spread over many warps).
+//   k_beam_items: per beam its first index entry, fan-out and chunk count
+//                 (0 for a dead beam);
+//   k_scan_items: one CTA turns the chunk counts into exclusive offsets;
+//   k_selective:  the scoring.
 // ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_beam_items(const __grid_constant__ StepLaunch a) {
+  const int N = a.B * a.Wc;
+  int32_t* cnt = a.bscan;             // chunk counts, scanned in place by k_scan_items
+  int32_t* rp = a.bscan + N + 1;
+  int32_t* fo = rp + N;
+  for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < N; b += gridDim.x * blockDim.x) {
+    const int q = b / a.Wc, k = b - q * a.Wc;
+    const BeamState bs = load_beam(a, q, k);
+    int items = 0;
+    uint32_t r0 = 0, F = 0;
+    if (bs.row != kDeadRow) {
+      if (bs.row >= a.tab.rows) {
+        flag(a.status, kStatusRow);
+      } else {
+        r0 = a.tab.rowptr[bs.row];
+        F = a.tab.rowptr[bs.row + 1] - r0;
+        items = (a.mode == kSelSparse) ? (int)((F + kChunk - 1) / kChunk) : a.nch;
+      }
+    }
+    cnt[b] = items;
+    rp[b] = (int32_t)r0;
+    fo[b] = (int32_t)F;
+  }
+}
+
+__global__ void __launch_bounds__(1024) k_scan_items(int32_t* cnt, int N) {
+  __shared__ int32_t wsum[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (N + 1023) / 1024;
+  const int b0 = tid * per, b1 = min(N, b0 + per);
+  int sum = 0;
+  for (int b = b0; b < b1; ++b) sum += cnt[b];
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = wsum[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, w, o);
+      if (lane >= o) w += y;
+    }
+    wsum[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  int run = incl - sum + (warp > 0 ? wsum[warp - 1] : 0);
+  for (int b = b0; b < b1; ++b) {
+    const int c = cnt[b];
+    cnt[b] = run;
+    run += c;
+  }
+  if (tid == 1023) cnt[N] = run;  // the last thread ends at the total
+}
+
 template <typename WT, int VPL>
 __global__ void __launch_bounds__(256) k_selective(const __grid_constant__ StepLaunch a) {
   const int lane = threadIdx.x & 31;
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
   const int N = a.B * a.Wc;
-  const int64_t items = (int64_t)N * a.nch;
-  for (int64_t it = wid; it < items; it += nw) {
-    const int c = (int)(it / N);
-    const int b = (int)(it - (int64_t)c * N);
+  const int32_t* off = a.bscan;
+  const int32_t* rp = a.bscan + N + 1;
+  const int32_t* fo = rp + N;
+  const int total = off[N];
+  const int per = (total + nw - 1) / nw;
+  const int i0 = wid * per, i1 = min(total, i0 + per);
+  if (i0 >= i1) return;
+  // the beam of the range's first item (largest b with off[b] <= i0): a
+  // 32-way search, each lane probing one point of the current interval
+  int lo = 0, hi = N - 1;  // off[lo] <= i0 always holds
+  while (hi > lo) {
+    const int span = hi - lo;
+    const int p = lo + (int)(((long long)span * (lane + 1)) / 32);  // lane 31 probes hi
+    const unsigned ok = __ballot_sync(kFull, off[p] <= i0);
+    const int top = ok ? 31 - __clz(ok) : -1;  // highest lane whose point is <= i0
+    const int nlo = (top >= 0) ? lo + (int)(((long long)span * (top + 1)) / 32) : lo;
+    const int nhi = (top < 31) ? lo + (int)(((long long)span * (top + 2)) / 32) - 1 : hi;
+    lo = nlo;
+    hi = max(nlo, nhi);
+  }
+  int b = lo, loaded = -1;
+  BeamState bs;
+  for (int it = i0; it < i1; ++it) {
+    while (off[b + 1] <= it) ++b;
     const int q = b / a.Wc, k = b - q * a.Wc;
-    const BeamState bs = load_beam(a, q, k);
-    if (bs.row == kDeadRow) continue;
-    if (bs.row >= a.tab.rows) {
-      if (lane == 0) flag(a.status, kStatusRow);
-      continue;
+    if (b != loaded) {  // consecutive chunks of one beam share its state
+      bs = load_beam(a, q, k);
+      loaded = b;
     }
-    const uint32_t rp0 = a.tab.rowptr[bs.row];
-    const uint32_t F = a.tab.rowptr[bs.row + 1] - rp0;
-    if (a.mode == kSelSparse && (uint32_t)(c * kChunk) >= F) continue;  // empty chunk
-    score_chunk<WT, VPL>(a, q, k, bs, rp0, F, c, lane);
+    score_chunk<WT, VPL>(a, q, k, bs, (uint32_t)rp[b], (uint32_t)fo[b], it - off[b], lane);
   }
 }
 
@@ -537,22 +618,35 @@ int vpl_for(int d) {
 
 template <typename WT>
 cudaError_t launch_sel_t(const StepLaunch& a, cudaStream_t st) {
-  const int64_t items = (int64_t)a.B * a.Wc * a.nch;
-  if (items == 0) return cudaSuccess;
-  const int64_t want = (items + 7) / 8;
-  const int blocks = (int)std::min<int64_t>(want, (int64_t)sm_count() * 16);
+  const int N = a.B * a.Wc;
+  if (N == 0 || a.nch == 0) return cudaSuccess;
+  k_beam_items<<<std::max(1, std::min((N + 255) / 256, sm_count() * 4)), 256, 0, st>>>(a);
+  k_scan_items<<<1, 1024, 0, st>>>(a.bscan, N);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // persistent: as many CTAs as are resident at once (the occupancy of this
+  // instantiation), each warp one contiguous range of the items; fewer when
+  // there cannot be that many items
+  const int64_t items = (int64_t)N * a.nch;
+  auto launch = [&](auto kern) {
+    static int resident = 0;  // per instantiation
+    if (!resident) {
+      int per_sm = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0) != cudaSuccess || per_sm < 1) per_sm = 1;
+      resident = per_sm * sm_count();
+    }
+    const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((items + 7) / 8, (int64_t)resident));
+    kern<<<blocks, 256, 0, st>>>(a);
+    return cudaGetLastError();
+  };
   switch (vpl_for<WT>(a.d)) {
     case 1:
-      k_selective<WT, 1><<<blocks, 256, 0, st>>>(a);
-      break;
+      return launch(k_selective<WT, 1>);
     case 2:
-      k_selective<WT, 2><<<blocks, 256, 0, st>>>(a);
-      break;
+      return launch(k_selective<WT, 2>);
     default:
-      k_selective<WT, 4><<<blocks, 256, 0, st>>>(a);
-      break;
+      return launch(k_selective<WT, 4>);
   }
-  return cudaGetLastError();
 }
 
 template <typename WT, int VPL>

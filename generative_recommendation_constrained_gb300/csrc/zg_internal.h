@@ -79,6 +79,9 @@ struct StepLaunch {
   float2* part;            // [B][pq] (max, sum exp) of the legal tokens per chunk
   const float2* part_all;  // [B][pq] (max, sum exp) of every token per chunk: score-first
                            // order (log-softmax over the codebook), else NULL
+  int32_t* bscan;          // stand-alone selective steps: [B*Wc + 1] exclusive prefix of the beams'
+                           // non-empty chunk counts (the last entry is the total), then [B*Wc] of
+                           // each beam's first index entry and [B*Wc] of its fan-out
   int32_t mask_by_beam;    // tab.bitmap holds one row per beam (b = q*Wc + k), not per
                            // index row: a sparse step's legal lists expanded (score-first)
   // chunk-top select (full steps whose scores were not written): ptop[q*pq +
