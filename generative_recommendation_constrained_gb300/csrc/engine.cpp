@@ -119,7 +119,7 @@ WsLayout layout(const Dims& m, bool host_io) {
     w.dVs = take((size_t)m.dlayers * (m.L + 1) * BW * m.d * 4);
     w.dH = take(BW * m.d * 4);
   }
-  w.bscan = take((3 * BW + 1) * 4);  // stand-alone selective steps: chunk offsets, first entries, fan-outs
+  w.bscan = take((3 * BW + kItemBlocks) * 4);  // stand-alone selective steps: chunk offsets, first entries, fan-outs, CTA totals
   w.trace_bytes = 32 + (size_t)((m.V + 31) / 32) * 4;  // 4 counters + token mask
   w.trace = take(w.trace_bytes);
   if (host_io) {

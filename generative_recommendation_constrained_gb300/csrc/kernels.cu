@@ -63,48 +63,28 @@ __device__ int select_large(const StepLaunch& a, int q, BeamTab& bt, SW& sw, uin
 
 // ---------------------------------------------------------------------------
 // Stand-alone selective step over every request at once: the non-empty
-// (beam, 32-slot chunk) items of the whole batch are numbered by a per-step
-// scan of the beams' chunk counts, and every warp of the grid scores one
-// contiguous range of them, so the work is balanced across requests (a beam
-// with thousands of legal tokens is spread over many warps).
+// (beam, 32-slot chunk) items of the whole batch are numbered by a scan of
+// the beams' chunk counts, and every warp of the grid scores one contiguous
+// range of them, so the work is balanced across requests (a beam with
+// thousands of legal tokens is spread over many warps).
 //   k_beam_items: per beam its first index entry, fan-out and chunk count
-//                 (0 for a dead beam);
-//   k_scan_items: one CTA turns the chunk counts into exclusive offsets;
-//   k_selective:  the scoring.
+//                 (0 for a dead beam); each CTA scans its beams' counts into
+//                 offsets within the CTA and writes its total;
+//   k_selective:  every CTA scans the (at most kItemBlocks) CTA totals in
+//                 shared memory, so a beam's first item is its CTA's offset
+//                 plus its offset within the CTA; then the scoring.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) k_beam_items(const __grid_constant__ StepLaunch a) {
-  const int N = a.B * a.Wc;
-  int32_t* cnt = a.bscan;             // chunk counts, scanned in place by k_scan_items
-  int32_t* rp = a.bscan + N + 1;
-  int32_t* fo = rp + N;
-  for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < N; b += gridDim.x * blockDim.x) {
-    const int q = b / a.Wc, k = b - q * a.Wc;
-    const BeamState bs = load_beam(a, q, k);
-    int items = 0;
-    uint32_t r0 = 0, F = 0;
-    if (bs.row != kDeadRow) {
-      if (bs.row >= a.tab.rows) {
-        flag(a.status, kStatusRow);
-      } else {
-        r0 = a.tab.rowptr[bs.row];
-        F = a.tab.rowptr[bs.row + 1] - r0;
-        items = (a.mode == kSelSparse) ? (int)((F + kChunk - 1) / kChunk) : a.nch;
-      }
-    }
-    cnt[b] = items;
-    rp[b] = (int32_t)r0;
-    fo[b] = (int32_t)F;
-  }
+// beams per k_beam_items CTA: a multiple of 256, enough for at most kItemBlocks CTAs
+__host__ __device__ __forceinline__ int item_block_beams(int N) {
+  const int per = (N + kItemBlocks - 1) / kItemBlocks;
+  return ((per + 255) / 256) * 256;
 }
 
-__global__ void __launch_bounds__(1024) k_scan_items(int32_t* cnt, int N) {
-  __shared__ int32_t wsum[32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int per = (N + 1023) / 1024;
-  const int b0 = tid * per, b1 = min(N, b0 + per);
-  int sum = 0;
-  for (int b = b0; b < b1; ++b) sum += cnt[b];
-  int incl = sum;
+// Exclusive scan of one value per thread over a 256-thread CTA; *total gets
+// the CTA's sum.  wsum: 8 ints of shared memory, free again on return.
+__device__ __forceinline__ int cta256_exclusive_scan(int v, int32_t* wsum, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int y = __shfl_up_sync(kFull, incl, o);
@@ -112,61 +92,123 @@ __global__ void __launch_bounds__(1024) k_scan_items(int32_t* cnt, int N) {
   }
   if (lane == 31) wsum[warp] = incl;
   __syncthreads();
-  if (warp == 0) {
-    int w = wsum[lane];
+  int before = 0, all = 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(kFull, w, o);
-      if (lane >= o) w += y;
-    }
-    wsum[lane] = w;  // inclusive over warps
+  for (int w = 0; w < 8; ++w) {
+    const int x = wsum[w];
+    before += (w < warp) ? x : 0;
+    all += x;
   }
   __syncthreads();
-  int run = incl - sum + (warp > 0 ? wsum[warp - 1] : 0);
-  for (int b = b0; b < b1; ++b) {
-    const int c = cnt[b];
-    cnt[b] = run;
-    run += c;
+  *total = all;
+  return before + incl - v;
+}
+
+__global__ void __launch_bounds__(256) k_beam_items(const __grid_constant__ StepLaunch a) {
+  __shared__ int32_t wsum[8];
+  const int N = a.B * a.Wc;
+  const int bper = item_block_beams(N);
+  int32_t* loc = a.bscan;  // first item of each beam, counted from its CTA's first
+  int32_t* rp = loc + N;
+  int32_t* fo = rp + N;
+  int32_t* bsum = fo + N;  // items per CTA
+  const int b0 = blockIdx.x * bper, b1 = min(N, b0 + bper);
+  int carry = 0;
+  for (int base = b0; base < b1; base += 256) {
+    const int b = base + (int)threadIdx.x;
+    int items = 0;
+    uint32_t r0 = 0, F = 0;
+    if (b < b1) {
+      const int q = b / a.Wc, k = b - q * a.Wc;
+      const BeamState bs = load_beam(a, q, k);
+      if (bs.row != kDeadRow) {
+        if (bs.row >= a.tab.rows) {
+          flag(a.status, kStatusRow);
+        } else {
+          r0 = a.tab.rowptr[bs.row];
+          F = a.tab.rowptr[bs.row + 1] - r0;
+          items = (a.mode == kSelSparse) ? (int)((F + kChunk - 1) / kChunk) : a.nch;
+        }
+      }
+    }
+    int sum;
+    const int ex = cta256_exclusive_scan(items, wsum, &sum);
+    if (b < b1) {
+      loc[b] = carry + ex;
+      rp[b] = (int32_t)r0;
+      fo[b] = (int32_t)F;
+    }
+    carry += sum;
   }
-  if (tid == 1023) cnt[N] = run;  // the last thread ends at the total
+  if (threadIdx.x == 0) bsum[blockIdx.x] = carry;
 }
 
 template <typename WT, int VPL>
 __global__ void __launch_bounds__(256) k_selective(const __grid_constant__ StepLaunch a) {
+  __shared__ int32_t boff[kItemBlocks + 1];  // exclusive offsets of the k_beam_items CTAs, then the total
+  __shared__ int32_t wsum[8];
   const int lane = threadIdx.x & 31;
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
   const int N = a.B * a.Wc;
-  const int32_t* off = a.bscan;
-  const int32_t* rp = a.bscan + N + 1;
+  const int bper = item_block_beams(N);
+  const int nblk = (N + bper - 1) / bper;
+  const int32_t* loc = a.bscan;
+  const int32_t* rp = loc + N;
   const int32_t* fo = rp + N;
-  const int total = off[N];
+  const int32_t* bsum = fo + N;
+  {
+    constexpr int PT = kItemBlocks / 256;  // CTA totals per thread
+    int v[PT], sum = 0;
+#pragma unroll
+    for (int j = 0; j < PT; ++j) {
+      const int i = (int)threadIdx.x * PT + j;
+      v[j] = (i < nblk) ? bsum[i] : 0;
+      sum += v[j];
+    }
+    int all;
+    int run = cta256_exclusive_scan(sum, wsum, &all);
+#pragma unroll
+    for (int j = 0; j < PT; ++j) {
+      boff[threadIdx.x * PT + j] = run;
+      run += v[j];
+    }
+    if (threadIdx.x == 0) boff[kItemBlocks] = all;
+    __syncthreads();
+  }
+  const int total = boff[kItemBlocks];
+  // first item of beam p (p = N: the total)
+  auto off = [&](int p) { return (p >= N) ? total : boff[p / bper] + loc[p]; };
   const int per = (total + nw - 1) / nw;
   const int i0 = wid * per, i1 = min(total, i0 + per);
   if (i0 >= i1) return;
-  // the beam of the range's first item (largest b with off[b] <= i0): a
+  // the beam of the range's first item (largest b with off(b) <= i0): a
   // 32-way search, each lane probing one point of the current interval
-  int lo = 0, hi = N - 1;  // off[lo] <= i0 always holds
+  int lo = 0, hi = N - 1;  // off(lo) <= i0 always holds
   while (hi > lo) {
     const int span = hi - lo;
     const int p = lo + (int)(((long long)span * (lane + 1)) / 32);  // lane 31 probes hi
-    const unsigned ok = __ballot_sync(kFull, off[p] <= i0);
+    const unsigned ok = __ballot_sync(kFull, off(p) <= i0);
     const int top = ok ? 31 - __clz(ok) : -1;  // highest lane whose point is <= i0
     const int nlo = (top >= 0) ? lo + (int)(((long long)span * (top + 1)) / 32) : lo;
     const int nhi = (top < 31) ? lo + (int)(((long long)span * (top + 2)) / 32) - 1 : hi;
     lo = nlo;
     hi = max(nlo, nhi);
   }
-  int b = lo, loaded = -1;
+  int b = lo, loaded = -1, ob = off(lo), onext = off(lo + 1);
   BeamState bs;
   for (int it = i0; it < i1; ++it) {
-    while (off[b + 1] <= it) ++b;
+    while (onext <= it) {
+      ++b;
+      ob = onext;
+      onext = off(b + 1);
+    }
     const int q = b / a.Wc, k = b - q * a.Wc;
     if (b != loaded) {  // consecutive chunks of one beam share its state
       bs = load_beam(a, q, k);
       loaded = b;
     }
-    score_chunk<WT, VPL>(a, q, k, bs, (uint32_t)rp[b], (uint32_t)fo[b], it - off[b], lane);
+    score_chunk<WT, VPL>(a, q, k, bs, (uint32_t)rp[b], (uint32_t)fo[b], it - ob, lane);
   }
 }
 
@@ -620,8 +662,8 @@ template <typename WT>
 cudaError_t launch_sel_t(const StepLaunch& a, cudaStream_t st) {
   const int N = a.B * a.Wc;
   if (N == 0 || a.nch == 0) return cudaSuccess;
-  k_beam_items<<<std::max(1, std::min((N + 255) / 256, sm_count() * 4)), 256, 0, st>>>(a);
-  k_scan_items<<<1, 1024, 0, st>>>(a.bscan, N);
+  const int bper = item_block_beams(N);
+  k_beam_items<<<(N + bper - 1) / bper, 256, 0, st>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // persistent: as many CTAs as are resident at once (the occupancy of this

@@ -73,11 +73,18 @@ struct Vec<__half> {
   }
 };
 
-__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+// A weight row gathered in place: not kept in L1 (each SM meets a row only a
+// few times), kept in L2 ahead of other lines (evict_last): every row of the
+// step's codebook is gathered by many beams of the batch, and with normal
+// priority the rows were evicted by one another inside a step whenever L2
+// already held other data (about 9x the compulsory misses).
+__device__ __forceinline__ uint4 ldg_wrow(const void* p) {
   uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+  uint64_t pol;
+  asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
+               : "l"(p), "l"(pol));
   return r;
 }
 
@@ -247,7 +254,7 @@ __device__ __forceinline__ void score_chunk(const StepLaunch& a, int q, int k, c
 #pragma unroll
       for (int vv = 0; vv < VPL; ++vv) {
         const int v = lane + 32 * vv;
-        raw[rr][vv] = (ok && v < nvec) ? ldg_stream(wrow + v * E) : make_uint4(0, 0, 0, 0);
+        raw[rr][vv] = (ok && v < nvec) ? ldg_wrow(wrow + v * E) : make_uint4(0, 0, 0, 0);
       }
     }
 #pragma unroll

@@ -15,6 +15,7 @@ namespace zg {
 
 constexpr uint32_t kDeadRow = 0xFFFFFFFFu;
 constexpr int kChunk = 32;  // slots scored by one warp work item (one per lane)
+constexpr int kItemBlocks = 1024;  // CTAs of a stand-alone selective step's item count, at most
 
 // Device status bits (see zg_check_device_status).
 constexpr uint32_t kStatusRow = 1u;
@@ -79,9 +80,9 @@ struct StepLaunch {
   float2* part;            // [B][pq] (max, sum exp) of the legal tokens per chunk
   const float2* part_all;  // [B][pq] (max, sum exp) of every token per chunk: score-first
                            // order (log-softmax over the codebook), else NULL
-  int32_t* bscan;          // stand-alone selective steps: [B*Wc + 1] exclusive prefix of the beams'
-                           // non-empty chunk counts (the last entry is the total), then [B*Wc] of
-                           // each beam's first index entry and [B*Wc] of its fan-out
+  int32_t* bscan;          // stand-alone selective steps: [B*Wc] each beam's first non-empty
+                           // chunk counted from the first of its counting CTA, [B*Wc] its first
+                           // index entry, [B*Wc] its fan-out, [kItemBlocks] chunks per CTA
   int32_t mask_by_beam;    // tab.bitmap holds one row per beam (b = q*Wc + k), not per
                            // index row: a sparse step's legal lists expanded (score-first)
   // chunk-top select (full steps whose scores were not written): ptop[q*pq +
