@@ -73,6 +73,17 @@ struct Vec<__half> {
   }
 };
 
+// Accumulate the dot of 16 bytes of weights with the matching fp32 hidden
+// lanes h[0..E) into the pair s (even elements into s.x, odd into s.y), one
+// packed fp32x2 FMA per pair of elements; the caller adds s.x + s.y.
+template <typename WT>
+__device__ __forceinline__ void dot_pairs(const uint4& r, const float* h, float2& s) {
+  float w[Vec<WT>::E];
+  Vec<WT>::cvt(r, w);
+#pragma unroll
+  for (int e = 0; e < Vec<WT>::E; e += 2) s = __ffma2_rn(make_float2(w[e], w[e + 1]), make_float2(h[e], h[e + 1]), s);
+}
+
 // A weight row gathered in place: not kept in L1 (each SM meets a row only a
 // few times), kept in L2 ahead of other lines (evict_last): every row of the
 // step's codebook is gathered by many beams of the batch, and with normal
@@ -259,15 +270,10 @@ __device__ __forceinline__ void score_chunk(const StepLaunch& a, int q, int k, c
     }
 #pragma unroll
     for (int rr = 0; rr < GR; ++rr) {
-      float sacc = 0.f;
+      float2 s2 = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int vv = 0; vv < VPL; ++vv) {
-        float w[E];
-        VT::cvt(raw[rr][vv], w);
-#pragma unroll
-        for (int e = 0; e < E; ++e) sacc = fmaf(w[e], h[vv][e], sacc);
-      }
-      acc[GR * g + rr] = sacc;
+      for (int vv = 0; vv < VPL; ++vv) dot_pairs<WT>(raw[rr][vv], h[vv], s2);
+      acc[GR * g + rr] = s2.x + s2.y;
     }
   }
 #pragma unroll
