@@ -690,21 +690,67 @@ __device__ __forceinline__ uint32_t cand_key_kj(const StepLaunch& a, const BeamT
   return f2ord(bt.cum[k] + (z - bt.lse[k]));
 }
 
-// Stage the keys of every candidate in shared memory (four independent
+// Keys of U candidates (slot jj[u] of beam kk[u]; jj[u] < 0: none, key 0),
+// with the step format's branch taken once outside the per-candidate loops
+// so that the U loads of each kind are issued together.
+template <int U>
+__device__ __forceinline__ void cand_keys_batch(const StepLaunch& a, const BeamTab& bt, int q, const int* kk,
+                                                const int* jj, uint32_t* key) {
+  float z[U];
+  bool ok[U];
+  if (a.mode == kSelSparse || a.mode == kUncon) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      ok[u] = jj[u] >= 0;
+      z[u] = ok[u] ? a.Z[(size_t)q * a.zq + (size_t)kk[u] * a.S + jj[u]] : 0.f;
+    }
+  } else if (a.mode == kFullSparse) {
+    uint32_t c[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      ok[u] = jj[u] >= 0;
+      c[u] = ok[u] ? a.tab.col[bt.rp[kk[u]] + jj[u]] : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) z[u] = ok[u] ? a.Z[(size_t)q * a.zq + (size_t)kk[u] * a.S + c[u]] : 0.f;
+  } else {  // kSelDense, kFullDense: the legal word and the slot together
+    uint32_t w[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const bool any = jj[u] >= 0;
+      w[u] = any ? legal_bits(a, bt, q, kk[u])[jj[u] >> 5] : 0u;
+      z[u] = any ? a.Z[(size_t)q * a.zq + (size_t)kk[u] * a.S + jj[u]] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) ok[u] = jj[u] >= 0 && ((w[u] >> (jj[u] & 31)) & 1u);
+  }
+#pragma unroll
+  for (int u = 0; u < U; ++u) key[u] = ok[u] ? f2ord(bt.cum[kk[u]] + (z[u] - bt.lse[kk[u]])) : 0u;
+}
+
+// Stage the keys of every candidate in shared memory (eight independent
 // candidates a thread in flight).
 template <int NT>
 __device__ void stage_keys_global(const StepLaunch& a, int q, const BeamTab& bt, uint32_t* keys) {
+  constexpr int U = 8;
   const int total = bt.total;
-  for (int c0 = threadIdx.x; c0 < total; c0 += 4 * NT) {
-    uint32_t kk[4];
+  for (int c0 = threadIdx.x; c0 < total; c0 += U * NT) {
+    int kk[U], jj[U];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < U; ++u) {
       const int c = c0 + u * NT;
-      kk[u] = (c < total) ? cand_key(a, bt, q, c) : 0u;
+      kk[u] = 0;
+      jj[u] = -1;
+      if (c < total) {
+        kk[u] = upper_find(bt.start, a.Wc, c);
+        jj[u] = c - bt.start[kk[u]];
+      }
     }
+    uint32_t key[U];
+    cand_keys_batch<U>(a, bt, q, kk, jj, key);
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
-      if (c0 + u * NT < total) keys[c0 + u * NT] = kk[u];
+    for (int u = 0; u < U; ++u)
+      if (c0 + u * NT < total) keys[c0 + u * NT] = key[u];
   }
 }
 
@@ -1191,6 +1237,18 @@ __device__ void place_winners(const unsigned long long* list, int nl, int keep_n
       const unsigned long long v = warp_sort_desc(lane < nl ? list[lane] : 0ull, lane);
       if (lane < keep_n) sw.win[lane] = v;
     }
+  } else if (2 * nl <= NT) {
+    // two threads an entry, each counting over half of the list
+    const int i = tid >> 1, half = tid & 1;
+    const bool act = i < nl;
+    const unsigned long long x = act ? list[i] : 0ull;
+    int r = 0;
+    if (act) {
+      const int j0 = half ? (nl >> 1) : 0, j1 = half ? nl : (nl >> 1);
+      for (int j = j0; j < j1; ++j) r += (list[j] > x);
+    }
+    r += __shfl_xor_sync(kFull, r, 1);
+    if (act && !half && r < keep_n) sw.win[r] = x;
   } else if (nl <= NT) {
     if (tid < nl) {
       const unsigned long long x = list[tid];
@@ -1300,6 +1358,7 @@ __device__ int stage_passing_chunks(const StepLaunch& a, int q, BeamTab& bt, SW&
   int* cid = reinterpret_cast<int*>(spare);
   uint32_t* kst = spare + maxc;
   if (tid == 0) sw.nwin = 0;
+  for (int i = tid; i < kBins; i += NT) hist[i] = 0u;  // counted while the keys are staged
   __syncthreads();
   for (int i0 = 0; i0 < nitems; i0 += NT) {
     const int i = i0 + tid;
@@ -1314,39 +1373,38 @@ __device__ int stage_passing_chunks(const StepLaunch& a, int q, BeamTab& bt, SW&
   const int npass = sw.nwin;
   if (npass > maxc) return -1;
   const int ne = npass * kChunk;
+  const uint32_t hi = bt.kceil;
+  const int sh = bin_shift(tc, hi);
   constexpr int UL = 16;  // global loads a thread keeps in flight
   for (int e0 = tid; e0 < ne; e0 += UL * NT) {
-    uint32_t key[UL];
+    int kk[UL], jj[UL];
 #pragma unroll
     for (int u = 0; u < UL; ++u) {
       const int e = e0 + u * NT;
-      key[u] = 0u;
+      kk[u] = 0;
+      jj[u] = -1;  // no candidate
       if (e < ne) {
         const int item = cid[e >> 5];
         const int k = (int)kb[(size_t)item * st];
         const int j = (item - bt.istart[k]) * kChunk + (e & 31);
-        if (j < bt.cnt[k]) key[u] = cand_key_kj(a, bt, q, k, j);
+        kk[u] = k;
+        if (j < bt.cnt[k]) jj[u] = j;
       }
     }
+    uint32_t key[UL];
+    cand_keys_batch<UL>(a, bt, q, kk, jj, key);
 #pragma unroll
-    for (int u = 0; u < UL; ++u)
-      if (e0 + u * NT < ne) kst[e0 + u * NT] = key[u] >= tc ? key[u] : 0u;
-  }
-  for (int i = tid; i < kBins; i += NT) hist[i] = 0u;
-  __syncthreads();
-  const uint32_t hi = bt.kceil;
-  const int sh = bin_shift(tc, hi);
-  for (int e = tid; e < ne; e += NT) {
-    const uint32_t key = kst[e];
-    if (key) atomicAdd(&hist[bin_of(key, tc, sh)], 1u);
+    for (int u = 0; u < UL; ++u) {
+      const uint32_t k2 = key[u] >= tc ? key[u] : 0u;
+      if (e0 + u * NT < ne) kst[e0 + u * NT] = k2;
+      if (k2) atomicAdd(&hist[bin_of(k2, tc, sh)], 1u);
+    }
   }
   __syncthreads();
   if (hist_cut<NT>(hist, sw, (uint32_t)keep_n) < (uint32_t)keep_n) return -1;
   if (sw.cnt_gt + sw.cnt_eq > LCAP) return -1;
   const uint32_t t2 = tc + (sw.prefix << sh);
-  __syncthreads();  // every thread has read the cut before the list overwrites the histogram
-  if (tid == 0) sw.nwin = 0;
-  __syncthreads();
+  // hist_cut has zeroed sw.nwin and synchronised after its last histogram read
   for (int e0 = 0; e0 < ne; e0 += NT) {
     const int e = e0 + tid;
     const uint32_t key = (e < ne) ? kst[e] : 0u;
