@@ -29,6 +29,32 @@ namespace {
 using namespace dev;
 namespace cg = cooperative_groups;
 
+// Programmatic dependent launch inside a selective step (k_beam_items ->
+// k_selective -> k_select -> next step's k_beam_items): each of these kernels
+// is launched so that it may start while its predecessor finishes.  It first
+// waits for the predecessor's completion (griddepcontrol.wait) and only then
+// lets its own successor launch, so a kernel that starts early knows that
+// everything before its predecessor is complete; k_select builds its beam
+// table (beam states of the previous select, index rows) before its wait.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t st,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 constexpr int kSelThreads = 512;
 constexpr int kSelCap = 32768;       // keys staged in shared memory by k_select (one CTA a request)
 constexpr int kClusterThreads = 256;
@@ -106,6 +132,8 @@ __device__ __forceinline__ int cta256_exclusive_scan(int v, int32_t* wsum, int* 
 
 __global__ void __launch_bounds__(256) k_beam_items(const __grid_constant__ StepLaunch a) {
   __shared__ int32_t wsum[8];
+  pdl_wait();
+  pdl_trigger();
   const int N = a.B * a.Wc;
   const int bper = item_block_beams(N);
   int32_t* loc = a.bscan;  // first item of each beam, counted from its CTA's first
@@ -157,6 +185,8 @@ __global__ void __launch_bounds__(256) k_selective(const __grid_constant__ StepL
   const int32_t* rp = loc + N;
   const int32_t* fo = rp + N;
   const int32_t* bsum = fo + N;
+  pdl_wait();
+  pdl_trigger();
   {
     constexpr int PT = kItemBlocks / 256;  // CTA totals per thread
     int v[PT], sum = 0;
@@ -197,6 +227,7 @@ __global__ void __launch_bounds__(256) k_selective(const __grid_constant__ StepL
   }
   int b = lo, loaded = -1, ob = off(lo), onext = off(lo + 1);
   BeamState bs;
+  float h[VPL][Vec<WT>::E];
   for (int it = i0; it < i1; ++it) {
     while (onext <= it) {
       ++b;
@@ -204,11 +235,17 @@ __global__ void __launch_bounds__(256) k_selective(const __grid_constant__ StepL
       onext = off(b + 1);
     }
     const int q = b / a.Wc, k = b - q * a.Wc;
-    if (b != loaded) {  // consecutive chunks of one beam share its state
-      bs = load_beam(a, q, k);
+    const int c = it - ob;
+    const bool fresh = (b != loaded);  // consecutive chunks of one beam share its state and hidden vector
+    if (fresh) bs = load_beam(a, q, k);
+    int t_lane;
+    const uint32_t vmask = chunk_tokens(a, bs, (uint32_t)rp[b], (uint32_t)fo[b], c, lane, t_lane);
+    if (fresh) {
+      // chunk 0 of a beam is the first of its chunks that its warp meets: that warp stores h
+      load_hidden<WT, VPL>(a, q, k, bs, lane, (c == 0) && a.h_out, h);
       loaded = b;
     }
-    score_chunk<WT, VPL>(a, q, k, bs, (uint32_t)rp[b], (uint32_t)fo[b], it - ob, lane);
+    score_rows<WT, VPL>(a, q, k, c, lane, vmask, t_lane, h);
   }
 }
 
@@ -532,6 +569,8 @@ __global__ void __launch_bounds__(kSelThreads) k_select(const __grid_constant__ 
   __shared__ SelWorkT<kSelThreads / 32> sw;
   const int q = blockIdx.x;
   build_beam_table<kSelThreads>(a, q, bt);
+  pdl_wait();  // the step's scores and partials
+  pdl_trigger();
   const bool staged = bt.total <= kSelCap;
   int rt, tw;
   tile_layout(a.Wc, a.S, kSelCap, &rt, &tw);
@@ -663,8 +702,7 @@ cudaError_t launch_sel_t(const StepLaunch& a, cudaStream_t st) {
   const int N = a.B * a.Wc;
   if (N == 0 || a.nch == 0) return cudaSuccess;
   const int bper = item_block_beams(N);
-  k_beam_items<<<(N + bper - 1) / bper, 256, 0, st>>>(a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(k_beam_items, (unsigned)((N + bper - 1) / bper), 256, 0, st, a);
   if (e != cudaSuccess) return e;
   // persistent: as many CTAs as are resident at once (the occupancy of this
   // instantiation), each warp one contiguous range of the items; fewer when
@@ -678,8 +716,7 @@ cudaError_t launch_sel_t(const StepLaunch& a, cudaStream_t st) {
       resident = per_sm * sm_count();
     }
     const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((items + 7) / 8, (int64_t)resident));
-    kern<<<blocks, 256, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(kern, (unsigned)blocks, 256, 0, st, a);
   };
   switch (vpl_for<WT>(a.d)) {
     case 1:
@@ -811,8 +848,7 @@ cudaError_t launch_select(const StepLaunch& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  k_select<<<a.B, kSelThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k_select, (unsigned)a.B, kSelThreads, smem, st, a);
 }
 
 cudaError_t launch_trace_touch(const StepLaunch& a, unsigned long long* counters, uint32_t* mask, cudaStream_t st) {

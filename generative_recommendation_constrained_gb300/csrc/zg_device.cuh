@@ -178,19 +178,13 @@ struct SlotSink {
   int cnt;         // slots of the beam (flat candidates it owns)
 };
 
-template <typename WT, int VPL>
-__device__ __forceinline__ void score_chunk(const StepLaunch& a, int q, int k, const BeamState& bs, uint32_t rp0,
-                                            uint32_t F, int c, int lane, const SlotSink* sink = nullptr) {
-  using VT = Vec<WT>;
-  constexpr int E = VT::E;
-  const int d = a.d;
-  const int nvec = d / E;
-  const int b = q * a.Wc + k;
+// The chunk's legal tokens: the lane mask and each lane's token (index
+// column entries on a sparse step, a bitmap word on a dense one).
+__device__ __forceinline__ uint32_t chunk_tokens(const StepLaunch& a, const BeamState& bs, uint32_t rp0, uint32_t F,
+                                                 int c, int lane, int& t_lane) {
   const int j0 = c * kChunk;
-  // the chunk's legal tokens (index column entries or bitmap word) and the
-  // hidden vector below are loaded together, then checked
   uint32_t vmask;
-  int t_lane = 0;
+  t_lane = 0;
   if (a.mode == kSelDense) {
     vmask = a.tab.bitmap[(size_t)bs.row * a.tab.words + c];
     t_lane = j0 + lane;
@@ -200,46 +194,66 @@ __device__ __forceinline__ void score_chunk(const StepLaunch& a, int q, int k, c
     vmask = (nvalid >= 32) ? kFull : ((1u << nvalid) - 1u);
     if (lane < nvalid) t_lane = a.tab.col[rp0 + j0 + lane];
   }
+  return vmask;
+}
 
-  float h[VPL][E];
-  {
-    const float* hp;
-    const float* cr = nullptr;
-    if (a.hpre) {  // the light decoder's hidden vector
-      hp = a.hpre + (size_t)b * d;
-    } else if (a.s == 1) {
-      hp = a.u + (size_t)q * d;
-    } else {
-      hp = a.h_prev + ((size_t)q * a.Wp + bs.par) * d;
-      cr = a.C_prev + (size_t)bs.tok * d;
-    }
-    const bool write_h = (c == 0) && a.h_out;
+// The beam's hidden vector h_b = h_parent + C_{s-1}[token] (or the request
+// vector at step 1, or the light decoder's output), lane-sliced: lane l holds
+// elements (l + 32 r) * E .. + E.  write_h: also store it for the next step.
+template <typename WT, int VPL>
+__device__ __forceinline__ void load_hidden(const StepLaunch& a, int q, int k, const BeamState& bs, int lane,
+                                            bool write_h, float (&h)[VPL][Vec<WT>::E]) {
+  constexpr int E = Vec<WT>::E;
+  const int d = a.d;
+  const int nvec = d / E;
+  const int b = q * a.Wc + k;
+  const float* hp;
+  const float* cr = nullptr;
+  if (a.hpre) {  // the light decoder's hidden vector
+    hp = a.hpre + (size_t)b * d;
+  } else if (a.s == 1) {
+    hp = a.u + (size_t)q * d;
+  } else {
+    hp = a.h_prev + ((size_t)q * a.Wp + bs.par) * d;
+    cr = a.C_prev + (size_t)bs.tok * d;
+  }
 #pragma unroll
-    for (int r = 0; r < VPL; ++r) {
-      const int v = lane + 32 * r;
+  for (int r = 0; r < VPL; ++r) {
+    const int v = lane + 32 * r;
 #pragma unroll
-      for (int e = 0; e < E; ++e) h[r][e] = 0.f;
-      if (v < nvec) {
+    for (int e = 0; e < E; ++e) h[r][e] = 0.f;
+    if (v < nvec) {
 #pragma unroll
-        for (int e4 = 0; e4 < E; e4 += 4) {
-          float4 x = *reinterpret_cast<const float4*>(hp + v * E + e4);
-          if (cr) {
-            const float4 y = *reinterpret_cast<const float4*>(cr + v * E + e4);
-            x.x += y.x;
-            x.y += y.y;
-            x.z += y.z;
-            x.w += y.w;
-          }
-          h[r][e4] = x.x;
-          h[r][e4 + 1] = x.y;
-          h[r][e4 + 2] = x.z;
-          h[r][e4 + 3] = x.w;
-          if (write_h) *reinterpret_cast<float4*>(a.h_out + (size_t)b * d + v * E + e4) = x;
+      for (int e4 = 0; e4 < E; e4 += 4) {
+        float4 x = *reinterpret_cast<const float4*>(hp + v * E + e4);
+        if (cr) {
+          const float4 y = *reinterpret_cast<const float4*>(cr + v * E + e4);
+          x.x += y.x;
+          x.y += y.y;
+          x.z += y.z;
+          x.w += y.w;
         }
+        h[r][e4] = x.x;
+        h[r][e4 + 1] = x.y;
+        h[r][e4 + 2] = x.z;
+        h[r][e4 + 3] = x.w;
+        if (write_h) *reinterpret_cast<float4*>(a.h_out + (size_t)b * d + v * E + e4) = x;
       }
     }
   }
+}
 
+// Scoring of chunk c of beam k once its tokens (vmask, t_lane) and hidden
+// vector h are in registers.
+template <typename WT, int VPL>
+__device__ __forceinline__ void score_rows(const StepLaunch& a, int q, int k, int c, int lane, uint32_t vmask,
+                                           int t_lane, const float (&h)[VPL][Vec<WT>::E],
+                                           const SlotSink* sink = nullptr) {
+  using VT = Vec<WT>;
+  constexpr int E = VT::E;
+  const int d = a.d;
+  const int nvec = d / E;
+  const int j0 = c * kChunk;
   if (((vmask >> lane) & 1u) && t_lane >= a.V) {
     flag(a.status, kStatusToken);
     vmask &= ~(1u << lane);
@@ -305,6 +319,17 @@ __device__ __forceinline__ void score_chunk(const StepLaunch& a, int q, int k, c
     }
     if (!sink || !sink->z) a.part[(size_t)q * a.pq + (size_t)k * a.nch + c] = pc;
   }
+}
+
+template <typename WT, int VPL>
+__device__ __forceinline__ void score_chunk(const StepLaunch& a, int q, int k, const BeamState& bs, uint32_t rp0,
+                                            uint32_t F, int c, int lane, const SlotSink* sink = nullptr) {
+  // the chunk's legal tokens and the hidden vector are loaded together, then checked
+  int t_lane;
+  const uint32_t vmask = chunk_tokens(a, bs, rp0, F, c, lane, t_lane);
+  float h[VPL][Vec<WT>::E];
+  load_hidden<WT, VPL>(a, q, k, bs, lane, (c == 0) && a.h_out, h);
+  score_rows<WT, VPL>(a, q, k, c, lane, vmask, t_lane, h, sink);
 }
 
 // ---------------------------------------------------------------------------
