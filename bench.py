@@ -460,6 +460,9 @@ def run_gpu(args, cfg):
         if st["variant"] == 0:
             kern.append((avg["ms_project"], [s], "k_selective", step_bytes(st, cfg, s), "hbm",
                          step_unique_bytes(st, cfg, s)))
+            # the chunk counting: per live beam its state (16 B) and index row bounds (8 B)
+            # read, its chunk count, first entry and fan-out (12 B) written
+            kern.append((avg["ms_gather"], [s], "k_beam_items", st["live_beams"] * 36, "hbm", None))
         else:
             name = "k_full_simt" if cfg.w_dtype == "f32" else "k_full_tc"
             kern.append((avg["ms_project"], [s], name, full_flops(st, cfg, s),
@@ -492,6 +495,9 @@ def run_gpu(args, cfg):
         roof = {"bound": "alu", "achieved": alg / (top_ms * 1e-3) / 1e12,
                 "peak": 152 * 128 * 2 * sm_mhz * 1e6 / 1e12, "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
+    if bound == "hbm" and top_name in ("k_selective", "k_decode_cluster"):
+        roof["note"] = ("per-(beam, slot) bytes, weight rows counted at every gather; the step's codebook "
+                        "is held in L2 (evict_last), so most are L2 hits: traffic is the DRAM bytes per launch")
     roof["traffic"] = ncu_traffic(top_name, cfg.name)
     roof["kernel"] = f"{top_name} (steps {top_steps[0]}-{top_steps[-1]})"
     roof["ms_per_launch"] = top_ms

@@ -402,8 +402,7 @@ zg_status run_step(const Run& r, int s, int variant, cudaStream_t st, const Step
     e = launch_naive_dot(a, off, list, temp, H, (int64_t)r.m.naive_rows, st);
     if (e != cudaSuccess) return cuda_fail(e, "naive scoring launch");
   } else if (a.mode == kSelSparse || a.mode == kSelDense) {
-    if (tm) cudaEventRecord(tm->ev[1], st);
-    e = launch_selective(a, st);
+    e = launch_selective(a, st, tm ? tm->ev[1] : nullptr);
     if (e != cudaSuccess) return cuda_fail(e, "selective projection launch");
   } else {
     const float* H = a.hpre ? a.hpre : r.u;
@@ -1035,8 +1034,9 @@ zg_status zg_decode_trace(const zg_index* idx, const zg_plan* plan, const zg_mod
   }
   // pass 1: zg_decode's own launch sequence
   const int s0 = fused_from(r, plan);
+  if ((e = launch_delay(50000ull, s)) != cudaSuccess) st = cuda_fail(e, "zg_decode_trace: delay launch");
   cudaEventRecord(ev[kEv - 2], s);
-  st = decode_steps(r, plan, s, s0 <= r.m.L ? &ev[kEv - 4] : nullptr);
+  if (st == ZG_OK) st = decode_steps(r, plan, s, s0 <= r.m.L ? &ev[kEv - 4] : nullptr);
   cudaEventRecord(ev[kEv - 1], s);
   if (st == ZG_OK && (e = cudaEventSynchronize(ev[kEv - 1])) != cudaSuccess) st = cuda_fail(e, "zg_decode_trace");
   if (st != ZG_OK) {
@@ -1058,6 +1058,11 @@ zg_status zg_decode_trace(const zg_index* idx, const zg_plan* plan, const zg_mod
     StepTimer tm;
     for (int j = 0; j < 4; ++j) tm.ev[j] = ev[4 * (step - 1) + j];
     cudaEvent_t* mev = &ev[4 * ZG_MAX_STEPS + 2 * (step - 1)];
+    // the step's launches are enqueued behind a delay, so the events time kernels, not launch gaps
+    if ((e = launch_delay(50000ull, s)) != cudaSuccess) {
+      st = cuda_fail(e, "zg_decode_trace: delay launch");
+      break;
+    }
     if (r.m.deco) {
       cudaEventRecord(mev[0], s);
       if ((st = run_deco_step(r, step, s)) != ZG_OK) break;
@@ -1090,7 +1095,7 @@ zg_status zg_decode_trace(const zg_index* idx, const zg_plan* plan, const zg_mod
     cudaEventElapsedTime(&g, tm.ev[0], tm.ev[1]);
     cudaEventElapsedTime(&pj, tm.ev[1], tm.ev[2]);
     cudaEventElapsedTime(&q, tm.ev[2], tm.ev[3]);
-    t.ms_gather = (v == ZG_NAIVE || (v == ZG_FULL && (step >= 2 || r.m.w_dtype != ZG_F32))) ? g : 0.f;
+    t.ms_gather = (v == ZG_NAIVE || v == ZG_SELECTIVE || (v == ZG_FULL && (step >= 2 || r.m.w_dtype != ZG_F32))) ? g : 0.f;
     t.ms_project = pj;
     t.ms_select = q;
     if (r.m.deco) cudaEventElapsedTime(&t.ms_model, mev[0], mev[1]);

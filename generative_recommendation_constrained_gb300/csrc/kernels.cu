@@ -698,12 +698,13 @@ int vpl_for(int d) {
 }
 
 template <typename WT>
-cudaError_t launch_sel_t(const StepLaunch& a, cudaStream_t st) {
+cudaError_t launch_sel_t(const StepLaunch& a, cudaStream_t st, cudaEvent_t after_count) {
   const int N = a.B * a.Wc;
   if (N == 0 || a.nch == 0) return cudaSuccess;
   const int bper = item_block_beams(N);
   cudaError_t e = launch_pdl(k_beam_items, (unsigned)((N + bper - 1) / bper), 256, 0, st, a);
   if (e != cudaSuccess) return e;
+  if (after_count) cudaEventRecord(after_count, st);
   // persistent: as many CTAs as are resident at once (the occupancy of this
   // instantiation), each warp one contiguous range of the items; fewer when
   // there cannot be that many items
@@ -779,15 +780,32 @@ int sm_count() {
   return n;
 }
 
-cudaError_t launch_selective(const StepLaunch& a, cudaStream_t st) {
+cudaError_t launch_selective(const StepLaunch& a, cudaStream_t st, cudaEvent_t after_count) {
   switch (a.w_dtype) {
     case ZG_F32:
-      return launch_sel_t<float>(a, st);
+      return launch_sel_t<float>(a, st, after_count);
     case ZG_BF16:
-      return launch_sel_t<__nv_bfloat16>(a, st);
+      return launch_sel_t<__nv_bfloat16>(a, st, after_count);
     default:
-      return launch_sel_t<__half>(a, st);
+      return launch_sel_t<__half>(a, st, after_count);
   }
+}
+
+namespace {
+__global__ void k_delay(unsigned long long ns) {
+  unsigned long long t0, t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  for (int i = 0; i < (1 << 20); ++i) {  // 2^20 sleeps of at least 1 us: the bound, if the timer stalls
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if (t - t0 >= ns) break;
+    __nanosleep(1000);
+  }
+}
+}  // namespace
+
+cudaError_t launch_delay(unsigned long long ns, cudaStream_t st) {
+  k_delay<<<1, 1, 0, st>>>(ns);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_decode_cluster(const StepLaunch* steps, int s0, int L, int G, const PrefetchRegion* pf, int npf,

@@ -141,7 +141,11 @@ __device__ __forceinline__ uint32_t epi_legal_mask(const FullEpi& e, int m, int 
 #endif
 
 // kernels (kernels.cu)
-cudaError_t launch_selective(const StepLaunch& a, cudaStream_t st);
+// after_count (optional): an event recorded between the chunk-counting and the scoring kernel
+cudaError_t launch_selective(const StepLaunch& a, cudaStream_t st, cudaEvent_t after_count = nullptr);
+// a one-thread kernel that returns once `ns` nanoseconds of the GPU's global timer have passed
+// (at most about a second), so that the host can enqueue the launches behind it
+cudaError_t launch_delay(unsigned long long ns, cudaStream_t st);
 cudaError_t launch_gather_add(const StepLaunch& a, float* H, cudaStream_t st);
 cudaError_t launch_full_simt(const StepLaunch& a, const float* H, const FullEpi& epi, cudaStream_t st);
 cudaError_t launch_select(const StepLaunch& a, cudaStream_t st);

@@ -337,7 +337,8 @@ typedef struct {
   int64_t unique_tokens;  /* distinct legal tokens = distinct W_s rows touched     */
   int64_t index_bytes;    /* table bytes the filter reads: rowptr pairs plus column
                              entries (sparse) or bitmap rows (dense)               */
-  float ms_gather;        /* gather-add kernel (full steps at s >= 2), else 0       */
+  float ms_gather;        /* gather-add kernel (full steps at s >= 2) or the       */
+                          /* selective step's chunk-counting kernel, else 0        */
   float ms_project;       /* selective or full projection kernel                   */
   float ms_select;        /* masked log-softmax + cumulative add + top-K kernel     */
   float ms_model;         /* the light decoder's kernels of this step (0 without)   */
@@ -357,7 +358,10 @@ typedef struct {
  * launch sequence (ms_fused, ms_total), then the stand-alone step kernels
  * step by step (ms_gather/ms_project/ms_select) with an untimed counting
  * kernel after each step that fills the work counts (the observability the
- * per-step variant choice of [Speed] rests on).  Both passes give the same
+ * per-step variant choice of [Speed] rests on).  Each step of the second
+ * pass is queued behind a 50 us device-side delay so that its launches are
+ * all enqueued before it starts: the events time the kernels, not the
+ * host's launch gaps.  Both passes give the same
  * results; the outputs hold the second pass's.  Synchronous; not for CUDA
  * graph capture.  The workspace is the one sized by zg_decode_workspace_size. */
 ZG_API zg_status zg_decode_trace(const zg_index* idx, const zg_plan* plan, const zg_model* model,
