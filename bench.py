@@ -168,8 +168,25 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:12]
 
 
-def ncu_traffic(kernel: str, cfg_name: str):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+def launches_per_decode(variants, s0: int, L: int, w_dtype: str) -> int:
+    """Kernels one decode launches: a stand-alone selective step three (chunk
+    counting, scoring, select); a full step its gather-add (steps >= 2), the
+    hidden split (half-precision weights), the projection and the select; a
+    naive step its gather-add (steps >= 2), four compaction kernels, the dot
+    products and the select; the fused steps from s0 on one launch."""
+    n = 0
+    for s, v in enumerate(variants[:s0 - 1]):
+        if v == 0:
+            n += 3
+        elif v == 1:
+            n += (1 if s >= 1 else 0) + (1 if w_dtype != "f32" else 0) + 2
+        else:
+            n += (1 if s >= 1 else 0) + 6
+    return n + (1 if s0 <= L else 0)
+
+
+def ncu_entry(kernel: str, cfg_name: str):
+    """The committed ncu summary of a kernel on a workload, if it was taken on
     the current kernel sources (else None)."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
@@ -181,7 +198,13 @@ def ncu_traffic(kernel: str, cfg_name: str):
     ent = d.get(f"{cfg_name}:{kernel}")
     if not ent or ent.get("source_hash") != kernel_source_hash():
         return None
-    return ent.get("dram_bytes_per_launch")
+    return ent
+
+
+def ncu_traffic(kernel: str, cfg_name: str):
+    """DRAM bytes per launch from a committed ncu summary (None when absent or stale)."""
+    ent = ncu_entry(kernel, cfg_name)
+    return ent.get("dram_bytes_per_launch") if ent else None
 
 
 def load_peaks() -> dict:
@@ -281,8 +304,10 @@ def oracle_rates(cfg, sids, model, u, budget_s: float) -> dict:
 def run_reference(args, cfg):
     """The oracle (this method exists only as web pages of text; there is no
     installable reference implementation) timed as it stands on every host
-    core: each step decodes one request per core (the requests of the batch
-    in turn), in a pool of forked worker processes, one a core."""
+    core: each step decodes four requests per core (the requests of the batch
+    in turn, at most the batch), handed one at a time to whichever of the
+    forked worker processes (one a core) is free, so that the step measures
+    the oracle's throughput rather than its slowest request."""
     import multiprocessing as mp
     rank, world, _ = dist_env()
     if rank != 0:
@@ -293,15 +318,14 @@ def run_reference(args, cfg):
     t_trie = oracle_setup(cfg, sids, model, u)
     _oracle_batch([0])  # warms the trie's first-step lookups once; the forked workers inherit them
     cores = os.cpu_count() or 1
-    per_step = max(1, min(cfg.batch, args.ref_requests or cores))
+    per_step = max(1, min(cfg.batch, args.ref_requests or 4 * cores))
     times = []
     with mp.get_context("fork").Pool(cores) as pool:
         def step(i):
             lo = (i * per_step) % cfg.batch
             sel = (np.arange(lo, lo + per_step) % cfg.batch).tolist()
-            chunks = [sel[w::cores] for w in range(cores) if sel[w::cores]]
             t0 = time.perf_counter()
-            pool.map(_oracle_batch, chunks)
+            pool.map(_oracle_batch, [[q] for q in sel], chunksize=1)
             return time.perf_counter() - t0
         for i in range(args.warmup):
             step(i)
@@ -499,6 +523,10 @@ def run_gpu(args, cfg):
         roof["note"] = ("per-(beam, slot) bytes, weight rows counted at every gather; the step's codebook "
                         "is held in L2 (evict_last), so most are L2 hits: traffic is the DRAM bytes per launch")
     roof["traffic"] = ncu_traffic(top_name, cfg.name)
+    ent = ncu_entry(top_name, cfg.name)
+    if ent and ent.get("lts_throughput_pct") is not None:
+        # the same launch's L2 throughput as a fraction of L2 peak (ncu, cold L2)
+        roof["l2_throughput_frac_ncu"] = ent["lts_throughput_pct"] / 100.0
     roof["kernel"] = f"{top_name} (steps {top_steps[0]}-{top_steps[-1]})"
     roof["ms_per_launch"] = top_ms
     roof["algorithmic"] = alg
@@ -529,8 +557,7 @@ def run_gpu(args, cfg):
     if cfg.name == "large" and not args.no_sweep:
         sweep = batch_sweep(zg, idx, dm, cfg, u, warm_u, flush, capture, timed, Decoder, dev, stream, world)
 
-    launches_per_step = sum(2 if v == 0 else (2 if s == 0 else 3) for s, v in enumerate(variants[:s0 - 1]))
-    launches_per_step += 1 if s0 <= L else 0
+    launches_per_step = launches_per_decode([int(v) for v in variants], s0, L, cfg.w_dtype)
 
     if rank == 0:
         line = {
@@ -799,7 +826,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true", help="skip the large catalogue's batch sweep")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--ref-requests", type=int, default=0, help="requests a reference-arm step (0: one per core)")
+    ap.add_argument("--ref-requests", type=int, default=0, help="requests a reference-arm step (0: four per core, at most the batch)")
     ap.add_argument("--quick", action="store_true",
                     help="tune, capture and replay only (a short command for profilers)")
     ap.add_argument("--plan", default="", help="fixed per-step variants instead of tuning, e.g. sss or fss")

@@ -44,6 +44,19 @@ def test_full_flops():
     assert b.full_flops({}, cfg, 1) == 2 * cfg.batch * cfg.V * cfg.d
 
 
+def test_launches_per_decode():
+    """Kernel launches of one decode, counted from the plan as the engine issues them."""
+    b = _bench()
+    # large catalogue plan: step 1 full (hidden split, tensor cores, select), steps 2-4 stand-alone selective
+    assert b.launches_per_decode([1, 0, 0, 0], 5, 4, "bf16") == 3 + 3 * 3
+    # every step in the fused cluster kernel: one launch
+    assert b.launches_per_decode([0, 0, 0], 1, 3, "f32") == 1
+    # two full steps (the second with its gather-add), then the fused rest
+    assert b.launches_per_decode([1, 1, 0, 0], 3, 4, "f16") == 3 + 4 + 1
+    # fp32 weights: no hidden split
+    assert b.launches_per_decode([1, 0], 3, 2, "f32") == 2 + 3
+
+
 def test_reference_arm_line():
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "tiny",
                           "--steps", "2", "--warmup", "1"], capture_output=True, text=True, timeout=600, cwd=ROOT)
