@@ -75,27 +75,44 @@ __global__ void __launch_bounds__(256) k_rms_rows(const float* __restrict__ X, f
 __global__ void __launch_bounds__(256) k_gemm_xwt(const float* __restrict__ A, const float* __restrict__ W,
                                                   float* __restrict__ Cm, int R, int N, int K, int accumulate,
                                                   int relu) {
-  constexpr int BM = 64, BN = 64, BK = 16;
+  // 64 x 64 output tile, 4 x 4 a thread; K in tiles of 32 staged transposed in
+  // shared memory, the next tile's loads in flight (registers) while the
+  // current one is multiplied.  K is a multiple of 4 (rows 16-byte aligned).
+  constexpr int BM = 64, BN = 64, BK = 32;
   __shared__ float As[BK][BM + 4];
   __shared__ float Bs[BK][BN + 4];
   const int tid = threadIdx.x;
   const int tx = tid & 15, ty = tid >> 4;
   const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+  const int lr = tid >> 3, kq = (tid & 7) * 4;  // staging: rows lr and lr + 32, columns kq..kq+3
+  float4 x[2], y[2];
+  auto load = [&](int k0) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int r = lr + 32 * h;
+      x[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+      y[h] = x[h];
+      if (m0 + r < R && k0 + kq < K) x[h] = *reinterpret_cast<const float4*>(A + (size_t)(m0 + r) * K + k0 + kq);
+      if (n0 + r < N && k0 + kq < K) y[h] = *reinterpret_cast<const float4*>(W + (size_t)(n0 + r) * K + k0 + kq);
+    }
+  };
   float acc[4][4] = {};
+  load(0);
   for (int k0 = 0; k0 < K; k0 += BK) {
-    const int r = tid >> 2, kq = (tid & 3) * 4;
-    float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
-    if (m0 + r < R && k0 + kq < K) x = *reinterpret_cast<const float4*>(A + (size_t)(m0 + r) * K + k0 + kq);
-    if (n0 + r < N && k0 + kq < K) y = *reinterpret_cast<const float4*>(W + (size_t)(n0 + r) * K + k0 + kq);
-    As[kq][r] = x.x;
-    As[kq + 1][r] = x.y;
-    As[kq + 2][r] = x.z;
-    As[kq + 3][r] = x.w;
-    Bs[kq][r] = y.x;
-    Bs[kq + 1][r] = y.y;
-    Bs[kq + 2][r] = y.z;
-    Bs[kq + 3][r] = y.w;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int r = lr + 32 * h;
+      As[kq][r] = x[h].x;
+      As[kq + 1][r] = x[h].y;
+      As[kq + 2][r] = x[h].z;
+      As[kq + 3][r] = x[h].w;
+      Bs[kq][r] = y[h].x;
+      Bs[kq + 1][r] = y[h].y;
+      Bs[kq + 2][r] = y[h].z;
+      Bs[kq + 3][r] = y[h].w;
+    }
     __syncthreads();
+    if (k0 + BK < K) load(k0 + BK);
 #pragma unroll
     for (int kk = 0; kk < BK; ++kk) {
       const float4 av = *reinterpret_cast<const float4*>(&As[kk][ty * 4]);
