@@ -527,6 +527,8 @@ def run_gpu(args, cfg):
     if ent and ent.get("lts_throughput_pct") is not None:
         # the same launch's L2 throughput as a fraction of L2 peak (ncu, cold L2)
         roof["l2_throughput_frac_ncu"] = ent["lts_throughput_pct"] / 100.0
+    if ent and ent.get("lts_bytes") is not None:
+        roof["l2_bytes"] = ent["lts_bytes"]  # lts__t_bytes of the launch: next to the DRAM traffic
     roof["kernel"] = f"{top_name} (steps {top_steps[0]}-{top_steps[-1]})"
     roof["ms_per_launch"] = top_ms
     roof["algorithmic"] = alg
